@@ -1,0 +1,109 @@
+"""Seeded synthetic inputs for the GEMM workloads.
+
+This module holds the workload table and the random draws only -- no GEMM
+arithmetic -- so that both the GPU path's tests/benchmark and the CPU oracle can
+take their inputs from it.
+
+Recipe: a CPU ``torch.Generator`` seeded with the workload's seed draws A (M x K)
+first, then B in its *stored* shape (K x N for NN, N x K for TN), in fp32; the
+values are scaled and rounded to fp16/bf16 by torch's round-to-nearest-even cast.
+Distributions: ``uniform`` = U[-1, 1) (``rand*2-1``), ``normal`` = N(0, 1)
+(``randn``), ``int`` = integers uniform in {-2..2} (``randint(-2, 3)``).
+A leading dimension larger than the row length pads each row with NaN, so a
+kernel that reads past the logical edge poisons its own result.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, replace
+
+import torch
+
+TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    M: int
+    N: int
+    K: int
+    layout: str      # "NN": B stored K x N; "TN": B stored N x K
+    dtype: str       # "f16" | "bf16" (inputs and output)
+    dist: str        # "uniform" | "normal" | "int" | "ones"
+    scale: float     # multiplies the draw (1/sqrt(K) for the normalised workloads)
+    seed: int
+
+    @property
+    def flops(self) -> int:
+        return 2 * self.M * self.N * self.K
+
+    @property
+    def algorithmic_bytes(self) -> int:
+        """Read A and B once, write C once (16-bit elements)."""
+        return 2 * (self.M * self.K + self.K * self.N + self.M * self.N)
+
+    def with_dist(self, dist: str, scale: float = 1.0) -> "Workload":
+        return replace(self, dist=dist, scale=scale)
+
+
+WORKLOADS = {
+    "c1": Workload("fp16 NN 128x256x192 (the page's worked example)", 128, 256, 192, "NN", "f16", "uniform", 1.0, 0),
+    "c2": Workload("ragged fp16 TN 1000^3", 1000, 1000, 1000, "TN", "f16", "normal", 1.0, 1),
+    "c3": Workload("square fp16 NN 4096^3", 4096, 4096, 4096, "NN", "f16", "normal", 1.0 / math.sqrt(4096), 2),
+    "c4": Workload("square bf16 TN 8192^3", 8192, 8192, 8192, "TN", "bf16", "normal", 1.0 / math.sqrt(8192), 3),
+    "c5": Workload("tall-skinny fp16 TN 16384x1024x8192", 16384, 1024, 8192, "TN", "f16", "uniform",
+                   1.0 / math.sqrt(8192), 4),
+}
+
+
+def stored_b_shape(M: int, N: int, K: int, layout: str):
+    return (K, N) if layout == "NN" else (N, K)
+
+
+def _draw(gen: torch.Generator, shape, dist: str) -> torch.Tensor:
+    if dist == "uniform":
+        return torch.rand(shape, generator=gen, dtype=torch.float32) * 2 - 1
+    if dist == "normal":
+        return torch.randn(shape, generator=gen, dtype=torch.float32)
+    if dist == "int":
+        return torch.randint(-2, 3, shape, generator=gen).to(torch.float32)
+    if dist == "ones":
+        return torch.ones(shape, dtype=torch.float32)
+    raise ValueError(f"unknown distribution {dist!r}")
+
+
+def _padded(x: torch.Tensor, ld: int | None) -> torch.Tensor:
+    rows, cols = x.shape
+    if ld is None or ld == cols:
+        return x.contiguous()
+    if ld < cols:
+        raise ValueError(f"leading dimension {ld} < row length {cols}")
+    buf = torch.full((rows, ld), float("nan"), dtype=x.dtype)
+    buf[:, :cols] = x
+    return buf[:, :cols]
+
+
+def make_inputs(M: int, N: int, K: int, layout: str, dtype: str, dist: str, seed: int,
+                scale: float = 1.0, lda: int | None = None, ldb: int | None = None):
+    """(A, B) as CPU tensors of the storage dtype; A is M x K, B its stored shape.
+
+    With ``lda``/``ldb`` the tensors are views into NaN-padded row-major buffers.
+    """
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(int(seed))
+    tdt = TORCH_DTYPES[dtype]
+    a = _draw(gen, (M, K), dist)
+    b = _draw(gen, stored_b_shape(M, N, K, layout), dist)
+    if scale != 1.0:
+        a = a * scale
+        b = b * scale
+    return _padded(a.to(tdt), lda), _padded(b.to(tdt), ldb)
+
+
+def workload_inputs(w: Workload, lda: int | None = None, ldb: int | None = None):
+    return make_inputs(w.M, w.N, w.K, w.layout, w.dtype, w.dist, w.seed, w.scale, lda, ldb)
+
+
+def round_up(x: int, m: int) -> int:
+    return -(-x // m) * m

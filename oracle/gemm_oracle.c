@@ -1,0 +1,263 @@
+/*
+ * CPU oracle for the tiled dense contraction C = A·B (fp16/bf16 in, wide accumulate,
+ * fp16/bf16 out).  TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * benchmark's CPU-baseline leg call it; the GPU library never does, and this file
+ * shares no code, header, table or helper with it.
+ *
+ * What it computes (the plain definition, no blocking, no reordering):
+ *
+ *     C[m,n] = round_out( sum_{k<K} A[m,k] * Beff[k,n] )        (sum taken in fp64)
+ *
+ *   - "NineToothed GEMM 语法入门" (NineToothed GEMM syntax primer) §2 "from the
+ *     symbolic layout to application": the accumulator starts at zero, every K block
+ *     adds its product, and the output is assigned once.  §3 "tracing one read" gives
+ *     the index identities lhs[p][r,t] = A[i*BM+r, p*BK+t], rhs[p][t,s] = B[p*BK+t, j*BN+s];
+ *     summed over all p and t they reduce to the single sum over k written above.
+ *   - same page §4: the result must contain the products over the whole K range.
+ *   - same page §5 "how tail blocks take part": reads outside M/N/K contribute zero
+ *     and writes outside M x N are suppressed, so only the real indices appear here.
+ *   - same page §6 "what float32 accumulation keeps": inputs and outputs are 16-bit,
+ *     the accumulator is wider and the value is rounded once when written back.  This
+ *     oracle accumulates in fp64 (wider than the kernel's fp32) and rounds once,
+ *     round-to-nearest-even, the IEEE default.
+ *
+ * Layouts (A is always M x K row-major with leading dimension lda):
+ *   NN: B stored K x N row-major, Beff[k,n] = B[k*ldb + n]   (the page's B is (192, 256))
+ *   TN: B stored N x K row-major, Beff[k,n] = B[n*ldb + k]   ("张量缩并：mma 语法", the
+ *       one-warp kernel takes rhs as [N, K])
+ *
+ * Codecs are written from the IEEE 754 binary16 definition (1 sign, 5 exponent bits with
+ * bias 15, 10 fraction bits) and from bfloat16 (1 sign, 8 exponent bits with bias 127,
+ * 7 fraction bits).  Widening to fp64 is exact; narrowing rounds to nearest, ties to even,
+ * overflows to +-inf and keeps subnormals.
+ *
+ * Compiled with -ffp-contract=off so that x86 and Arm builds perform the same roundings.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+enum { OR_LAYOUT_NN = 0, OR_LAYOUT_TN = 1 };
+enum { OR_F16 = 0, OR_BF16 = 1 };
+
+/* ---------------------------------------------------------------- decode */
+
+double oracle_f16_to_f64(uint16_t h)
+{
+    const int sign = (h >> 15) & 1;
+    const int e = (h >> 10) & 0x1f;
+    const int f = h & 0x3ff;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -24);              /* subnormal: f * 2^(1-15-10) */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x400), e - 25); /* (1024+f) * 2^(e-15-10) */
+    return sign ? -v : v;
+}
+
+double oracle_bf16_to_f64(uint16_t b)
+{
+    const int sign = (b >> 15) & 1;
+    const int e = (b >> 7) & 0xff;
+    const int f = b & 0x7f;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -133);             /* subnormal: f * 2^(1-127-7) */
+    else if (e == 255)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x80), e - 134); /* (128+f) * 2^(e-127-7) */
+    return sign ? -v : v;
+}
+
+/* ---------------------------------------------------------------- encode */
+
+/* Round a non-negative integer-valued-or-not double n to the nearest integer,
+ * ties to the even one.  n < 2^52 here, so floor and the difference are exact. */
+static double round_half_even(double n)
+{
+    const double fl = floor(n);
+    const double d = n - fl;
+    if (d > 0.5) return fl + 1.0;
+    if (d < 0.5) return fl;
+    return (fmod(fl, 2.0) == 0.0) ? fl : fl + 1.0;
+}
+
+/* Generic narrowing of x to a binary format with `mbits` fraction bits, minimum
+ * normal exponent `emin`, largest finite value `maxv`.  Returns the rounded value
+ * as a double (exactly representable in the target format) or +-inf. */
+static double round_to_format(double x, int mbits, int emin, double maxv)
+{
+    const double a = fabs(x);
+    if (a == 0.0 || isinf(a) || isnan(a)) return x;
+    int e2;
+    frexp(a, &e2);           /* a in [2^(e2-1), 2^e2) */
+    int E = e2 - 1;          /* binade exponent of a */
+    if (E < emin) E = emin;  /* subnormal binade shares the quantum of the smallest normal */
+    const double q = ldexp(1.0, E - mbits);   /* spacing of representable values */
+    const double r = round_half_even(a / q) * q;
+    const double v = (r > maxv) ? INFINITY : r;
+    return signbit(x) ? -v : v;
+}
+
+static uint16_t pack_format(double v, int mbits, int ebits, int emin)
+{
+    const uint16_t sign = signbit(v) ? (uint16_t)(1u << 15) : 0;
+    const int bias = (1 << (ebits - 1)) - 1;
+    const double a = fabs(v);
+    if (isnan(v)) /* quiet NaN with the top fraction bit set */
+        return (uint16_t)(((1u << ebits) - 1) << mbits | (1u << (mbits - 1)));
+    if (isinf(a)) return (uint16_t)(sign | (((1u << ebits) - 1) << mbits));
+    if (a == 0.0) return sign;
+    if (a < ldexp(1.0, emin)) { /* subnormal: a = f * 2^(emin - mbits) */
+        const double f = a / ldexp(1.0, emin - mbits);
+        return (uint16_t)(sign | (uint16_t)f);
+    }
+    int e2;
+    frexp(a, &e2);
+    const int E = e2 - 1;
+    const double frac = a / ldexp(1.0, E - mbits) - ldexp(1.0, mbits);
+    return (uint16_t)(sign | (uint16_t)((E + bias) << mbits) | (uint16_t)frac);
+}
+
+uint16_t oracle_f64_to_f16(double x)
+{
+    return pack_format(round_to_format(x, 10, -14, 65504.0), 10, 5, -14);
+}
+
+uint16_t oracle_f64_to_bf16(double x)
+{
+    /* largest finite bfloat16: (2 - 2^-7) * 2^127 */
+    return pack_format(round_to_format(x, 7, -126, ldexp(255.0, 120)), 7, 8, -126);
+}
+
+/* ---------------------------------------------------------------- GEMM */
+
+static void build_table(double* t, int dtype)
+{
+    for (uint32_t c = 0; c < 65536u; ++c)
+        t[c] = (dtype == OR_BF16) ? oracle_bf16_to_f64((uint16_t)c) : oracle_f16_to_f64((uint16_t)c);
+}
+
+/* One output row m of the fp64 accumulator: acc[n] for n < N. */
+static void row_f64(const double* T, const uint16_t* A, const uint16_t* B, int64_t m,
+                    int64_t N, int64_t K, int64_t lda, int64_t ldb, int layout, double* acc)
+{
+    const uint16_t* arow = A + m * lda;
+    if (layout == OR_LAYOUT_NN) {
+        for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const double a = T[arow[k]];
+            const uint16_t* brow = B + k * ldb;
+            for (int64_t n = 0; n < N; ++n) acc[n] += a * T[brow[n]];
+        }
+    } else {
+        for (int64_t n = 0; n < N; ++n) {
+            const uint16_t* bcol = B + n * ldb; /* column n of Beff is row n of the stored N x K array */
+            double s = 0.0;
+            for (int64_t k = 0; k < K; ++k) s += T[arow[k]] * T[bcol[k]];
+            acc[n] = s;
+        }
+    }
+}
+
+/* Rows `rows[0..nrows)` of C.  If `out16` is non-null, writes the rounded 16-bit codes
+ * (row i of the output at out16 + i*ldo); if `out64` is non-null, writes the unrounded
+ * fp64 sums (row i at out64 + i*ldo).  Returns the number of threads used. */
+int oracle_gemm_rows(const uint16_t* A, const uint16_t* B, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int layout, int dtype,
+                     const int64_t* rows, int64_t nrows,
+                     uint16_t* out16, double* out64, int64_t ldo, int nthreads)
+{
+    double* T = (double*)malloc(65536 * sizeof(double));
+    if (!T) return -1;
+    build_table(T, dtype);
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+        double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            row_f64(T, A, B, rows[i], N, K, lda, ldb, layout, acc);
+            for (int64_t n = 0; n < N; ++n) {
+                if (out64) out64[i * ldo + n] = acc[n];
+                if (out16) out16[i * ldo + n] = (dtype == OR_BF16) ? oracle_f64_to_bf16(acc[n])
+                                                                    : oracle_f64_to_f16(acc[n]);
+            }
+        }
+        free(acc);
+    }
+#else
+    (void)nthreads;
+    double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    for (int64_t i = 0; i < nrows; ++i) {
+        row_f64(T, A, B, rows[i], N, K, lda, ldb, layout, acc);
+        for (int64_t n = 0; n < N; ++n) {
+            if (out64) out64[i * ldo + n] = acc[n];
+            if (out16) out16[i * ldo + n] = (dtype == OR_BF16) ? oracle_f64_to_bf16(acc[n])
+                                                                : oracle_f64_to_f16(acc[n]);
+        }
+    }
+    free(acc);
+#endif
+    free(T);
+    return used;
+}
+
+/* Individual elements (ms[i], ns[i]) of C, for sampled checks at sizes where whole rows
+ * are too slow.  Same definition, one dot product per element. */
+int oracle_gemm_elems(const uint16_t* A, const uint16_t* B, int64_t K, int64_t lda, int64_t ldb,
+                      int layout, int dtype, const int64_t* ms, const int64_t* ns, int64_t count,
+                      uint16_t* out16, double* out64)
+{
+    double* T = (double*)malloc(65536 * sizeof(double));
+    if (!T) return -1;
+    build_table(T, dtype);
+#ifdef _OPENMP
+#pragma omp parallel for schedule(static)
+#endif
+    for (int64_t i = 0; i < count; ++i) {
+        const uint16_t* arow = A + ms[i] * lda;
+        double s = 0.0;
+        for (int64_t k = 0; k < K; ++k) {
+            const uint16_t b = (layout == OR_LAYOUT_NN) ? B[k * ldb + ns[i]] : B[ns[i] * ldb + k];
+            s += T[arow[k]] * T[b];
+        }
+        if (out64) out64[i] = s;
+        if (out16) out16[i] = (dtype == OR_BF16) ? oracle_f64_to_bf16(s) : oracle_f64_to_f16(s);
+    }
+    free(T);
+    return 0;
+}
+
+int oracle_max_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Batch forms of the codecs, for the exhaustive codec tests. */
+void oracle_decode_array(const uint16_t* in, double* out, int64_t n, int dtype)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (dtype == OR_BF16) ? oracle_bf16_to_f64(in[i]) : oracle_f16_to_f64(in[i]);
+}
+
+void oracle_encode_array(const double* in, uint16_t* out, int64_t n, int dtype)
+{
+    for (int64_t i = 0; i < n; ++i)
+        out[i] = (dtype == OR_BF16) ? oracle_f64_to_bf16(in[i]) : oracle_f64_to_f16(in[i]);
+}

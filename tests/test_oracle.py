@@ -1,0 +1,265 @@
+"""Pins for the CPU oracle, against what the pages and the mathematics fix.
+
+No GPU.  Each test checks the oracle against something other than itself: values the
+pages print (``tests/golden``), closed forms, exhaustive comparison with library casts,
+identity/permutation matrices, and an independent numpy fp64 matmul on small shapes.
+"""
+import itertools
+
+import numpy as np
+import pytest
+import torch
+
+from conftest import read_golden, read_shape_cases
+from dense_tiled_gemm_04_gb300.workloads import make_inputs
+
+import oracle
+from oracle import tiled
+
+
+def _f64(x):
+    """fp64 values of a 16-bit torch tensor (torch's widening cast; exact)."""
+    return x.to(torch.float64).numpy()
+
+
+# ------------------------------------------------------------------ codecs
+
+
+@pytest.mark.parametrize("dtype,tdt", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+def test_decode_every_code_matches_torch(dtype, tdt):
+    codes = np.arange(65536, dtype=np.uint16)
+    mine = oracle.decode(codes, dtype)
+    ref = torch.from_numpy(codes.view(np.int16)).view(tdt).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    # signed zeros keep their sign
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(ref[~nan]))
+
+
+def _sweep_values(dtype: str, tdt) -> np.ndarray:
+    """fp32-representable test points: every finite code, every midpoint between
+    neighbours (ties), midpoints +-1 fp32 ulp, random log-uniform values, overflow edges."""
+    codes = np.arange(65536, dtype=np.uint16)
+    vals = torch.from_numpy(codes.view(np.int16)).view(tdt).to(torch.float64).numpy()
+    fin = np.sort(np.unique(vals[np.isfinite(vals)]))
+    mids = (fin[:-1] + fin[1:]) / 2  # exact in fp64 and in fp32 (one extra bit)
+    mids32 = mids.astype(np.float32)
+    assert np.array_equal(mids32.astype(np.float64), mids)
+    up = np.nextafter(mids32, np.float32(np.inf)).astype(np.float64)
+    dn = np.nextafter(mids32, np.float32(-np.inf)).astype(np.float64)
+    rng = np.random.default_rng(123)
+    rnd = (rng.choice([-1.0, 1.0], 400_000) * np.exp2(rng.uniform(-140, 127.9, 400_000))).astype(np.float32)
+    big = np.array([6.5504e4, 6.5519e4, 6.552e4, 6.5536e4, 1e5, 3.3895e38, 3.39e38, 3.4e38], dtype=np.float32)
+    allv = np.concatenate([fin, mids, up, dn, rnd.astype(np.float64), big.astype(np.float64),
+                           -big.astype(np.float64), [0.0, -0.0]])
+    return allv.astype(np.float32).astype(np.float64)  # all exactly fp32
+
+
+@pytest.mark.parametrize("dtype,tdt", [("f16", torch.float16), ("bf16", torch.bfloat16)])
+def test_encode_matches_torch_rne_cast(dtype, tdt):
+    # torch's fp32 -> fp16/bf16 cast rounds to nearest even with overflow to inf: a
+    # library routine the oracle's own encoder must agree with on every fp32 input.
+    x = _sweep_values(dtype, tdt)
+    mine = oracle.encode(x, dtype)
+    ref = torch.from_numpy(x.astype(np.float32)).to(tdt).view(torch.int16).numpy().view(np.uint16)
+    bad = np.nonzero(mine != ref)[0]
+    assert bad.size == 0, f"{bad.size} mismatches, e.g. x={x[bad[:5]]} mine={mine[bad[:5]]} torch={ref[bad[:5]]}"
+
+
+def test_encode_ties_to_even_closed_form():
+    # 2049 lies halfway between the fp16 neighbours 2048 and 2050: ties go to the even code.
+    assert oracle.decode(oracle.encode([2049.0, 2051.0, 2050.0], "f16"), "f16").tolist() == [2048.0, 2052.0, 2050.0]
+    # fp16 max is 65504; 65520 is the halfway point to 65536, which overflows.
+    assert np.isinf(oracle.decode(oracle.encode([65520.0], "f16"), "f16"))[0]
+    assert oracle.decode(oracle.encode([65519.0], "f16"), "f16")[0] == 65504.0
+    # bf16 keeps 8 significant bits: 257 is a tie between 256 and 258 -> 256.
+    assert oracle.decode(oracle.encode([257.0, 259.0], "bf16"), "bf16").tolist() == [256.0, 260.0]
+
+
+# ------------------------------------------------------------------ the pages' worked example
+
+
+def _shape_str_levels(levels):
+    return [tuple(l) for l in levels]
+
+
+def test_arrangement_shapes_match_page():
+    cases = read_shape_cases("arrangement_shapes.txt")
+    assert cases, "fixture empty"
+    for (M, N, K, BM, BN, BK), expected in cases.items():
+        got = tiled.arrangement_shapes(M, N, K, BM, BN, BK)
+        for label, levels in expected.items():
+            assert _shape_str_levels(got[label]) == levels, (label, got[label], levels)
+
+
+def test_worked_example_grid_and_block_identities():
+    g = read_golden("worked_example.txt")
+    M, N, K, BM, BN, BK = g["M"], g["N"], g["K"], g["BM"], g["BN"], g["BK"]
+    TM, TN, KB = tiled.grid(M, N, K, BM, BN, BK)
+    assert (TM, TN) == g["grid"] and KB == g["k_blocks"] and TM * TN == g["programs"]
+
+    A, B = make_inputs(M, N, K, "NN", "f16", "int", seed=0)
+    A64, B64 = _f64(A), _f64(B)
+    i, j = g["program"]
+    p = g["p"]
+    # lhs[p][r,t] = A[i*BM+r, p*BK+t] and rhs[p][t,s] = B[p*BK+t, j*BN+s]
+    r0, r1 = g["a_rows"]
+    c0, c1 = g["a_cols"]
+    assert np.array_equal(tiled.lhs_block(A64, i, p, BM, BK), A64[r0:r1, c0:c1])
+    r0, r1 = g["b_rows"]
+    c0, c1 = g["b_cols"]
+    assert np.array_equal(tiled.rhs_block(B64, j, p, BK, BN), B64[r0:r1, c0:c1])
+
+    # The oracle's direct sum equals the tile-by-tile K-block sum exactly (integers).
+    codes, direct = oracle.gemm(A, B, "NN", "f16", want_f64=True)
+    blocked = tiled.tiled_gemm(A64, B64, BM, BN, BK)
+    assert np.array_equal(direct, blocked)
+    # C_tile[1,2] = sum_p A[i*BM:, p*BK:] B[p*BK:, j*BN:] covers C[64:128, 128:192]
+    cr0, cr1 = g["c_rows"]
+    cc0, cc1 = g["c_cols"]
+    tile = sum(A64[cr0:cr1, q * BK:(q + 1) * BK] @ B64[q * BK:(q + 1) * BK, cc0:cc1] for q in range(KB))
+    assert np.array_equal(direct[cr0:cr1, cc0:cc1], tile)
+    # BK = 32 (§8 exercise one): 6 K blocks, same result
+    assert tiled.grid(M, N, K, 64, 64, 32)[2] == 6
+    assert np.array_equal(direct, tiled.tiled_gemm(A64, B64, 64, 64, 32))
+
+
+def test_worked_example_random_inputs_blocked_vs_direct():
+    # Uniform inputs (the worked example's own distribution): fp64 sums of fp16
+    # products are exact here, so blocking must not change a single bit.
+    A, B = make_inputs(128, 256, 192, "NN", "f16", "uniform", seed=0)
+    codes, direct = oracle.gemm(A, B, "NN", "f16", want_f64=True)
+    blocked = tiled.tiled_gemm(_f64(A), _f64(B), 64, 64, 64)
+    np.testing.assert_allclose(direct, blocked, rtol=0, atol=1e-12)
+    assert np.array_equal(codes, oracle.encode(direct, "f16"))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_tail_all_ones_is_130(layout):
+    g = read_golden("tail_allones.txt")
+    M, N, K, BM, BN, BK = g["M"], g["N"], g["K"], g["BM"], g["BN"], g["BK"]
+    TM, TN, KB = tiled.grid(M, N, K, BM, BN, BK)
+    assert (TM, TN) == g["grid"] and KB == g["k_blocks"]
+    rows, cols, kv = tiled.tail_valid_counts(M, N, K, BM, BN, BK)
+    assert (rows, cols) == g["corner_valid"] and kv == g["last_k_valid"]
+
+    A, B = make_inputs(M, N, K, layout, "f16", "ones", seed=0)
+    C = oracle.decode(oracle.gemm(A, B, layout, "f16"), "f16")
+    assert C.shape == (M, N) and np.all(C == g["allones_value"])
+    # The mistake the page's exercise is built to catch: a K loop one block short.
+    Bl = _f64(B) if layout == "NN" else _f64(B).T
+    short = tiled.tiled_gemm(_f64(A), Bl, BM, BN, BK, drop_last_k_block=True)
+    assert np.all(short == g["allones_value_without_last_k_tile"])
+    assert np.all(tiled.tiled_gemm(_f64(A), Bl, BM, BN, BK) == g["allones_value"])
+
+
+def test_fp32_accumulation_example():
+    g = read_golden("fp32_accumulation.txt")
+    a = np.array([g["a_row"]], dtype=np.float32)
+    b = np.array([g["b_col"]], dtype=np.float32).T
+    A = torch.from_numpy(a).to(torch.float16)
+    B = torch.from_numpy(b).to(torch.float16)
+    C = oracle.decode(oracle.gemm(A, B, "NN", "f16"), "f16")
+    assert C[0, 0] == g["fp16_output"] == g["fp32_accumulate"]
+    # The same sum rounded back to fp16 after every add stays at 2048.
+    acc = 0.0
+    for x, y in zip(g["a_row"], g["b_col"]):
+        acc = float(oracle.decode(oracle.encode([acc + x * y], "f16"), "f16")[0])
+    assert acc == g["fp16_accumulate"]
+
+
+# ------------------------------------------------------------------ closed forms
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_identity_and_permutation(layout, dtype):
+    M, K = 37, 29
+    A, _ = make_inputs(M, K, K, layout, dtype, "uniform", seed=5)
+    tdt = A.dtype
+    eye = torch.eye(K, dtype=tdt)
+    assert np.array_equal(oracle.gemm(A, eye, layout, dtype), oracle._codes(A))
+    perm = torch.randperm(K, generator=torch.Generator().manual_seed(9))
+    P = torch.zeros(K, K, dtype=tdt)
+    P[perm, torch.arange(K)] = 1  # Beff = P: (A P)[:, j] = A[:, perm[j]]
+    Bstored = P if layout == "NN" else P.T.contiguous()
+    got = oracle.gemm(A, Bstored, layout, dtype)
+    assert np.array_equal(got, oracle._codes(A)[:, perm.numpy()])
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_tn_equals_nn_of_transposed_b(dtype):
+    A, B = make_inputs(23, 41, 19, "NN", dtype, "normal", seed=11)
+    nn = oracle.gemm(A, B, "NN", dtype)
+    tn = oracle.gemm(A, B.T.contiguous(), "TN", dtype)
+    assert np.array_equal(nn, tn)
+
+
+SIZES = [1, 2, 3, 5, 8, 9, 15, 16, 17, 63, 64, 65, 127, 128, 129]
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_brute_force_against_numpy_f64(dtype):
+    """Independent numpy fp64 matmul on every (M, N, K) from a size set: equal sums
+    (within fp64 reordering) and, on integer data, identical rounded codes."""
+    rng = np.random.default_rng(7)
+    combos = list(itertools.product(SIZES, repeat=3))
+    rng.shuffle(combos)
+    for idx, (M, N, K) in enumerate(combos[:400]):
+        layout = "NN" if idx % 2 == 0 else "TN"
+        dist = "int" if idx % 3 == 0 else "normal"
+        A, B = make_inputs(M, N, K, layout, dtype, dist, seed=idx)
+        codes, f64 = oracle.gemm(A, B, layout, dtype, want_f64=True)
+        Bl = _f64(B) if layout == "NN" else _f64(B).T
+        ref = _f64(A) @ Bl
+        np.testing.assert_allclose(f64, ref, rtol=1e-13, atol=1e-13, err_msg=str((M, N, K, layout)))
+        if dist == "int":
+            assert np.array_equal(f64, ref)
+            assert np.array_equal(codes, oracle.encode(ref, dtype))
+            if dtype == "f16":  # numpy's own fp64 -> fp16 cast, a separate rounding routine
+                assert np.array_equal(codes, ref.astype(np.float16).view(np.uint16))
+
+
+def test_blocked_equals_direct_on_small_tiles():
+    """Tile-by-tile formulation with small tiles vs the direct sum, ragged in M, N, K."""
+    for (M, N, K) in [(1, 1, 1), (5, 9, 3), (9, 8, 17), (16, 15, 16), (17, 17, 9)]:
+        A, B = make_inputs(M, N, K, "NN", "f16", "int", seed=M * 100 + N + K)
+        direct = oracle.gemm(A, B, "NN", "f16", want_f64=True)[1]
+        for (BM, BN, BK) in [(4, 8, 4), (8, 4, 16), (16, 16, 8)]:
+            assert np.array_equal(direct, tiled.tiled_gemm(_f64(A), _f64(B), BM, BN, BK))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_padded_leading_dimensions(layout):
+    M, N, K = 19, 21, 13
+    A, B = make_inputs(M, N, K, layout, "f16", "normal", seed=3)
+    Ap, Bp = make_inputs(M, N, K, layout, "f16", "normal", seed=3, lda=24, ldb=32)
+    assert torch.isnan(Ap.as_strided((M, 24), (24, 1))[:, K:]).all()  # NaN padding really there
+    assert np.array_equal(oracle.gemm(A, B, layout, "f16"), oracle.gemm(Ap, Bp, layout, "f16"))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_elems_and_rows_agree_with_full(layout):
+    M, N, K = 70, 90, 50
+    A, B = make_inputs(M, N, K, layout, "bf16", "uniform", seed=21)
+    full = oracle.gemm(A, B, layout, "bf16")
+    rng = np.random.default_rng(0)
+    ms, ns = rng.integers(0, M, 200), rng.integers(0, N, 200)
+    assert np.array_equal(oracle.gemm_elems(A, B, layout, "bf16", ms, ns), full[ms, ns])
+    rows = np.array([0, 69, 33])
+    assert np.array_equal(oracle.gemm_rows(A, B, layout, "bf16", rows)[0], full[rows])
+
+
+def test_k_zero_is_the_empty_sum():
+    A = torch.zeros(4, 0, dtype=torch.float16)
+    B = torch.zeros(0, 6, dtype=torch.float16)
+    C = oracle.gemm(A, B, "NN", "f16")
+    assert C.shape == (4, 6) and np.all(C == 0)
+
+
+def test_overflow_rounds_to_inf():
+    A = torch.full((1, 4), 200.0, dtype=torch.float16)
+    B = torch.full((4, 1), 200.0, dtype=torch.float16)  # 4 * 40000 = 160000 > 65504
+    C = oracle.decode(oracle.gemm(A, B, "NN", "f16"), "f16")
+    assert np.isposinf(C[0, 0])
