@@ -1,0 +1,369 @@
+"""Benchmark: C = A·B through the library's C ABI on the square bf16 8192^3 TN GEMM.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+One step = one full GEMM (the whole hot path: TMA ring, tcgen05 MMA, epilogue) on
+inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank runs
+its own independent GEMM of the same size (weak scaling; no collective on the data
+path); the timed region is bracketed by a barrier and the maximum over ranks is kept.
+
+``--impl reference`` times the CPU oracle (fp64 triple loop) on bounded samples of the
+same workload on the host cores: the slow reference arm, not a GPU implementation.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor roofline"
+WORKLOAD = "c4"
+FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+KERNEL_SOURCES = ["dense_tiled_gemm_04_gb300/csrc/gemm_kernel.cuh", "dense_tiled_gemm_04_gb300/csrc/sm103_ptx.cuh",
+                  "dense_tiled_gemm_04_gb300/csrc/gemm_api.cu"]
+
+
+def kernel_fingerprint() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def load_traffic(workload_key: str):
+    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        d = json.load(f)
+    entry = d.get(workload_key)
+    if not entry or entry.get("kernel_sha") != kernel_fingerprint():
+        return None
+    return entry.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle sampling while the timed region runs."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index: int):
+        self.dev = device_index
+        self.proc = None
+        self.lines = []
+        self.t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (FileNotFoundError, OSError):
+            self.proc = None
+            return
+        self.t = threading.Thread(target=self._read, daemon=True)
+        self.t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def stop(self, t0: float, t1: float):
+        if not self.proc:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.t.join(timeout=2)
+        sm, mx, pw, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ts, line in self.lines:
+            if not (t0 <= ts <= t1):
+                continue
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+                pw.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[4:8]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def reduce_max(values, world, device=None):
+    """Max of per-rank floats over all ranks (identity when world == 1)."""
+    if world == 1:
+        return list(values)
+    import torch
+    import torch.distributed as dist
+
+    t = torch.tensor(values, dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return t.tolist()
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.barrier()
+
+
+# ------------------------------------------------------------------ CPU oracle timing
+
+
+def oracle_rows_sample(A, B, w, target_s: float):
+    """Time the oracle on whole rows of C: calibrate on one batch, then run ~target_s."""
+    import numpy as np
+
+    import oracle
+
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(0)
+    calib = rng.integers(0, w.M, threads)
+    t0 = time.perf_counter()
+    _, _, used = oracle.gemm_rows(A, B, w.layout, w.dtype, calib)
+    t_cal = time.perf_counter() - t0
+    batches = max(1, int(target_s / max(t_cal, 1e-3)))
+    rows = rng.integers(0, w.M, threads * batches)
+    t0 = time.perf_counter()
+    _, _, used = oracle.gemm_rows(A, B, w.layout, w.dtype, rows)
+    dt = time.perf_counter() - t0
+    flops = 2.0 * rows.size * w.N * w.K
+    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
+            "sample": f"{rows.size} random rows of C ({rows.size}x{w.N} outputs, K={w.K}), fp64 sums, "
+                      f"{dt:.1f} s on {used} threads"}
+
+
+def run_reference(args, w):
+    """The reference arm: the CPU oracle on bounded samples of the workload, per step."""
+    import numpy as np
+
+    import oracle
+    from dense_tiled_gemm_04_gb300.workloads import workload_inputs
+
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    oracle.build()
+    A, B = workload_inputs(w)
+    threads = oracle.max_threads()
+    rng = np.random.default_rng(1)
+    # Elements per step sized so warm-up + timed steps take about a minute in total.
+    probe = 64 * threads
+    t0 = time.perf_counter()
+    oracle.gemm_elems(A, B, w.layout, w.dtype, rng.integers(0, w.M, probe), rng.integers(0, w.N, probe))
+    per_elem = (time.perf_counter() - t0) / probe
+    total_steps = args.steps + args.warmup
+    elems = int(max(threads, min(1 << 20, 60.0 / max(total_steps, 1) / max(per_elem, 1e-9))))
+    samples = [(rng.integers(0, w.M, elems), rng.integers(0, w.N, elems)) for _ in range(total_steps)]
+    for i in range(args.warmup):
+        oracle.gemm_elems(A, B, w.layout, w.dtype, *samples[i])
+    t0 = time.perf_counter()
+    for i in range(args.warmup, total_steps):
+        oracle.gemm_elems(A, B, w.layout, w.dtype, *samples[i])
+    dt = time.perf_counter() - t0
+    step_s = dt / max(args.steps, 1)
+    value = 2.0 * elems * w.K / step_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic: seeded N(0,1)/sqrt(K) bf16 inputs (torch CPU generator, seed 3)",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in_dtype": w.dtype,
+                   "sample_per_step": f"{elems} random elements of C"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{elems} random elements of C per step (each a {w.K}-term fp64 dot product)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ------------------------------------------------------------------ GPU arm
+
+
+def run_ours(args, w):
+    import torch
+
+    from dense_tiled_gemm_04_gb300 import build as lib_build
+    from dense_tiled_gemm_04_gb300 import native
+    from dense_tiled_gemm_04_gb300.workloads import workload_inputs
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA device")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=dev)
+    lib_build.build()
+    g = native.Gemm(local)
+
+    A_cpu, B_cpu = workload_inputs(w)
+    A, B = A_cpu.to(dev), B_cpu.to(dev)
+    C = native.empty_output(w.M, w.N, A.dtype, dev)
+    stream = torch.cuda.current_stream(dev)
+    sp = stream.cuda_stream
+    lay, dt = native.LAYOUTS[w.layout], native.DTYPES[w.dtype]
+    args_raw = (A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, A.stride(0), B.stride(0), C.stride(0),
+                lay, dt, sp)
+    plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
+
+    def step():
+        st = g.run_raw(*args_raw)
+        if st != native.OK:
+            raise native.GemmError(st, "gemm_run")
+
+    for _ in range(max(args.warmup, 3)):
+        step()
+    torch.cuda.synchronize(dev)
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)  # let the sampler start before the timed region
+    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    barrier(world)
+    torch.cuda.synchronize(dev)
+    t_wall0 = time.perf_counter()
+    ev0.record(stream)
+    for _ in range(args.steps):
+        step()
+    ev1.record(stream)
+    torch.cuda.synchronize(dev)
+    t_wall1 = time.perf_counter()
+    barrier(world)
+    clocks = sampler.stop(t_wall0, t_wall1)
+    st = g.sync_status(stream)
+    if st != native.OK:
+        raise native.GemmError(st, "watchdog")
+    ms_total = ev0.elapsed_time(ev1)
+    ms_total = reduce_max([ms_total], world, dev)[0]
+    ms_step = ms_total / args.steps
+    flops = float(w.flops)
+    value = flops * world / (ms_step * 1e-3) / 1e12
+
+    # End to end through the public C ABI on pinned host buffers: H2D of A and B, the
+    # kernel, D2H of C, synchronised every step.
+    Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
+    Ch = torch.empty((w.M, w.N), dtype=A_cpu.dtype).pin_memory()
+    e2e_steps = max(3, min(args.steps, 20))
+    if g.run_host(Ah, Bh, Ch, w.layout, stream) != native.OK:  # sizes the device staging buffers
+        raise RuntimeError("gemm_run_host failed")
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        st = g.run_host(Ah, Bh, Ch, w.layout, stream)
+        if st != native.OK:
+            raise native.GemmError(st, "gemm_run_host")
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_s = reduce_max([e2e_s], world, dev)[0]
+    e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+           "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
+
+    peaks, peak_src = load_peaks()
+    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+                "traffic": load_traffic(WORKLOAD),
+                "peak_source": f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback",
+                "nominal_dense_peak_tflops": 2250.0, "frac_of_nominal": achieved / 2250.0,
+                "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
+    if "bf16_tflops_sustained" in peaks:
+        roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        cpu = oracle_rows_sample(A_cpu, B_cpu, w, target_s=args.cpu_seconds)
+
+    g.close()
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16",
+            "data": "synthetic: seeded N(0,1)/sqrt(K) inputs rounded to bf16 (torch CPU generator, seed 3)",
+            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
+                       "accumulate": "fp32", "out": w.dtype,
+                       "kernel": f"tcgen05 {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
+                                 f"ring, {plan['grid']} persistent CTAs",
+                       "l2": "inputs larger than L2 (A, B, C = 384 MiB > 129 MB), no flush",
+                       "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU"},
+            "roofline": roofline,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": args.steps,
+            "clocks": clocks,
+        }
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-oracle sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    from dense_tiled_gemm_04_gb300.workloads import WORKLOADS
+
+    w = WORKLOADS[WORKLOAD]
+    if args.impl == "reference":
+        return run_reference(args, w)
+    return run_ours(args, w)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

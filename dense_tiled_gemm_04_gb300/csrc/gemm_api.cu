@@ -1,0 +1,510 @@
+// Host side of the C ABI declared in include/gemm.h: argument validation, TMA
+// tensor-map encoding (cached per handle), the choice of kernel configuration and the
+// launch.  All arithmetic runs in the kernels of gemm_kernel.cuh.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <cstdint>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "gemm.h"
+#include "gemm_kernel.cuh"
+
+namespace {
+
+using dtg::KernelParams;
+
+constexpr int kGroupDefault = 16;
+constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
+constexpr int kTmapCacheMax = 64;
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool load_encode_fn()
+{
+    std::call_once(g_encode_once, [] {
+        void* fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    });
+    return g_encode != nullptr;
+}
+
+struct TmapKey {
+    const void* ptr;
+    uint64_t inner, outer, pitch_bytes;
+    uint32_t box_inner, box_outer;
+    int32_t dtype;
+    bool operator==(const TmapKey& o) const
+    {
+        return ptr == o.ptr && inner == o.inner && outer == o.outer && pitch_bytes == o.pitch_bytes &&
+               box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype;
+    }
+};
+
+struct TmapEntry {
+    TmapKey key;
+    CUtensorMap map;
+};
+
+// Which kernel instantiation a plan launches.
+struct KernelChoice {
+    int config;
+    int bn;
+    int stages;
+    const void* fn;
+    int smem;
+};
+
+}  // namespace
+
+struct gemm_handle_s {
+    int device = 0;
+    int num_sms = 0;
+    int32_t* d_err = nullptr;  // 4 ints
+    int32_t last_info[4] = {0, 0, 0, 0};
+    int64_t config = GEMM_CONFIG_AUTO;
+    int64_t timeout_ns = kTimeoutDefaultNs;
+    int64_t max_ctas = 0;
+    int64_t raster_group = kGroupDefault;
+    int64_t fault_inject = 0;
+    std::vector<TmapEntry> tmaps;
+    bool attrs_set[8] = {false, false, false, false, false, false, false, false};
+    // gemm_run_host staging
+    void* d_stage = nullptr;
+    size_t stage_bytes = 0;
+};
+
+namespace {
+
+// Keeps the caller's current device unchanged across a call made on h->device.
+struct DeviceGuard {
+    int prev = -1;
+    bool ok = false;
+    explicit DeviceGuard(int dev)
+    {
+        if (cudaGetDevice(&prev) != cudaSuccess) return;
+        ok = (prev == dev) || (cudaSetDevice(dev) == cudaSuccess);
+    }
+    ~DeviceGuard()
+    {
+        int cur = -1;
+        if (prev >= 0 && cudaGetDevice(&cur) == cudaSuccess && cur != prev) cudaSetDevice(prev);
+    }
+};
+
+// Encode (or fetch) a 2-D row-major tensor map: `inner` contiguous elements per row,
+// `outer` rows `pitch_bytes` apart, box = box_inner x box_outer, 128-byte swizzle,
+// zero fill outside the tensor.
+bool get_tmap(gemm_handle_s* h, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+              uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out)
+{
+    const TmapKey key{ptr, inner, outer, pitch_bytes, box_inner, box_outer, dtype};
+    for (const TmapEntry& e : h->tmaps)
+        if (e.key == key) {
+            *out = e.map;
+            return true;
+        }
+    if (!load_encode_fn()) return false;
+    CUtensorMap map;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const CUresult r = g_encode(&map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) return false;
+    if (static_cast<int>(h->tmaps.size()) >= kTmapCacheMax) h->tmaps.clear();
+    h->tmaps.push_back({key, map});
+    *out = map;
+    return true;
+}
+
+template <int BN, int STAGES, bool BF16, bool NN>
+KernelChoice choice_of(int config)
+{
+    return {config, BN, STAGES, reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN>),
+            dtg::Smem<BN, STAGES>::kAlloc};
+}
+
+template <int BN, int STAGES>
+KernelChoice choice_for(int config, gemm_dtype_t dtype, gemm_layout_t layout)
+{
+    const bool bf16 = dtype == GEMM_DTYPE_BF16, nn = layout == GEMM_LAYOUT_NN;
+    if (bf16) return nn ? choice_of<BN, STAGES, true, true>(config) : choice_of<BN, STAGES, true, false>(config);
+    return nn ? choice_of<BN, STAGES, false, true>(config) : choice_of<BN, STAGES, false, false>(config);
+}
+
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int pick_config(const gemm_handle_s* h, int64_t M, int64_t N)
+{
+    if (h->config == GEMM_CONFIG_128x256 || h->config == GEMM_CONFIG_128x128) return static_cast<int>(h->config);
+    // AUTO: the 128 x 256 tile unless it leaves most SMs idle, then 128 x 128.
+    const int64_t tiles256 = cdiv(M, 128) * cdiv(N, 256);
+    if (tiles256 < h->num_sms / 2) return GEMM_CONFIG_128x128;
+    return GEMM_CONFIG_128x256;
+}
+
+KernelChoice kernel_choice(int config, gemm_dtype_t dtype, gemm_layout_t layout)
+{
+    if (config == GEMM_CONFIG_128x128) return choice_for<128, 6>(config, dtype, layout);
+    return choice_for<256, 4>(config, dtype, layout);
+}
+
+void fill_plan(const gemm_handle_s* h, int64_t M, int64_t N, int64_t K, const KernelChoice& kc, gemm_plan_t* plan)
+{
+    std::memset(plan, 0, sizeof(*plan));
+    plan->config = kc.config;
+    plan->bm = dtg::kBM;
+    plan->bn = kc.bn;
+    plan->bk = dtg::kBK;
+    plan->stages = kc.stages;
+    plan->cluster = 1;
+    plan->tiles_m = cdiv(M, dtg::kBM);
+    plan->tiles_n = cdiv(N, kc.bn);
+    plan->k_blocks = cdiv(K, dtg::kBK);
+    const int64_t tiles = plan->tiles_m * plan->tiles_n;
+    int64_t grid = h->num_sms > 0 ? h->num_sms : 1;
+    if (h->max_ctas > 0 && h->max_ctas < grid) grid = h->max_ctas;
+    if (tiles < grid) grid = tiles;
+    plan->grid = grid;
+    plan->threads = dtg::kThreads;
+    plan->smem_bytes = kc.smem;
+}
+
+int attr_slot(const KernelChoice& kc, gemm_dtype_t dtype, gemm_layout_t layout)
+{
+    return (kc.config == GEMM_CONFIG_128x128 ? 4 : 0) + (dtype == GEMM_DTYPE_BF16 ? 2 : 0) +
+           (layout == GEMM_LAYOUT_NN ? 1 : 0);
+}
+
+gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype)
+{
+    if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || N == 0) return GEMM_OK;
+    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (K > 0) {
+        if (!A || !B) return GEMM_ERR_INVALID_ARG;
+        if (lda < K) return GEMM_ERR_INVALID_ARG;
+        if (ldb < (layout == GEMM_LAYOUT_NN ? N : K)) return GEMM_ERR_INVALID_ARG;
+    }
+    const int64_t lim = (int64_t(1) << 31) - 1;
+    if (M > lim || N > lim || K > lim) return GEMM_ERR_UNSUPPORTED;
+    if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ldc & 7) != 0) return GEMM_ERR_UNSUPPORTED;
+    if (K > 0) {
+        if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0)
+            return GEMM_ERR_UNSUPPORTED;
+        if ((lda & 7) != 0 || (ldb & 7) != 0) return GEMM_ERR_UNSUPPORTED;
+    }
+    return GEMM_OK;
+}
+
+gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void* C, int64_t M, int64_t N,
+                       int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout,
+                       gemm_dtype_t dtype)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    return validate_args(A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
+}
+
+gemm_status_t launch(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                     int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
+                     cudaStream_t stream)
+{
+    if (K == 0) {
+        const int64_t total = M * N;
+        int blocks = static_cast<int>(cdiv(total, 256));
+        const int cap = h->num_sms * 8;
+        if (blocks > cap) blocks = cap;
+        if (dtype == GEMM_DTYPE_BF16)
+            dtg::zero_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc);
+        else
+            dtg::zero_fill_kernel<__half><<<blocks, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc);
+        return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    const int config = pick_config(h, M, N);
+    const KernelChoice kc = kernel_choice(config, dtype, layout);
+    gemm_plan_t plan;
+    fill_plan(h, M, N, K, kc, &plan);
+
+    CUtensorMap tA, tB, tC;
+    const bool nn = layout == GEMM_LAYOUT_NN;
+    if (!get_tmap(h, A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
+    if (nn) {
+        if (!get_tmap(h, B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)) return GEMM_ERR_CUDA;
+    } else {
+        if (!get_tmap(h, B, K, N, ldb * 2, dtg::kBK, kc.bn, dtype, &tB)) return GEMM_ERR_CUDA;
+    }
+    if (!get_tmap(h, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
+
+    const int slot = attr_slot(kc, dtype, layout);
+    if (!h->attrs_set[slot]) {
+        if (cudaFuncSetAttribute(kc.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        h->attrs_set[slot] = true;
+    }
+
+    KernelParams kp;
+    kp.M = static_cast<int32_t>(M);
+    kp.N = static_cast<int32_t>(N);
+    kp.K = static_cast<int32_t>(K);
+    kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
+    kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
+    kp.num_kb = static_cast<int32_t>(plan.k_blocks);
+    kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
+    kp.group_m = static_cast<int32_t>(h->raster_group);
+    kp.fault_inject = static_cast<int32_t>(h->fault_inject);
+    kp.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
+    kp.err = h->d_err;
+
+    void* args[] = {&tA, &tB, &tC, &kp};
+    cudaLaunchConfig_t cfg;
+    std::memset(&cfg, 0, sizeof(cfg));
+    cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+    cfg.blockDim = dim3(dtg::kThreads, 1, 1);
+    cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
+    cfg.stream = stream;
+    if (cudaLaunchKernelExC(&cfg, kc.fn, args) != cudaSuccess) return GEMM_ERR_CUDA;
+    return GEMM_OK;
+}
+
+gemm_status_t read_error_word(gemm_handle_t h, cudaStream_t stream)
+{
+    int32_t info[4] = {0, 0, 0, 0};
+    if (cudaMemcpyAsync(info, h->d_err, sizeof(info), cudaMemcpyDeviceToHost, stream) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (info[0] != 0) {
+        std::memcpy(h->last_info, info, sizeof(info));
+        if (cudaMemsetAsync(h->d_err, 0, sizeof(info), stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+gemm_status_t gemm_create(gemm_handle_t* out, int device)
+{
+    if (!out) return GEMM_ERR_INVALID_ARG;
+    *out = nullptr;
+    int count = 0;
+    if (cudaGetDeviceCount(&count) != cudaSuccess) {
+        cudaGetLastError();
+        return GEMM_ERR_CUDA;
+    }
+    if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
+    DeviceGuard g(device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    gemm_handle_s* h = new (std::nothrow) gemm_handle_s();
+    if (!h) return GEMM_ERR_CUDA;
+    h->device = device;
+    h->num_sms = sms;
+    if (cudaMalloc(&h->d_err, 4 * sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->d_err, 0, 4 * sizeof(int32_t)) != cudaSuccess) {
+        if (h->d_err) cudaFree(h->d_err);
+        delete h;
+        return GEMM_ERR_CUDA;
+    }
+    *out = h;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_destroy(gemm_handle_t h)
+{
+    if (!h) return GEMM_OK;
+    gemm_status_t st = GEMM_OK;
+    {
+        DeviceGuard g(h->device);
+        if (cudaDeviceSynchronize() != cudaSuccess) st = GEMM_ERR_CUDA;
+        if (h->d_err && cudaFree(h->d_err) != cudaSuccess) st = GEMM_ERR_CUDA;
+        if (h->d_stage && cudaFree(h->d_stage) != cudaSuccess) st = GEMM_ERR_CUDA;
+    }
+    delete h;
+    return st;
+}
+
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
+                       void* stream)
+{
+    const gemm_status_t v = validate(h, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
+    if (v != GEMM_OK || M == 0 || N == 0) return v;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    return launch(h, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
+                            int64_t K, int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout,
+                            gemm_dtype_t dtype, void* stream)
+{
+    const gemm_status_t v = validate(h, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
+    if (v != GEMM_OK || M == 0 || N == 0) return v;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // Device copies are packed: ld rounded up to 8 elements (16 bytes) keeps TMA alignment.
+    auto r8 = [](int64_t x) { return (x + 7) & ~int64_t(7); };
+    auto r256 = [](size_t x) { return (x + 255) & ~size_t(255); };
+    const bool nn = layout == GEMM_LAYOUT_NN;
+    const int64_t b_rows = nn ? K : N, b_cols = nn ? N : K;
+    const int64_t dlda = r8(K > 0 ? K : 1), dldb = r8(b_cols > 0 ? b_cols : 1), dldc = r8(N);
+    const size_t bytes_a = r256(static_cast<size_t>(M) * dlda * 2);
+    const size_t bytes_b = r256(static_cast<size_t>(b_rows) * dldb * 2);
+    const size_t bytes_c = r256(static_cast<size_t>(M) * dldc * 2);
+    const size_t need = bytes_a + bytes_b + bytes_c;
+    if (need > h->stage_bytes) {
+        if (h->d_stage) {
+            if (cudaStreamSynchronize(s) != cudaSuccess || cudaFree(h->d_stage) != cudaSuccess) return GEMM_ERR_CUDA;
+            h->d_stage = nullptr;
+            h->stage_bytes = 0;
+        }
+        if (cudaMalloc(&h->d_stage, need) != cudaSuccess) {
+            h->d_stage = nullptr;
+            return GEMM_ERR_CUDA;
+        }
+        h->stage_bytes = need;
+    }
+    char* dA = static_cast<char*>(h->d_stage);
+    char* dB = dA + bytes_a;
+    char* dC = dB + bytes_b;
+    if (K > 0) {
+        if (cudaMemcpy2DAsync(dA, dlda * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, s) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMemcpy2DAsync(dB, dldb * 2, B, ldb * 2, b_cols * 2, b_rows, cudaMemcpyHostToDevice, s) !=
+            cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    const gemm_status_t st = launch(h, dA, dB, dC, M, N, K, dlda, dldb, dldc, layout, dtype, s);
+    if (st != GEMM_OK) return st;
+    if (cudaMemcpy2DAsync(C, ldc * 2, dC, dldc * 2, N * 2, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    return read_error_word(h, s);
+}
+
+gemm_status_t gemm_sync_status(gemm_handle_t h, void* stream)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    return read_error_word(h, static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_error_info(gemm_handle_t h, int32_t info[4])
+{
+    if (!h || !info) return GEMM_ERR_INVALID_ARG;
+    std::memcpy(info, h->last_info, sizeof(h->last_info));
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
+{
+    if (!h) return GEMM_ERR_INVALID_ARG;
+    switch (opt) {
+    case GEMM_OPT_CONFIG:
+        if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128)
+            return value == GEMM_CONFIG_256x256 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
+        h->config = value;
+        return GEMM_OK;
+    case GEMM_OPT_TIMEOUT_NS:
+        if (value < 1000000) return GEMM_ERR_INVALID_ARG;
+        h->timeout_ns = value;
+        return GEMM_OK;
+    case GEMM_OPT_MAX_CTAS:
+        if (value < 0) return GEMM_ERR_INVALID_ARG;
+        h->max_ctas = value;
+        return GEMM_OK;
+    case GEMM_OPT_RASTER_GROUP:
+        if (value < 1 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+        h->raster_group = value;
+        return GEMM_OK;
+    case GEMM_OPT_FAULT_INJECT:
+        if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+        h->fault_inject = value;
+        return GEMM_OK;
+    default:
+        return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value)
+{
+    if (!h || !value) return GEMM_ERR_INVALID_ARG;
+    switch (opt) {
+    case GEMM_OPT_CONFIG: *value = h->config; return GEMM_OK;
+    case GEMM_OPT_TIMEOUT_NS: *value = h->timeout_ns; return GEMM_OK;
+    case GEMM_OPT_MAX_CTAS: *value = h->max_ctas; return GEMM_OK;
+    case GEMM_OPT_RASTER_GROUP: *value = h->raster_group; return GEMM_OK;
+    case GEMM_OPT_FAULT_INJECT: *value = h->fault_inject; return GEMM_OK;
+    default: return GEMM_ERR_INVALID_ARG;
+    }
+}
+
+gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_layout_t layout,
+                              gemm_dtype_t dtype, gemm_plan_t* plan)
+{
+    if (!h || !plan || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    const KernelChoice kc = kernel_choice(pick_config(h, M, N), dtype, layout);
+    fill_plan(h, M, N, K, kc, plan);
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype)
+{
+    return validate_args(A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
+}
+
+gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t group_m, int64_t* tile_m,
+                              int64_t* tile_n)
+{
+    if (!tile_m || !tile_n || tiles_m <= 0 || tiles_n <= 0 || group_m <= 0) return GEMM_ERR_INVALID_ARG;
+    if (tile < 0 || tile >= tiles_m * tiles_n) return GEMM_ERR_INVALID_ARG;
+    dtg::tile_coord(tile, tiles_m, tiles_n, group_m, *tile_m, *tile_n);
+    return GEMM_OK;
+}
+
+const char* gemm_status_string(gemm_status_t s)
+{
+    switch (s) {
+    case GEMM_OK: return "GEMM_OK";
+    case GEMM_ERR_INVALID_ARG: return "GEMM_ERR_INVALID_ARG: invalid argument";
+    case GEMM_ERR_UNSUPPORTED: return "GEMM_ERR_UNSUPPORTED: misaligned pointer/leading dimension or size too large";
+    case GEMM_ERR_ARCH: return "GEMM_ERR_ARCH: device is not sm_103";
+    case GEMM_ERR_CUDA: return "GEMM_ERR_CUDA: CUDA call or kernel launch failed";
+    case GEMM_ERR_TIMEOUT: return "GEMM_ERR_TIMEOUT: device watchdog expired";
+    default: return "unknown gemm_status_t";
+    }
+}
+
+int32_t gemm_api_version(void) { return GEMM_API_VERSION; }
+
+}  // extern "C"

@@ -1,0 +1,225 @@
+"""ctypes binding of the C ABI in ``include/gemm.h`` (``libdtgemm.so``).
+
+Argument marshalling only: every step of C = A·B runs in the library's CUDA kernels.
+The binding never falls back to another implementation -- if the library is missing
+or the device is not an sm_103 GPU, the call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+LAYOUT_NN, LAYOUT_TN = 0, 1
+DTYPE_F16, DTYPE_BF16 = 0, 1
+LAYOUTS = {"NN": LAYOUT_NN, "TN": LAYOUT_TN}
+DTYPES = {"f16": DTYPE_F16, "bf16": DTYPE_BF16}
+TORCH_TO_DTYPE = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+
+OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
+OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT = range(5)
+CONFIG_AUTO, CONFIG_128x256, CONFIG_128x128, CONFIG_256x256 = range(4)
+
+
+class gemm_plan_t(ctypes.Structure):
+    _fields_ = [("config", ctypes.c_int32), ("bm", ctypes.c_int32), ("bn", ctypes.c_int32),
+                ("bk", ctypes.c_int32), ("stages", ctypes.c_int32), ("cluster", ctypes.c_int32),
+                ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
+                ("grid", ctypes.c_int64), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+
+
+class GemmError(RuntimeError):
+    def __init__(self, status: int, what: str = ""):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)}" if what else status_string(status))
+
+
+_lib = None
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load() -> ctypes.CDLL:
+    """Load ``libdtgemm.so``; raises if it has not been built (no silent fallback)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_build.LIB):
+        raise ImportError(f"{_build.LIB} is missing: build it with dense_tiled_gemm_04_gb300.build.build()")
+    lib = ctypes.CDLL(_build.LIB)
+    i32, i64, p = ctypes.c_int32, ctypes.c_int64, ctypes.c_void_p
+    sig = {
+        "gemm_create": ([ctypes.POINTER(p), ctypes.c_int], i32),
+        "gemm_destroy": ([p], i32),
+        "gemm_run": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
+        "gemm_run_host": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
+        "gemm_sync_status": ([p, p], i32),
+        "gemm_error_info": ([p, ctypes.POINTER(i32)], i32),
+        "gemm_set_option": ([p, i32, i64], i32),
+        "gemm_get_option": ([p, i32, ctypes.POINTER(i64)], i32),
+        "gemm_query_plan": ([p, i64, i64, i64, i32, i32, ctypes.POINTER(gemm_plan_t)], i32),
+        "gemm_check_args": ([p, p, p, i64, i64, i64, i64, i64, i64, i32, i32], i32),
+        "gemm_tile_coord": ([i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
+        "gemm_status_string": ([i32], ctypes.c_char_p),
+        "gemm_api_version": ([], i32),
+    }
+    for name, (args, res) in sig.items():
+        f = getattr(lib, name)
+        f.argtypes = args
+        f.restype = res
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().gemm_status_string(int(status)).decode()
+
+
+def check_args(A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int) -> int:
+    """gemm_check_args on raw addresses (no GPU needed)."""
+    return int(load().gemm_check_args(A or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype))
+
+
+def tile_coord(tile: int, tiles_m: int, tiles_n: int, group_m: int):
+    tm, tn = ctypes.c_int64(), ctypes.c_int64()
+    st = load().gemm_tile_coord(tile, tiles_m, tiles_n, group_m, ctypes.byref(tm), ctypes.byref(tn))
+    if st != OK:
+        raise GemmError(st, "gemm_tile_coord")
+    return tm.value, tn.value
+
+
+def _ld(t: torch.Tensor) -> int:
+    """Leading dimension of a 2-D row-major tensor (one-row tensors: the padded row length)."""
+    if t.dim() != 2:
+        raise ValueError("expected a 2-D tensor")
+    if t.size(1) > 1 and t.stride(1) != 1:
+        raise ValueError("expected unit stride along the last dimension (row-major)")
+    if t.size(0) <= 1:
+        return max(-(-t.size(1) // 8) * 8, 8)
+    return t.stride(0)
+
+
+def _stream_ptr(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return int(stream.cuda_stream) if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def empty_output(M: int, N: int, dtype: torch.dtype, device) -> torch.Tensor:
+    """An M x N output whose row pitch is a multiple of 8 elements (TMA alignment)."""
+    ldc = max(-(-N // 8) * 8, 8)
+    return torch.empty((M, ldc), dtype=dtype, device=device)[:, :N]
+
+
+class Gemm:
+    """A library handle bound to one CUDA device."""
+
+    def __init__(self, device=None):
+        lib = load()
+        if device is None:
+            device = torch.cuda.current_device()
+        self.device = torch.device("cuda", device) if isinstance(device, int) else torch.device(device)
+        h = ctypes.c_void_p()
+        st = lib.gemm_create(ctypes.byref(h), self.device.index or 0)
+        if st != OK:
+            raise GemmError(st, "gemm_create")
+        self._h = h
+        self._lib = lib
+
+    # -------------------------------------------------------------- lifecycle
+    def close(self):
+        if getattr(self, "_h", None):
+            st = self._lib.gemm_destroy(self._h)
+            self._h = None
+            if st != OK:
+                raise GemmError(st, "gemm_destroy")
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def __enter__(self):
+        return self
+
+    def __exit__(self, *exc):
+        self.close()
+
+    # -------------------------------------------------------------- options
+    def set_option(self, opt: int, value: int):
+        st = self._lib.gemm_set_option(self._h, opt, int(value))
+        if st != OK:
+            raise GemmError(st, "gemm_set_option")
+
+    def get_option(self, opt: int) -> int:
+        v = ctypes.c_int64()
+        st = self._lib.gemm_get_option(self._h, opt, ctypes.byref(v))
+        if st != OK:
+            raise GemmError(st, "gemm_get_option")
+        return v.value
+
+    def plan(self, M, N, K, layout="NN", dtype="f16") -> dict:
+        pl = gemm_plan_t()
+        st = self._lib.gemm_query_plan(self._h, M, N, K, LAYOUTS[layout], DTYPES[dtype], ctypes.byref(pl))
+        if st != OK:
+            raise GemmError(st, "gemm_query_plan")
+        return {f: getattr(pl, f) for f, _ in gemm_plan_t._fields_}
+
+    def error_info(self):
+        arr = (ctypes.c_int32 * 4)()
+        self._lib.gemm_error_info(self._h, arr)
+        return list(arr)
+
+    # -------------------------------------------------------------- compute
+    def run_raw(self, A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int, stream: int) -> int:
+        """gemm_run on raw device addresses; returns the status code."""
+        return int(self._lib.gemm_run(self._h, A or None, B or None, C or None, M, N, K, lda, ldb, ldc,
+                                      layout, dtype, stream or None))
+
+    def run(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, layout: str = "NN",
+            stream=None) -> torch.Tensor:
+        """C = A·B (NN: B is K x N) or A·B^T (TN: B is N x K) on device tensors; async on `stream`."""
+        M, K = A.shape
+        N = B.shape[1] if layout == "NN" else B.shape[0]
+        if (B.shape[0] if layout == "NN" else B.shape[1]) != K:
+            raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, layout {layout}")
+        if A.dtype != B.dtype or A.dtype not in TORCH_TO_DTYPE:
+            raise TypeError("A and B must both be float16 or both bfloat16")
+        if C is None:
+            C = empty_output(M, N, A.dtype, A.device)
+        if C.shape != (M, N) or C.dtype != A.dtype:
+            raise ValueError("C has the wrong shape or dtype")
+        st = self.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _ld(A), _ld(B), _ld(C),
+                          LAYOUTS[layout], TORCH_TO_DTYPE[A.dtype], _stream_ptr(stream))
+        if st != OK:
+            raise GemmError(st, "gemm_run")
+        return C
+
+    def run_host(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, layout: str = "NN", stream=None) -> int:
+        """gemm_run_host on CPU tensors (pin them for DMA copies); synchronous; returns the status."""
+        M, K = A.shape
+        N = C.shape[1]
+        return int(self._lib.gemm_run_host(self._h, A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K,
+                                           _ld(A), _ld(B), _ld(C), LAYOUTS[layout], TORCH_TO_DTYPE[A.dtype],
+                                           _stream_ptr(stream) or None))
+
+    def sync_status(self, stream=None) -> int:
+        return int(self._lib.gemm_sync_status(self._h, _stream_ptr(stream) or None))
+
+
+_default: dict = {}
+
+
+def matmul(A: torch.Tensor, B: torch.Tensor, layout: str = "NN", out: torch.Tensor | None = None,
+           stream=None) -> torch.Tensor:
+    """C = A·B with the library's kernel, on a per-device default handle."""
+    dev = A.device.index if A.device.index is not None else torch.cuda.current_device()
+    if dev not in _default:
+        _default[dev] = Gemm(dev)
+    return _default[dev].run(A, B, out, layout, stream)

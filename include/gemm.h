@@ -1,0 +1,164 @@
+/*
+ * gemm.h -- C ABI of the GB300 (sm_103a) tiled dense GEMM library.
+ *
+ * Operation (every entry point that computes): C = A·B with 16-bit inputs, an fp32
+ * accumulator and a 16-bit output in the input type, rounded to nearest-even once.
+ *   - "NineToothed GEMM 语法入门" (NineToothed GEMM syntax primer) §2: the accumulator
+ *     starts at zero, each K block adds dot(A tile, B tile), the output is assigned once
+ *     (so C is overwritten, alpha = 1, beta = 0); §6: fp32 accumulation, 16-bit storage.
+ *   - same page §3: output tile (i, j) covers C[i*BM:, j*BN:] and reads A[i*BM:, p*BK:] and
+ *     B[p*BK:, j*BN:] for every K block p; §5: reads past M/N/K count as zero and writes
+ *     past M x N are dropped, so any M, N, K >= 0 is accepted.
+ *   - "张量缩并：mma 语法" (Croqtile tutorial ch. 4), the one-warp kernel: the kernel
+ *     writes its output in place and takes B as [N, K] -- the TN layout below.
+ *
+ * Layouts.  Every matrix is row-major with a leading dimension (elements between rows):
+ *   A: M x K, lda >= K.
+ *   GEMM_LAYOUT_NN: B stored K x N, ldb >= N   (C = A · B)
+ *   GEMM_LAYOUT_TN: B stored N x K, ldb >= K   (C = A · Bstored^T)
+ *   C: M x N, ldc >= N.  Elements of C outside the M x N window (row padding) are never
+ *   written; elements of A/B outside their logical window are never read.
+ *
+ * Alignment (the tensor-memory-access engine needs 16-byte aligned bases and row
+ * pitches): A, B, C must be 16-byte aligned and lda, ldb, ldc multiples of 8 elements,
+ * otherwise GEMM_ERR_UNSUPPORTED.  There is no fallback path.
+ *
+ * Ownership.  The caller owns A, B, C and the stream; the handle owns a small device
+ * workspace (the watchdog's error word), a cache of tensor-map descriptors and, after
+ * the first gemm_run_host, device staging buffers.  A handle may be used from one host
+ * thread at a time.  Aliasing C with A or B is undefined.
+ *
+ * Errors.  Every entry point returns a status; nothing throws across the ABI.
+ */
+#ifndef DTG_GEMM_H
+#define DTG_GEMM_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define GEMM_API_VERSION 1
+
+typedef struct gemm_handle_s* gemm_handle_t;
+
+typedef int32_t gemm_layout_t;
+enum { GEMM_LAYOUT_NN = 0, GEMM_LAYOUT_TN = 1 };
+
+typedef int32_t gemm_dtype_t;
+enum { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1 };
+
+typedef int32_t gemm_status_t;
+enum {
+    GEMM_OK = 0,
+    GEMM_ERR_INVALID_ARG = 1, /* null handle/pointer, negative size, ld too small, bad enum   */
+    GEMM_ERR_UNSUPPORTED = 2, /* misaligned base or ld, a dimension >= 2^31                  */
+    GEMM_ERR_ARCH = 3,        /* device is not compute capability 10.3 (sm_103)               */
+    GEMM_ERR_CUDA = 4,        /* a CUDA runtime/driver call or a launch failed                 */
+    GEMM_ERR_TIMEOUT = 5      /* a device-side wait gave up (watchdog); see gemm_error_info   */
+};
+
+/* Tunables and test hooks for gemm_set_option / gemm_get_option. */
+typedef int32_t gemm_option_t;
+enum {
+    GEMM_OPT_CONFIG = 0,       /* kernel configuration: GEMM_CONFIG_* (default AUTO)          */
+    GEMM_OPT_TIMEOUT_NS = 1,   /* device watchdog limit per wait, ns (default 2e9, min 1e6)   */
+    GEMM_OPT_MAX_CTAS = 2,     /* cap on persistent CTAs (0 = one per SM); tests use it to
+                                  make each CTA walk several tiles                            */
+    GEMM_OPT_RASTER_GROUP = 3, /* output-tile raster: M tiles per group (L2 reuse), >= 1      */
+    GEMM_OPT_FAULT_INJECT = 4  /* test hook: 1 = CTA 0's producer leaves one ring stage unarmed,
+                                  so a consumer wait runs out and the watchdog path returns
+                                  GEMM_ERR_TIMEOUT through gemm_sync_status (no GPU fault)   */
+};
+
+typedef int32_t gemm_config_t;
+enum {
+    GEMM_CONFIG_AUTO = 0,
+    GEMM_CONFIG_128x256 = 1,   /* 1-CTA tile 128 x 256 x 64, 4-stage ring                      */
+    GEMM_CONFIG_128x128 = 2,   /* 1-CTA tile 128 x 128 x 64, 6-stage ring (more tiles)         */
+    GEMM_CONFIG_256x256 = 3    /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
+};
+
+/* What gemm_run would launch for a problem (for benchmarks and tests). */
+typedef struct {
+    int32_t config;     /* GEMM_CONFIG_* actually chosen                                     */
+    int32_t bm, bn, bk; /* output tile (per cluster) and K block                             */
+    int32_t stages;     /* shared-memory ring depth                                          */
+    int32_t cluster;    /* CTAs per cluster (1 or 2)                                         */
+    int64_t tiles_m, tiles_n, k_blocks;
+    int64_t grid;       /* CTAs launched (persistent)                                        */
+    int32_t threads;    /* threads per CTA                                                   */
+    int32_t smem_bytes; /* dynamic shared memory per CTA                                     */
+} gemm_plan_t;
+
+/* Create a handle bound to CUDA device `device`.  Checks that the device is sm_103,
+ * reads its SM count and allocates the 16-byte device error word.
+ * Returns INVALID_ARG (out == NULL or no such device), ARCH, or CUDA. */
+gemm_status_t gemm_create(gemm_handle_t* out, int device);
+
+/* Free everything the handle owns.  Synchronises the device first.  NULL is accepted. */
+gemm_status_t gemm_destroy(gemm_handle_t h);
+
+/* Enqueue C = A·B on `stream` (a cudaStream_t; NULL = legacy default stream) and return
+ * without waiting.  A, B, C are device pointers.  M == 0 or N == 0 is a no-op; K == 0
+ * writes zeros to C (the empty sum).  Device-side watchdog expiries are reported later
+ * by gemm_sync_status.  Launch failures return GEMM_ERR_CUDA. */
+gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C,
+                       int64_t M, int64_t N, int64_t K,
+                       int64_t lda, int64_t ldb, int64_t ldc,
+                       gemm_layout_t layout, gemm_dtype_t dtype, void* stream);
+
+/* Same operation on HOST buffers (pinned memory lets the copies run as DMA): copies A and
+ * B to handle-owned device buffers on `stream`, runs the kernel, copies C back (only the
+ * M x N window, never the row padding) and synchronises the stream.  Returns the
+ * watchdog status as gemm_sync_status does.  Grows its device buffers on demand
+ * (cudaMalloc) -- call once outside any timed region to size them. */
+gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C,
+                            int64_t M, int64_t N, int64_t K,
+                            int64_t lda, int64_t ldb, int64_t ldc,
+                            gemm_layout_t layout, gemm_dtype_t dtype, void* stream);
+
+/* Synchronise `stream`, then read and clear the device error word.  Returns
+ * GEMM_ERR_TIMEOUT if any kernel launched through this handle since the last call hit
+ * its watchdog, GEMM_ERR_CUDA if the stream reports an error, else GEMM_OK. */
+gemm_status_t gemm_sync_status(gemm_handle_t h, void* stream);
+
+/* Details of the last watchdog expiry seen by gemm_sync_status / gemm_run_host:
+ * info[0] = 1 (timeout), info[1] = role (0 producer, 1 mma, 2 epilogue, 3 drain),
+ * info[2] = CTA index, info[3] = tile index * 65536 + K block.  Zeros if none. */
+gemm_status_t gemm_error_info(gemm_handle_t h, int32_t info[4]);
+
+gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value);
+gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value);
+
+/* Fill *plan with the launch gemm_run would make for this problem (no GPU work). */
+gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                              gemm_layout_t layout, gemm_dtype_t dtype, gemm_plan_t* plan);
+
+/* The argument checks gemm_run applies, without a handle or a GPU: INVALID_ARG,
+ * UNSUPPORTED or OK exactly as gemm_run would return them before launching.  Pointers
+ * are only inspected (null, alignment), never dereferenced. */
+gemm_status_t gemm_check_args(const void* A, const void* B, const void* C,
+                              int64_t M, int64_t N, int64_t K,
+                              int64_t lda, int64_t ldb, int64_t ldc,
+                              gemm_layout_t layout, gemm_dtype_t dtype);
+
+/* Host copy of the device tile scheduler's map: linear tile index -> (tile row, tile
+ * column) for a tiles_m x tiles_n grid rastered in groups of `group_m` tile rows.
+ * Pure function, needs no GPU (tests check it is a bijection).  Returns INVALID_ARG if
+ * tile is out of range or an argument is not positive. */
+gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t group_m,
+                              int64_t* tile_m, int64_t* tile_n);
+
+/* Static description of a status code.  Never NULL. */
+const char* gemm_status_string(gemm_status_t s);
+
+/* GEMM_API_VERSION of the built library. */
+int32_t gemm_api_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DTG_GEMM_H */

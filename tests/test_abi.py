@@ -1,0 +1,116 @@
+"""C ABI checks that need no GPU: the library loads, exports every declared entry point,
+validates arguments exactly as documented, and its tile scheduler map is a bijection."""
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+HEADER = os.path.join(ROOT, "include", "gemm.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from dense_tiled_gemm_04_gb300 import build, native
+
+    build.build()
+    return native
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:const\s+)?\w+\*?\s+\**(gemm_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_core_entry_points():
+    names = declared_functions()
+    for core in ("gemm_create", "gemm_run", "gemm_destroy", "gemm_status_string", "gemm_sync_status"):
+        assert core in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    so = lib.load()
+    missing = [n for n in declared_functions() if not hasattr(so, n)]
+    assert not missing, missing
+
+
+def test_status_strings_and_version(lib):
+    so = lib.load()
+    assert so.gemm_api_version() == 1
+    for s in range(6):
+        assert lib.status_string(s).startswith("GEMM_")
+    assert "unknown" in lib.status_string(99)
+
+
+def test_null_handle_is_rejected_without_a_gpu(lib):
+    so = lib.load()
+    assert so.gemm_run(None, None, None, None, 1, 1, 1, 8, 8, 8, 0, 0, None) == lib.ERR_INVALID_ARG
+    assert so.gemm_sync_status(None, None) == lib.ERR_INVALID_ARG
+    assert so.gemm_set_option(None, 0, 0) == lib.ERR_INVALID_ARG
+    assert so.gemm_destroy(None) == lib.OK
+    assert so.gemm_create(None, 0) == lib.ERR_INVALID_ARG
+
+
+def test_create_without_a_gpu_reports_an_error(lib):
+    import ctypes
+    import torch
+
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    h = ctypes.c_void_p()
+    st = lib.load().gemm_create(ctypes.byref(h), 0)
+    assert st in (lib.ERR_CUDA, lib.ERR_INVALID_ARG)
+    assert not h.value
+
+
+P = 1 << 20  # a 16-byte-aligned fake address: gemm_check_args never dereferences
+
+
+@pytest.mark.parametrize("case,expected", [
+    # (A, B, C, M, N, K, lda, ldb, ldc, layout, dtype)
+    ((P, P, P, 128, 256, 192, 192, 256, 256, 0, 0), 0),
+    ((P, P, P, 1000, 1000, 1000, 1000, 1000, 1000, 1, 0), 0),
+    ((P, P, P, 0, 5, 7, 0, 0, 0, 0, 0), 0),            # M == 0: no-op, nothing else checked
+    ((P, P, P, 5, 0, 7, 0, 0, 0, 0, 0), 0),            # N == 0
+    ((0, 0, P, 5, 8, 0, 0, 0, 8, 0, 0), 0),            # K == 0: A, B unused
+    ((P, P, P, -1, 8, 8, 8, 8, 8, 0, 0), 1),           # negative size
+    ((P, P, P, 8, 8, 8, 8, 8, 8, 2, 0), 1),            # bad layout
+    ((P, P, P, 8, 8, 8, 8, 8, 8, 0, 7), 1),            # bad dtype
+    ((0, P, P, 8, 8, 8, 8, 8, 8, 0, 0), 1),            # null A
+    ((P, P, 0, 8, 8, 8, 8, 8, 8, 0, 0), 1),            # null C
+    ((P, P, P, 8, 16, 16, 8, 16, 16, 0, 0), 1),        # lda < K
+    ((P, P, P, 8, 16, 8, 8, 8, 16, 0, 0), 1),          # NN: ldb < N
+    ((P, P, P, 8, 16, 24, 24, 16, 16, 1, 0), 1),       # TN: ldb < K
+    ((P, P, P, 8, 16, 8, 8, 16, 8, 0, 0), 1),          # ldc < N
+    ((P + 2, P, P, 8, 8, 8, 8, 8, 8, 0, 0), 2),        # A not 16-byte aligned
+    ((P, P + 8, P, 8, 8, 8, 8, 8, 8, 0, 1), 2),        # B not 16-byte aligned
+    ((P, P, P + 4, 8, 8, 8, 8, 8, 8, 0, 0), 2),        # C not 16-byte aligned
+    ((P, P, P, 8, 8, 12, 12, 8, 8, 0, 0), 2),          # lda not a multiple of 8
+    ((P, P, P, 65, 97, 130, 136, 104, 104, 0, 0), 0),  # the page's tail case with padded ld
+    ((P, P, P, 65, 97, 130, 130, 97, 97, 0, 0), 2),    # ... and without padding
+    ((P, P, P, 1 << 31, 8, 8, 8, 8, 8, 0, 0), 2),      # dimension beyond int32
+])
+def test_check_args(lib, case, expected):
+    assert lib.check_args(*case) == expected
+
+
+@pytest.mark.parametrize("tiles_m,tiles_n,group", [(1, 1, 1), (2, 4, 16), (64, 32, 16), (8, 4, 3),
+                                                   (17, 5, 4), (7, 9, 7), (5, 3, 100), (33, 1, 8)])
+def test_tile_coord_is_a_bijection(lib, tiles_m, tiles_n, group):
+    seen = set()
+    for t in range(tiles_m * tiles_n):
+        tm, tn = lib.tile_coord(t, tiles_m, tiles_n, group)
+        assert 0 <= tm < tiles_m and 0 <= tn < tiles_n
+        seen.add((tm, tn))
+    assert len(seen) == tiles_m * tiles_n
+
+
+def test_tile_coord_groups_rows(lib):
+    # With a group of 4 tile rows, consecutive tiles walk down the rows of one column
+    # before moving to the next column.
+    coords = [lib.tile_coord(t, 8, 3, 4) for t in range(6)]
+    assert coords == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1), (1, 1)]
+    with pytest.raises(Exception):
+        lib.tile_coord(24, 8, 3, 4)

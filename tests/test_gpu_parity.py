@@ -1,0 +1,321 @@
+"""GPU parity: the CUDA path (through the C ABI) against the CPU oracle.
+
+Bar: bit-exact on integer-valued inputs (every partial sum is an integer of magnitude
+<= 4K < 2^24, exact in fp32 in any order, then one round-to-nearest-even on both sides);
+within |gpu - ref| <= atol + rtol*|ref| otherwise, with atol = rtol = 1e-2 for fp16
+output and 3e-2 for bf16 output.  Small and ragged sizes are compared element by
+element in full; the full-size workloads on sampled rows the oracle computes one by one.
+"""
+import numpy as np
+import pytest
+import torch
+
+from dense_tiled_gemm_04_gb300 import native
+from dense_tiled_gemm_04_gb300.workloads import WORKLOADS, make_inputs, round_up, workload_inputs
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+TOL = {"f16": (1e-2, 1e-2), "bf16": (3e-2, 3e-2)}
+SENTINEL = 0x7777  # a finite 16-bit code that C = A·B never produces in these tests
+
+
+@pytest.fixture(scope="module")
+def g():
+    if not torch.cuda.is_available():
+        pytest.skip("no CUDA device")
+    from dense_tiled_gemm_04_gb300 import build
+
+    build.build()
+    oracle.build()
+    h = native.Gemm(0)
+    yield h
+    h.close()
+
+
+def to_device(x: torch.Tensor) -> torch.Tensor:
+    """Copy a (possibly row-padded) CPU view to the GPU keeping its row pitch."""
+    rows, cols = x.shape
+    if x.numel() == 0:
+        return x.cuda()
+    ld = x.stride(0) if rows > 1 else cols
+    base = x.as_strided((rows, ld), (ld, 1)) if rows > 1 else x
+    return base.cuda()[:, :cols]
+
+
+def codes(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
+
+
+def gpu_gemm(g, A, B, layout, dtype, extra_rows=0, ldc_pad=0, stream=None):
+    """Run through the C ABI; C sits in a sentinel-filled buffer with spare rows/columns.
+
+    Returns (C codes M x N, whole buffer codes) so callers can check the guard region."""
+    M, K = A.shape
+    N = B.shape[1] if layout == "NN" else B.shape[0]
+    ldc = round_up(max(N, 1), 8) + ldc_pad
+    tdt = A.dtype
+    buf = torch.full((M + extra_rows, ldc), 0, dtype=torch.int16, device="cuda")
+    buf.fill_(SENTINEL)
+    buf = buf.view(tdt)
+    C = buf[:M, :N]
+    dA, dB = to_device(A), to_device(B)
+    lda = dA.stride(0) if M > 1 else round_up(max(K, 1), 8)
+    brows = B.shape[0]
+    ldb = dB.stride(0) if brows > 1 else round_up(max(B.shape[1], 1), 8)
+    s = 0 if stream is None else stream.cuda_stream
+    st = g.run_raw(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, lda, ldb, ldc,
+                   native.LAYOUTS[layout], native.DTYPES[dtype], s)
+    assert st == native.OK, native.status_string(st)
+    assert g.sync_status(stream) == native.OK
+    return codes(C), codes(buf)
+
+
+def assert_close(got: np.ndarray, ref: np.ndarray, dtype: str, what=""):
+    a, r = oracle.decode(got, dtype), oracle.decode(ref, dtype)
+    atol, rtol = TOL[dtype]
+    bad = ~(np.abs(a - r) <= atol + rtol * np.abs(r))
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} outside tolerance; first at {idx.tolist()}: "
+                             f"gpu {a[tuple(idx[0])]} ref {r[tuple(idx[0])]}")
+
+
+def assert_exact(got: np.ndarray, ref: np.ndarray, what=""):
+    bad = got != ref
+    if bad.any():
+        idx = np.argwhere(bad)[:5]
+        raise AssertionError(f"{what}: {bad.sum()} of {bad.size} codes differ; first at {idx.tolist()}: "
+                             f"gpu {got[tuple(idx[0])]:#06x} ref {ref[tuple(idx[0])]:#06x}")
+
+
+def assert_guard(buf: np.ndarray, M: int, N: int):
+    guard = buf.copy()
+    guard[:M, :N] = SENTINEL
+    assert np.all(guard == SENTINEL), "a write landed outside the M x N window of C"
+
+
+# ------------------------------------------------------------------ the five workloads
+
+
+def sample_rows(M: int, n: int, seed: int) -> np.ndarray:
+    rng = np.random.default_rng(seed)
+    fixed = [0, 1, 127, 128, M - 129, M - 128, M - 2, M - 1]
+    rows = np.unique(np.clip(np.concatenate([fixed, rng.integers(0, M, n)]), 0, M - 1))
+    return rows
+
+
+@pytest.mark.parametrize("name", ["c1", "c2"])
+@pytest.mark.parametrize("dist", ["workload", "int"])
+def test_small_workloads_full(g, name, dist):
+    w = WORKLOADS[name]
+    if dist == "int":
+        w = w.with_dist("int")
+    A, B = workload_inputs(w)
+    got, buf = gpu_gemm(g, A, B, w.layout, w.dtype, extra_rows=2, ldc_pad=8)
+    ref = oracle.gemm(A, B, w.layout, w.dtype)
+    assert_guard(buf, w.M, w.N)
+    if dist == "int":
+        assert_exact(got, ref, f"{name} int")
+    else:
+        assert_close(got, ref, w.dtype, name)
+
+
+@pytest.mark.parametrize("name", ["c3", "c4", "c5"])
+@pytest.mark.parametrize("dist", ["workload", "int"])
+def test_full_size_workloads_sampled(g, name, dist):
+    w = WORKLOADS[name]
+    if dist == "int":
+        w = w.with_dist("int")
+    A, B = workload_inputs(w)
+    got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    rows = sample_rows(w.M, 24 if w.M * w.N * w.K < 2**40 else 12, seed=w.seed)
+    ref, _, _ = oracle.gemm_rows(A, B, w.layout, w.dtype, rows)
+    if dist == "int":
+        assert_exact(got[rows], ref, f"{name} int")
+    else:
+        assert_close(got[rows], ref, w.dtype, name)
+    # The sampled rows cover every column tile; also check every row is finite and written.
+    vals = oracle.decode(got, w.dtype)
+    assert np.isfinite(vals).all()
+
+
+# ------------------------------------------------------------------ edges and pins
+
+SHAPES = [(1, 1, 1), (1, 8, 3), (3, 5, 7), (8, 8, 8), (17, 9, 33), (64, 64, 64), (65, 97, 130),
+          (127, 129, 63), (128, 256, 64), (129, 257, 65), (200, 300, 1), (255, 511, 200), (1, 1000, 129),
+          (300, 1, 77), (257, 130, 1000)]
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128])
+def test_ragged_shapes(g, layout, dtype, config):
+    g.set_option(native.OPT_CONFIG, config)
+    try:
+        for i, (M, N, K) in enumerate(SHAPES):
+            for dist in ("int", "normal"):
+                bcols = N if layout == "NN" else K
+                A, B = make_inputs(M, N, K, layout, dtype, dist, seed=1000 + i,
+                                   lda=round_up(K, 8) + (8 if i % 2 else 0),
+                                   ldb=round_up(bcols, 8) + (8 if i % 3 == 0 else 0))
+                got, buf = gpu_gemm(g, A, B, layout, dtype, extra_rows=1, ldc_pad=8 * (i % 2))
+                ref = oracle.gemm(A, B, layout, dtype)
+                assert_guard(buf, M, N)
+                what = f"{(M, N, K)} {layout} {dtype} {dist} cfg{config}"
+                if dist == "int":
+                    assert_exact(got, ref, what)
+                else:
+                    assert_close(got, ref, dtype, what)
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_tail_all_ones_is_130(g, layout):
+    # M=65, N=97, K=130: leading dimensions padded to multiples of 8 (136, 104) while the
+    # logical sizes stay ragged; every output must be 130, not 128.
+    M, N, K = 65, 97, 130
+    A, B = make_inputs(M, N, K, layout, "f16", "ones", seed=0, lda=136, ldb=104 if layout == "NN" else 136)
+    got, buf = gpu_gemm(g, A, B, layout, "f16", extra_rows=3, ldc_pad=8)
+    vals = oracle.decode(got, "f16")
+    assert np.all(vals == 130.0), np.unique(vals)
+    assert_guard(buf, M, N)
+
+
+def test_fp32_accumulation_pin(g):
+    # Row [2048, 1, 1] times column [1, 1, 1]: 2050 only if partial sums are kept in fp32.
+    A = torch.tensor([[2048.0, 1.0, 1.0]], dtype=torch.float16)
+    B = torch.ones((3, 1), dtype=torch.float16)
+    got, _ = gpu_gemm(g, A, B, "NN", "f16")
+    assert oracle.decode(got, "f16")[0, 0] == 2050.0
+    # Same in the TN layout and with the 1s spread across two K blocks of 64.
+    A2 = torch.zeros((1, 130), dtype=torch.float16)
+    A2[0, 0], A2[0, 64], A2[0, 129] = 2048.0, 1.0, 1.0
+    B2 = torch.ones((1, 130), dtype=torch.float16)
+    got2, _ = gpu_gemm(g, A2, B2, "TN", "f16")
+    assert oracle.decode(got2, "f16")[0, 0] == 2050.0
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_identity_and_permutation(g, layout, dtype):
+    M, K = 300, 384
+    A, _ = make_inputs(M, K, K, layout, dtype, "uniform", seed=77)
+    eye = torch.eye(K, dtype=A.dtype)
+    got, _ = gpu_gemm(g, A, eye, layout, dtype)
+    assert_exact(got, oracle._codes(A), "A·I")
+    perm = torch.randperm(K, generator=torch.Generator().manual_seed(3))
+    P = torch.zeros(K, K, dtype=A.dtype)
+    P[perm, torch.arange(K)] = 1
+    got, _ = gpu_gemm(g, A, P if layout == "NN" else P.T.contiguous(), layout, dtype)
+    assert_exact(got, oracle._codes(A)[:, perm.numpy()], "A·P")
+
+
+def test_k_zero_writes_zeros_and_m_n_zero_is_noop(g):
+    for dtype in ("f16", "bf16"):
+        A = torch.empty((37, 0), dtype=native_dtype(dtype))
+        B = torch.empty((0, 45), dtype=native_dtype(dtype))
+        got, buf = gpu_gemm(g, A, B, "NN", dtype, extra_rows=1, ldc_pad=8)
+        assert np.all(got == 0)
+        assert_guard(buf, 37, 45)
+    C = torch.full((4, 8), 3.0, dtype=torch.float16, device="cuda")
+    for (M, N) in [(0, 8), (4, 0)]:
+        st = g.run_raw(C.data_ptr(), C.data_ptr(), C.data_ptr(), M, N, 8, 8, 8, 8, 0, 0, 0)
+        assert st == native.OK
+    torch.cuda.synchronize()
+    assert torch.all(C == 3.0)
+
+
+def native_dtype(dtype):
+    return {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
+
+
+def test_several_tiles_per_cta_and_raster_groups(g):
+    M, N, K = 1000, 1000, 520
+    A, B = make_inputs(M, N, K, "TN", "f16", "int", seed=5)
+    ref = oracle.gemm(A, B, "TN", "f16")
+    try:
+        for max_ctas, group in [(1, 16), (3, 1), (7, 3), (0, 64), (5, 1000)]:
+            g.set_option(native.OPT_MAX_CTAS, max_ctas)
+            g.set_option(native.OPT_RASTER_GROUP, group)
+            got, _ = gpu_gemm(g, A, B, "TN", "f16")
+            assert_exact(got, ref, f"max_ctas={max_ctas} group={group}")
+    finally:
+        g.set_option(native.OPT_MAX_CTAS, 0)
+        g.set_option(native.OPT_RASTER_GROUP, 16)
+
+
+def test_large_extents(g):
+    # Long M (131072 rows) and long N (65536 columns) with a short K: the TMA coordinates
+    # and the tile scheduler at sizes far beyond the workloads' tile counts.
+    for (M, N, K, layout) in [(131072, 136, 72, "TN"), (136, 65536, 72, "NN")]:
+        A, B = make_inputs(M, N, K, layout, "bf16", "int", seed=M + N)
+        got, _ = gpu_gemm(g, A, B, layout, "bf16")
+        rows = sample_rows(M, 16, seed=1)
+        ref, _, _ = oracle.gemm_rows(A, B, layout, "bf16", rows)
+        assert_exact(got[rows], ref, f"{(M, N, K)}")
+
+
+def test_side_stream(g):
+    w = WORKLOADS["c2"].with_dist("int")
+    A, B = workload_inputs(w)
+    s = torch.cuda.Stream()
+    got, _ = gpu_gemm(g, A, B, w.layout, w.dtype, stream=s)
+    assert_exact(got, oracle.gemm(A, B, w.layout, w.dtype), "side stream")
+
+
+def test_torch_binding_matmul(g):
+    A, B = make_inputs(333, 444, 555, "NN", "bf16", "int", seed=8, lda=560, ldb=448)
+    C = native.matmul(to_device(A), to_device(B), "NN")
+    torch.cuda.synchronize()
+    assert_exact(codes(C), oracle.gemm(A, B, "NN", "bf16"), "matmul")
+
+
+def test_misaligned_arguments_are_rejected(g):
+    A = torch.zeros((64, 72), dtype=torch.float16, device="cuda")
+    B = torch.zeros((72, 64), dtype=torch.float16, device="cuda")
+    C = torch.zeros((64, 72), dtype=torch.float16, device="cuda")
+    ok = g.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 64, 64, 64, 72, 64, 72, 0, 0, 0)
+    assert ok == native.OK
+    assert g.run_raw(A.data_ptr() + 2, B.data_ptr(), C.data_ptr(), 64, 64, 64, 72, 64, 72, 0, 0, 0) \
+        == native.ERR_UNSUPPORTED
+    assert g.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 64, 64, 64, 68, 64, 72, 0, 0, 0) \
+        == native.ERR_UNSUPPORTED
+    assert g.run_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), 64, 64, 64, 72, 64, 32, 0, 0, 0) \
+        == native.ERR_INVALID_ARG
+    assert g.sync_status() == native.OK
+
+
+def test_run_host_matches_oracle(g):
+    w = WORKLOADS["c2"]
+    A, B = workload_inputs(w)
+    C = torch.empty((w.M, w.N), dtype=A.dtype).pin_memory()
+    st = g.run_host(A.pin_memory(), B.pin_memory(), C, w.layout)
+    assert st == native.OK, native.status_string(st)
+    assert_close(codes(C), oracle.gemm(A, B, w.layout, w.dtype), w.dtype, "run_host")
+
+
+def test_watchdog_timeout_is_reported_and_context_survives(g):
+    # One ring stage is left unarmed in CTA 0: the MMA thread's wait on it must run out,
+    # the kernel must leave cleanly, and the host must read GEMM_ERR_TIMEOUT.
+    w = WORKLOADS["c2"].with_dist("int")
+    A, B = workload_inputs(w)
+    g.set_option(native.OPT_TIMEOUT_NS, 50_000_000)
+    g.set_option(native.OPT_FAULT_INJECT, 1)
+    try:
+        dA, dB = to_device(A), to_device(B)
+        C = native.empty_output(w.M, w.N, A.dtype, "cuda")
+        st = g.run_raw(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), w.M, w.N, w.K, dA.stride(0), dB.stride(0),
+                       C.stride(0), native.LAYOUTS[w.layout], native.DTYPES[w.dtype], 0)
+        assert st == native.OK
+        assert g.sync_status() == native.ERR_TIMEOUT
+        info = g.error_info()
+        assert info[0] == 1 and info[2] == 0, info  # timeout, in CTA 0
+    finally:
+        g.set_option(native.OPT_FAULT_INJECT, 0)
+        g.set_option(native.OPT_TIMEOUT_NS, 2_000_000_000)
+    # The context is still usable and the next run is correct.
+    got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    assert_exact(got, oracle.gemm(A, B, w.layout, w.dtype), "after timeout")
