@@ -81,7 +81,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except (FileNotFoundError, OSError):
             self.proc = None
             return
@@ -288,27 +288,29 @@ def run_ours(args, w):
 
     # End to end through the public C ABI on pinned host buffers: H2D of A and B, the
     # kernel, D2H of C, synchronised every step.
-    Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
-    Ch = torch.empty((w.M, w.N), dtype=A_cpu.dtype).pin_memory()
-    e2e_steps = max(3, min(args.steps, 20))
-    if g.run_host(Ah, Bh, Ch, w.layout, stream) != native.OK:  # sizes the device staging buffers
-        raise RuntimeError("gemm_run_host failed")
-    barrier(world)
-    t0 = time.perf_counter()
-    for _ in range(e2e_steps):
-        st = g.run_host(Ah, Bh, Ch, w.layout, stream)
-        if st != native.OK:
-            raise native.GemmError(st, "gemm_run_host")
-    e2e_s = (time.perf_counter() - t0) / e2e_steps
-    e2e_s = reduce_max([e2e_s], world, dev)[0]
-    e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
-           "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
+    e2e = None
+    if not args.no_e2e:
+        Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
+        Ch = torch.empty((w.M, w.N), dtype=A_cpu.dtype).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        if g.run_host(Ah, Bh, Ch, w.layout, stream) != native.OK:  # sizes the device staging buffers
+            raise RuntimeError("gemm_run_host failed")
+        barrier(world)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            st = g.run_host(Ah, Bh, Ch, w.layout, stream)
+            if st != native.OK:
+                raise native.GemmError(st, "gemm_run_host")
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e_s = reduce_max([e2e_s], world, dev)[0]
+        e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+               "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
 
     peaks, peak_src = load_peaks()
     peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(WORKLOAD),
+                "traffic": load_traffic(args.workload),
                 "peak_source": f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback",
                 "nominal_dense_peak_tflops": 2250.0, "frac_of_nominal": achieved / 2250.0,
                 "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
@@ -324,13 +326,15 @@ def run_ours(args, w):
         line = {
             "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": "bf16",
-            "data": "synthetic: seeded N(0,1)/sqrt(K) inputs rounded to bf16 (torch CPU generator, seed 3)",
+            "vs_baseline": None, "dtype": w.dtype,
+            "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
+                    f"(torch CPU generator, seed {w.seed})",
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
                        "accumulate": "fp32", "out": w.dtype,
                        "kernel": f"tcgen05 {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
                                  f"ring, {plan['grid']} persistent CTAs",
-                       "l2": "inputs larger than L2 (A, B, C = 384 MiB > 129 MB), no flush",
+                       "l2": (f"inputs larger than L2 (A, B, C = {w.algorithmic_bytes / 2**20:.0f} MiB > 129 MB), "
+                              "no flush") if w.algorithmic_bytes > 129e6 else "inputs fit in L2: warm-L2 number",
                        "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU"},
             "roofline": roofline,
             "cpu_baseline": cpu,
@@ -349,17 +353,19 @@ def run_ours(args, w):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawDescriptionHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
+    ap.add_argument("--workload", default=WORKLOAD, help="c1..c5 (default c4, the headline workload)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     from dense_tiled_gemm_04_gb300.workloads import WORKLOADS
 
-    w = WORKLOADS[WORKLOAD]
+    w = WORKLOADS[args.workload]
     if args.impl == "reference":
         return run_reference(args, w)
     return run_ours(args, w)

@@ -272,6 +272,8 @@ gemm_status_t launch(gemm_handle_t h, const void* A, const void* B, void* C, int
     kp.fault_inject = static_cast<int32_t>(h->fault_inject);
     kp.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
     kp.err = h->d_err;
+    kp.C = C;
+    kp.ldc = ldc;
 
     void* args[] = {&tA, &tB, &tC, &kp};
     cudaLaunchConfig_t cfg;

@@ -59,6 +59,8 @@ struct KernelParams {
     int32_t fault_inject;        // test hook, see GEMM_OPT_FAULT_INJECT
     uint64_t timeout_ns;         // watchdog per wait
     int32_t* err;                // device error word [4]
+    void* C;                     // output base, for the ragged-N edge written without TMA
+    int64_t ldc;                 // output row pitch (elements)
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -380,6 +382,36 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int i = 0; i < 64; ++i) v[i] = 0u;  // K == 0: the empty sum
                 }
+                const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
+                if ((p.N & 7) != 0 && x + kEpiCols > p.N) {
+                    // Ragged right edge with N not a multiple of 8: a TMA store clips only at
+                    // 16-byte granularity and would write C's row padding, so this box is
+                    // written with plain masked stores (one row per thread).
+                    const int64_t row = static_cast<int64_t>(y) + lane;
+                    if (row < p.M && x < p.N) {
+                        uint16_t* crow = static_cast<uint16_t*>(p.C) + row * p.ldc;
+#pragma unroll
+                        for (int ch = 0; ch < 8; ++ch) {
+                            const int32_t col = x + ch * 8;
+                            if (col + 8 <= p.N) {  // a whole 16-byte chunk: one vector store
+                                uint4 q;
+                                q.x = pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]);
+                                q.y = pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]);
+                                q.z = pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]);
+                                q.w = pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]);
+                                *reinterpret_cast<uint4*>(crow + col) = q;
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; e += 2) {
+                                    const uint32_t two = pack2<BF16>(v[8 * ch + e], v[8 * ch + e + 1]);
+                                    if (col + e < p.N) crow[col + e] = static_cast<uint16_t>(two & 0xFFFFu);
+                                    if (col + e + 1 < p.N) crow[col + e + 1] = static_cast<uint16_t>(two >> 16);
+                                }
+                            }
+                        }
+                    }
+                    continue;
+                }
                 // The staging buffer is reusable once the store issued from it two boxes
                 // ago has finished reading it.
                 if (lane == 0) ptx::bulk_wait_group_read<1>();
@@ -398,7 +430,6 @@ __global__ void __launch_bounds__(kThreads, 1)
                 ptx::fence_proxy_async_smem();
                 __syncwarp();
                 if (lane == 0) {
-                    const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
                     if (x < p.N && y < p.M) ptx::tma_store_2d(&tmC, stg0 + sbuf * kStgBytes, x, y);
                     ptx::bulk_commit_group();
                 }

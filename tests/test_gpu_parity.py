@@ -35,10 +35,15 @@ def g():
 
 
 def to_device(x: torch.Tensor) -> torch.Tensor:
-    """Copy a (possibly row-padded) CPU view to the GPU keeping its row pitch."""
+    """Copy a (possibly row-padded) CPU view to the GPU keeping its row pitch; a row pitch
+    that is not a multiple of 8 elements is widened to one (NaN padding)."""
     rows, cols = x.shape
     if x.numel() == 0:
         return x.cuda()
+    if rows > 1 and x.stride(0) % 8 != 0:
+        buf = torch.full((rows, round_up(cols, 8)), float("nan"), dtype=x.dtype)
+        buf[:, :cols] = x
+        x = buf[:, :cols]
     ld = x.stride(0) if rows > 1 else cols
     base = x.as_strided((rows, ld), (ld, 1)) if rows > 1 else x
     return base.cuda()[:, :cols]
