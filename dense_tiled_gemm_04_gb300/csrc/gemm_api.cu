@@ -510,3 +510,160 @@ const char* gemm_status_string(gemm_status_t s)
 int32_t gemm_api_version(void) { return GEMM_API_VERSION; }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------- allocation-free entry point
+//
+// gemm_run_noalloc serves callers that cannot allocate device memory (stream capture in
+// progress, a host engine that owns all device memory, paths that cannot take the device
+// synchronisation an allocation may imply).  The GEMM kernel's only scratch -- the
+// 16-byte watchdog record that a handle normally cudaMallocs -- lives in the file-scope
+// array below instead.  Nothing here calls cudaMalloc, cudaFree or any allocating routine.
+namespace {
+
+constexpr size_t kNoallocScratchBytes = 256;                    // stated maximum
+constexpr size_t kNoallocRecordBytes = 4 * sizeof(int32_t);     // what the kernel writes
+constexpr int kNoallocMaxDevices = 64;
+
+// One copy per device, kept until the process exits.  On the host this name is only a
+// stand-in for the symbol; its device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) int32_t g_noalloc_scratch[kNoallocScratchBytes / sizeof(int32_t)];
+
+struct NoallocDevice {
+    std::once_flag once;
+    gemm_status_t setup = GEMM_ERR_CUDA;
+    int32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
+    int num_sms = 0;
+    std::mutex mu;               // guards attrs_set
+    bool attrs_set[8] = {false, false, false, false, false, false, false, false};
+};
+
+NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
+
+// Runs once per device, with that device current (the caller's current device).
+void noalloc_setup(NoallocDevice& d, int device)
+{
+    int major = 0, minor = 0, sms = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
+        d.setup = GEMM_ERR_CUDA;
+        return;
+    }
+    if (major != 10 || minor != 3) {
+        d.setup = GEMM_ERR_ARCH;
+        return;
+    }
+    void* addr = nullptr;
+    if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
+        d.setup = GEMM_ERR_CUDA;
+        return;
+    }
+    d.scratch = static_cast<int32_t*>(addr);
+    d.num_sms = sms;
+    d.setup = GEMM_OK;
+}
+
+// Tensor-map encoding without the handle's cache (host-only work, no allocation).
+bool encode_tmap_uncached(const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+                          uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out)
+{
+    if (!load_encode_fn()) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {pitch_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    const CUtensorMapDataType dt =
+        dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    return g_encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
+
+extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
+                                          int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout,
+                                          gemm_dtype_t dtype, void* stream, int32_t* watchdog_info)
+{
+    const gemm_status_t v = validate_args(A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
+    if (v != GEMM_OK) return v;
+    if (kNoallocRecordBytes > kNoallocScratchBytes) return GEMM_ERR_UNSUPPORTED;  // scratch need above the maximum
+    int device = -1;
+    if (cudaGetDevice(&device) != cudaSuccess) return GEMM_ERR_CUDA;
+    if (device < 0 || device >= kNoallocMaxDevices) return GEMM_ERR_UNSUPPORTED;
+    NoallocDevice& d = g_noalloc_devices[device];
+    std::call_once(d.once, [&] { noalloc_setup(d, device); });
+    if (d.setup != GEMM_OK) return d.setup;
+    if (watchdog_info) std::memset(watchdog_info, 0, kNoallocRecordBytes);
+    if (M == 0 || N == 0) return GEMM_OK;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // The record keeps the previous call's contents: clear it before this launch.
+    if (cudaMemsetAsync(d.scratch, 0, kNoallocRecordBytes, s) != cudaSuccess) return GEMM_ERR_CUDA;
+
+    if (K == 0) {
+        int blocks = static_cast<int>(cdiv(M * N, 256));
+        if (blocks > d.num_sms * 8) blocks = d.num_sms * 8;
+        if (dtype == GEMM_DTYPE_BF16)
+            dtg::zero_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc);
+        else
+            dtg::zero_fill_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<__half*>(C), M, N, ldc);
+        if (cudaPeekAtLastError() != cudaSuccess) return GEMM_ERR_CUDA;
+    } else {
+        gemm_handle_s opts;  // default options; only num_sms is read by the planners
+        opts.num_sms = d.num_sms;
+        const int config = pick_config(&opts, M, N);
+        const KernelChoice kc = kernel_choice(config, dtype, layout);
+        gemm_plan_t plan;
+        fill_plan(&opts, M, N, K, kc, &plan);
+
+        CUtensorMap tA, tB, tC;
+        const bool nn = layout == GEMM_LAYOUT_NN;
+        if (!encode_tmap_uncached(A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
+        if (nn ? !encode_tmap_uncached(B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)
+               : !encode_tmap_uncached(B, K, N, ldb * 2, dtg::kBK, kc.bn, dtype, &tB))
+            return GEMM_ERR_CUDA;
+        if (!encode_tmap_uncached(C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
+        {
+            std::lock_guard<std::mutex> lock(d.mu);
+            const int slot = attr_slot(kc, dtype, layout);
+            if (!d.attrs_set[slot]) {
+                if (cudaFuncSetAttribute(kc.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
+                    return GEMM_ERR_CUDA;
+                d.attrs_set[slot] = true;
+            }
+        }
+        KernelParams kp;
+        kp.M = static_cast<int32_t>(M);
+        kp.N = static_cast<int32_t>(N);
+        kp.K = static_cast<int32_t>(K);
+        kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
+        kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
+        kp.num_kb = static_cast<int32_t>(plan.k_blocks);
+        kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
+        kp.group_m = static_cast<int32_t>(opts.raster_group);
+        kp.fault_inject = 0;
+        kp.timeout_ns = static_cast<uint64_t>(opts.timeout_ns);
+        kp.err = d.scratch;
+        kp.C = C;
+        kp.ldc = ldc;
+        void* args[] = {&tA, &tB, &tC, &kp};
+        cudaLaunchConfig_t cfg;
+        std::memset(&cfg, 0, sizeof(cfg));
+        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
+        cfg.blockDim = dim3(dtg::kThreads, 1, 1);
+        cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
+        cfg.stream = s;
+        if (cudaLaunchKernelExC(&cfg, kc.fn, args) != cudaSuccess) return GEMM_ERR_CUDA;
+    }
+
+    if (watchdog_info) {
+        int32_t info[4] = {0, 0, 0, 0};
+        if (cudaMemcpyAsync(info, d.scratch, kNoallocRecordBytes, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaStreamSynchronize(s) != cudaSuccess) return GEMM_ERR_CUDA;
+        std::memcpy(watchdog_info, info, kNoallocRecordBytes);
+        if (info[0] != 0) return GEMM_ERR_TIMEOUT;
+    }
+    return GEMM_OK;
+}

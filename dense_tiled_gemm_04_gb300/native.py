@@ -65,6 +65,7 @@ def load() -> ctypes.CDLL:
         "gemm_query_plan": ([p, i64, i64, i64, i32, i32, ctypes.POINTER(gemm_plan_t)], i32),
         "gemm_check_args": ([p, p, p, i64, i64, i64, i64, i64, i64, i32, i32], i32),
         "gemm_tile_coord": ([i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
+        "gemm_run_noalloc": ([p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p, ctypes.POINTER(i32)], i32),
         "gemm_status_string": ([i32], ctypes.c_char_p),
         "gemm_api_version": ([], i32),
     }

@@ -151,6 +151,38 @@ gemm_status_t gemm_check_args(const void* A, const void* B, const void* C,
 gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, int64_t group_m,
                               int64_t* tile_m, int64_t* tile_n);
 
+/* C = A·B without a handle and without allocating any device memory.
+ *
+ * The paper has no counterpart to this entry point; it exists for callers that cannot
+ * call cudaMalloc: code enqueuing work while a stream is being captured into a graph,
+ * plug-ins running inside an engine that owns every byte of device memory through its
+ * own pool, latency-critical paths that cannot afford the implicit device-wide
+ * synchronisation an allocation may cause, or a process already at its memory limit.
+ *
+ * Arguments and layouts are those of gemm_run (A, B, C device pointers; same checks and
+ * status codes); the kernel, tile configuration and results are the same.  The only
+ * scratch the kernel needs -- its 16-byte watchdog record -- lives in a 256-byte
+ * file-scope __device__ array inside the library (every GPU that loads the library keeps
+ * those 256 bytes until the process exits).  A call whose scratch need exceeded that
+ * maximum would be rejected with GEMM_ERR_UNSUPPORTED; this kernel's need is fixed at
+ * 16 bytes, so no problem size is rejected for that reason.
+ *
+ * Set-up: the first call on a device (the caller's current device) looks up the array's
+ * device address with cudaGetSymbolAddress and checks the device is sm_103; make that
+ * first call before any stream capture.  Every call clears the record with
+ * cudaMemsetAsync on `stream`, then launches.  All calls share the one record, so calls
+ * that overlap on the GPU (different streams, no ordering) race on it.
+ *
+ * watchdog_info: NULL -> the call returns as soon as the work is enqueued (asynchronous,
+ * like gemm_run) and a watchdog expiry is not reported.  Non-NULL (host memory, 4 int32)
+ * -> the call synchronises `stream`, copies the record there ({1, role, CTA, tile*65536 +
+ * K block} after an expiry, zeros otherwise) and returns GEMM_ERR_TIMEOUT on an expiry. */
+gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
+                               int64_t M, int64_t N, int64_t K,
+                               int64_t lda, int64_t ldb, int64_t ldc,
+                               gemm_layout_t layout, gemm_dtype_t dtype, void* stream,
+                               int32_t* watchdog_info);
+
 /* Static description of a status code.  Never NULL. */
 const char* gemm_status_string(gemm_status_t s);
 
