@@ -30,7 +30,8 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor roofline"
 WORKLOAD = "c4"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["dense_tiled_gemm_04_gb300/csrc/gemm_kernel.cuh", "dense_tiled_gemm_04_gb300/csrc/sm103_ptx.cuh",
+KERNEL_SOURCES = ["dense_tiled_gemm_04_gb300/csrc/gemm_kernel.cuh", "dense_tiled_gemm_04_gb300/csrc/gemm_kernel_pair.cuh",
+                  "dense_tiled_gemm_04_gb300/csrc/sm103_ptx.cuh",
                   "dense_tiled_gemm_04_gb300/csrc/gemm_api.cu"]
 
 
@@ -242,6 +243,8 @@ def run_ours(args, w):
         dist.init_process_group("nccl", device_id=dev)
     lib_build.build()
     g = native.Gemm(local)
+    g.set_option(native.OPT_CONFIG, {"auto": native.CONFIG_AUTO, "128x256": native.CONFIG_128x256,
+                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256}[args.config])
 
     A_cpu, B_cpu = workload_inputs(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
@@ -332,7 +335,9 @@ def run_ours(args, w):
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
                        "accumulate": "fp32", "out": w.dtype,
                        "kernel": f"tcgen05 {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
-                                 f"ring, {plan['grid']} persistent CTAs",
+                                 f"ring, {plan['grid']} persistent CTAs"
+                                 + (f" in {plan['grid'] // plan['cluster']} CTA pairs (cta_group::2)"
+                                    if plan["cluster"] == 2 else ""),
                        "l2": (f"inputs larger than L2 (A, B, C = {w.algorithmic_bytes / 2**20:.0f} MiB > 129 MB), "
                               "no flush") if w.algorithmic_bytes > 129e6 else "inputs fit in L2: warm-L2 number",
                        "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU"},
@@ -360,6 +365,8 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD, help="c1..c5 (default c4, the headline workload)")
+    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
+                    help="kernel configuration (default: the library's own choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -1,6 +1,6 @@
-// Host side of the C ABI declared in include/gemm.h: argument validation, TMA
-// tensor-map encoding (cached per handle), the choice of kernel configuration and the
-// launch.  All arithmetic runs in the kernels of gemm_kernel.cuh.
+// Host side of the C ABI declared in include/gemm.h: argument validation, TMA tensor-map
+// encoding, the choice of kernel configuration and the launch.  All arithmetic runs in
+// the kernels of gemm_kernel.cuh / gemm_kernel_pair.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -13,6 +13,7 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
+#include "gemm_kernel_pair.cuh"
 
 namespace {
 
@@ -21,6 +22,8 @@ using dtg::KernelParams;
 constexpr int kGroupDefault = 16;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
+constexpr int kPairStages = 6;
+constexpr int kNumSlots = 12;  // 3 configurations x 2 dtypes x 2 layouts
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -55,11 +58,30 @@ struct TmapEntry {
     CUtensorMap map;
 };
 
+// Tunables a launch reads (a handle's options, or the defaults).
+struct LaunchOptions {
+    int64_t config = GEMM_CONFIG_AUTO;
+    int64_t timeout_ns = kTimeoutDefaultNs;
+    int64_t max_ctas = 0;
+    int64_t raster_group = kGroupDefault;
+    int64_t fault_inject = 0;
+};
+
+// Per-device facts and lazily-set per-kernel state.  Guarded by `mu`.
+struct DeviceState {
+    int num_sms = 0;
+    std::mutex mu;
+    bool attrs_set[kNumSlots] = {};
+    int max_clusters[kNumSlots] = {};  // pair kernels: co-resident clusters (0 = not yet queried)
+};
+
 // Which kernel instantiation a plan launches.
 struct KernelChoice {
     int config;
-    int bn;
+    int bm, bn;     // output tile of one CTA (1-CTA) or of the pair
+    int b_box;      // rows (TN) / columns (NN) of B one CTA loads per stage
     int stages;
+    int cluster;    // CTAs per cluster
     const void* fn;
     int smem;
 };
@@ -68,16 +90,11 @@ struct KernelChoice {
 
 struct gemm_handle_s {
     int device = 0;
-    int num_sms = 0;
     int32_t* d_err = nullptr;  // 4 ints
     int32_t last_info[4] = {0, 0, 0, 0};
-    int64_t config = GEMM_CONFIG_AUTO;
-    int64_t timeout_ns = kTimeoutDefaultNs;
-    int64_t max_ctas = 0;
-    int64_t raster_group = kGroupDefault;
-    int64_t fault_inject = 0;
+    LaunchOptions opts;
+    DeviceState dev;
     std::vector<TmapEntry> tmaps;
-    bool attrs_set[8] = {false, false, false, false, false, false, false, false};
     // gemm_run_host staging
     void* d_stage = nullptr;
     size_t stage_bytes = 0;
@@ -101,93 +118,139 @@ struct DeviceGuard {
     }
 };
 
-// Encode (or fetch) a 2-D row-major tensor map: `inner` contiguous elements per row,
-// `outer` rows `pitch_bytes` apart, box = box_inner x box_outer, 128-byte swizzle,
-// zero fill outside the tensor.
-bool get_tmap(gemm_handle_s* h, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
+// Encode a 2-D row-major tensor map: `inner` contiguous elements per row, `outer` rows
+// `pitch_bytes` apart, box = box_inner x box_outer, 128-byte swizzle, zero fill outside.
+// With a cache (a handle's), identical requests reuse the earlier encoding.
+bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
               uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out)
 {
     const TmapKey key{ptr, inner, outer, pitch_bytes, box_inner, box_outer, dtype};
-    for (const TmapEntry& e : h->tmaps)
-        if (e.key == key) {
-            *out = e.map;
-            return true;
-        }
+    if (cache)
+        for (const TmapEntry& e : *cache)
+            if (e.key == key) {
+                *out = e.map;
+                return true;
+            }
     if (!load_encode_fn()) return false;
-    CUtensorMap map;
     const cuuint64_t dims[2] = {inner, outer};
     const cuuint64_t strides[1] = {pitch_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     const CUtensorMapDataType dt =
         dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    const CUresult r = g_encode(&map, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-                                CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-    if (r != CUDA_SUCCESS) return false;
-    if (static_cast<int>(h->tmaps.size()) >= kTmapCacheMax) h->tmaps.clear();
-    h->tmaps.push_back({key, map});
-    *out = map;
+    if (g_encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+        return false;
+    if (cache) {
+        if (static_cast<int>(cache->size()) >= kTmapCacheMax) cache->clear();
+        cache->push_back({key, *out});
+    }
     return true;
-}
-
-template <int BN, int STAGES, bool BF16, bool NN>
-KernelChoice choice_of(int config)
-{
-    return {config, BN, STAGES, reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN>),
-            dtg::Smem<BN, STAGES>::kAlloc};
-}
-
-template <int BN, int STAGES>
-KernelChoice choice_for(int config, gemm_dtype_t dtype, gemm_layout_t layout)
-{
-    const bool bf16 = dtype == GEMM_DTYPE_BF16, nn = layout == GEMM_LAYOUT_NN;
-    if (bf16) return nn ? choice_of<BN, STAGES, true, true>(config) : choice_of<BN, STAGES, true, false>(config);
-    return nn ? choice_of<BN, STAGES, false, true>(config) : choice_of<BN, STAGES, false, false>(config);
 }
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-int pick_config(const gemm_handle_s* h, int64_t M, int64_t N)
+template <int BN, int STAGES, bool BF16, bool NN>
+KernelChoice one_cta_choice(int config)
 {
-    if (h->config == GEMM_CONFIG_128x256 || h->config == GEMM_CONFIG_128x128) return static_cast<int>(h->config);
-    // AUTO: the 128 x 256 tile unless it leaves most SMs idle, then 128 x 128.
-    const int64_t tiles256 = cdiv(M, 128) * cdiv(N, 256);
-    if (tiles256 < h->num_sms / 2) return GEMM_CONFIG_128x128;
-    return GEMM_CONFIG_128x256;
+    return {config, dtg::kBM, BN, BN, STAGES, 1,
+            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN>),
+            dtg::Smem<BN, STAGES>::kAlloc};
+}
+
+template <bool BF16, bool NN>
+KernelChoice pair_choice()
+{
+    return {GEMM_CONFIG_256x256, dtg::kPairBM, dtg::kPairBN, 128, kPairStages, 2,
+            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_pair_kernel<kPairStages, BF16, NN>),
+            dtg::PairSmem<kPairStages>::kAlloc};
+}
+
+template <bool BF16, bool NN>
+KernelChoice choice_typed(int config)
+{
+    if (config == GEMM_CONFIG_256x256) return pair_choice<BF16, NN>();
+    if (config == GEMM_CONFIG_128x128) return one_cta_choice<128, 6, BF16, NN>(config);
+    return one_cta_choice<256, 4, BF16, NN>(GEMM_CONFIG_128x256);
 }
 
 KernelChoice kernel_choice(int config, gemm_dtype_t dtype, gemm_layout_t layout)
 {
-    if (config == GEMM_CONFIG_128x128) return choice_for<128, 6>(config, dtype, layout);
-    return choice_for<256, 4>(config, dtype, layout);
+    const bool bf16 = dtype == GEMM_DTYPE_BF16, nn = layout == GEMM_LAYOUT_NN;
+    if (bf16) return nn ? choice_typed<true, true>(config) : choice_typed<true, false>(config);
+    return nn ? choice_typed<false, true>(config) : choice_typed<false, false>(config);
 }
 
-void fill_plan(const gemm_handle_s* h, int64_t M, int64_t N, int64_t K, const KernelChoice& kc, gemm_plan_t* plan)
+int slot_of(int config, gemm_dtype_t dtype, gemm_layout_t layout)
+{
+    const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
+    return c * 4 + (dtype == GEMM_DTYPE_BF16 ? 2 : 0) + (layout == GEMM_LAYOUT_NN ? 1 : 0);
+}
+
+// Opt the kernel into its shared memory and, for pair kernels, ask how many clusters can
+// be resident at once (the persistent grid never exceeds that).  Once per device and slot.
+gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int slot)
+{
+    std::lock_guard<std::mutex> lock(dev.mu);
+    if (!dev.attrs_set[slot]) {
+        if (cudaFuncSetAttribute(kc.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (kc.cluster > 1) {
+            cudaLaunchConfig_t cfg;
+            std::memset(&cfg, 0, sizeof(cfg));
+            cfg.gridDim = dim3(static_cast<unsigned>(kc.cluster * (dev.num_sms / kc.cluster)), 1, 1);
+            cfg.blockDim = dim3(dtg::kThreads, 1, 1);
+            cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
+            int n = 0;
+            if (cudaOccupancyMaxActiveClusters(&n, kc.fn, &cfg) != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
+            dev.max_clusters[slot] = n;
+        }
+        dev.attrs_set[slot] = true;
+    }
+    return GEMM_OK;
+}
+
+int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N)
+{
+    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256)
+        return static_cast<int>(o.config);
+    // AUTO: the 256 x 256 CTA-pair tile when there is at least one pair tile per pair of
+    // SMs (it halves each SM's shared-memory traffic for B); otherwise the 128 x 256 tile
+    // unless that leaves most SMs idle, then 128 x 128.
+    const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
+    if (pair_tiles >= dev.num_sms / 2) return GEMM_CONFIG_256x256;
+    const int64_t tiles256 = cdiv(M, 128) * cdiv(N, 256);
+    if (tiles256 < dev.num_sms / 2) return GEMM_CONFIG_128x128;
+    return GEMM_CONFIG_128x256;
+}
+
+void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters, int64_t M, int64_t N, int64_t K,
+               const KernelChoice& kc, gemm_plan_t* plan)
 {
     std::memset(plan, 0, sizeof(*plan));
     plan->config = kc.config;
-    plan->bm = dtg::kBM;
+    plan->bm = kc.bm;
     plan->bn = kc.bn;
     plan->bk = dtg::kBK;
     plan->stages = kc.stages;
-    plan->cluster = 1;
-    plan->tiles_m = cdiv(M, dtg::kBM);
+    plan->cluster = kc.cluster;
+    plan->tiles_m = cdiv(M, kc.bm);
     plan->tiles_n = cdiv(N, kc.bn);
     plan->k_blocks = cdiv(K, dtg::kBK);
     const int64_t tiles = plan->tiles_m * plan->tiles_n;
-    int64_t grid = h->num_sms > 0 ? h->num_sms : 1;
-    if (h->max_ctas > 0 && h->max_ctas < grid) grid = h->max_ctas;
-    if (tiles < grid) grid = tiles;
-    plan->grid = grid;
+    // Clusters (CTA pairs, or single CTAs) that can run at once, capped by the option.
+    int64_t units = kc.cluster > 1 ? (max_clusters > 0 ? max_clusters : dev.num_sms / kc.cluster)
+                                   : (dev.num_sms > 0 ? dev.num_sms : 1);
+    if (o.max_ctas > 0) {
+        const int64_t cap = o.max_ctas / kc.cluster;
+        units = cap < 1 ? 1 : (cap < units ? cap : units);
+    }
+    if (tiles < units) units = tiles;
+    if (units < 1) units = 1;
+    plan->grid = units * kc.cluster;
     plan->threads = dtg::kThreads;
     plan->smem_bytes = kc.smem;
-}
-
-int attr_slot(const KernelChoice& kc, gemm_dtype_t dtype, gemm_layout_t layout)
-{
-    return (kc.config == GEMM_CONFIG_128x128 ? 4 : 0) + (dtype == GEMM_DTYPE_BF16 ? 2 : 0) +
-           (layout == GEMM_LAYOUT_NN ? 1 : 0);
 }
 
 gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
@@ -222,14 +285,14 @@ gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void
     return validate_args(A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
 }
 
-gemm_status_t launch(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K,
-                     int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
-                     cudaStream_t stream)
+// Enqueue C = A·B (arguments already validated, M, N > 0) on the current device.
+gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, std::vector<TmapEntry>* cache, int32_t* err,
+                          const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                          int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream)
 {
     if (K == 0) {
-        const int64_t total = M * N;
-        int blocks = static_cast<int>(cdiv(total, 256));
-        const int cap = h->num_sms * 8;
+        int blocks = static_cast<int>(cdiv(M * N, 256));
+        const int cap = dev.num_sms * 8;
         if (blocks > cap) blocks = cap;
         if (dtype == GEMM_DTYPE_BF16)
             dtg::zero_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc);
@@ -238,27 +301,23 @@ gemm_status_t launch(gemm_handle_t h, const void* A, const void* B, void* C, int
         return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    const int config = pick_config(h, M, N);
+    const int config = pick_config(o, dev, M, N);
     const KernelChoice kc = kernel_choice(config, dtype, layout);
+    const int slot = slot_of(config, dtype, layout);
+    const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
+    if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
-    fill_plan(h, M, N, K, kc, &plan);
+    fill_plan(o, dev, dev.max_clusters[slot], M, N, K, kc, &plan);
 
     CUtensorMap tA, tB, tC;
     const bool nn = layout == GEMM_LAYOUT_NN;
-    if (!get_tmap(h, A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
+    if (!get_tmap(cache, A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
     if (nn) {
-        if (!get_tmap(h, B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)) return GEMM_ERR_CUDA;
+        if (!get_tmap(cache, B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)) return GEMM_ERR_CUDA;
     } else {
-        if (!get_tmap(h, B, K, N, ldb * 2, dtg::kBK, kc.bn, dtype, &tB)) return GEMM_ERR_CUDA;
+        if (!get_tmap(cache, B, K, N, ldb * 2, dtg::kBK, kc.b_box, dtype, &tB)) return GEMM_ERR_CUDA;
     }
-    if (!get_tmap(h, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
-
-    const int slot = attr_slot(kc, dtype, layout);
-    if (!h->attrs_set[slot]) {
-        if (cudaFuncSetAttribute(kc.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        h->attrs_set[slot] = true;
-    }
+    if (!get_tmap(cache, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
 
     KernelParams kp;
     kp.M = static_cast<int32_t>(M);
@@ -268,10 +327,10 @@ gemm_status_t launch(gemm_handle_t h, const void* A, const void* B, void* C, int
     kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
     kp.num_kb = static_cast<int32_t>(plan.k_blocks);
     kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
-    kp.group_m = static_cast<int32_t>(h->raster_group);
-    kp.fault_inject = static_cast<int32_t>(h->fault_inject);
-    kp.timeout_ns = static_cast<uint64_t>(h->timeout_ns);
-    kp.err = h->d_err;
+    kp.group_m = static_cast<int32_t>(o.raster_group);
+    kp.fault_inject = static_cast<int32_t>(o.fault_inject);
+    kp.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
+    kp.err = err;
     kp.C = C;
     kp.ldc = ldc;
 
@@ -301,6 +360,18 @@ gemm_status_t read_error_word(gemm_handle_t h, cudaStream_t stream)
     return GEMM_OK;
 }
 
+// Compute capability and SM count of `device`; ARCH unless it is sm_103.
+gemm_status_t query_device(int device, int* sms)
+{
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
+        cudaDeviceGetAttribute(sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
+    return GEMM_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -315,18 +386,15 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device)
         return GEMM_ERR_CUDA;
     }
     if (device < 0 || device >= count) return GEMM_ERR_INVALID_ARG;
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
+    int sms = 0;
+    const gemm_status_t q = query_device(device, &sms);
+    if (q != GEMM_OK) return q;
     DeviceGuard g(device);
     if (!g.ok) return GEMM_ERR_CUDA;
     gemm_handle_s* h = new (std::nothrow) gemm_handle_s();
     if (!h) return GEMM_ERR_CUDA;
     h->device = device;
-    h->num_sms = sms;
+    h->dev.num_sms = sms;
     if (cudaMalloc(&h->d_err, 4 * sizeof(int32_t)) != cudaSuccess ||
         cudaMemset(h->d_err, 0, 4 * sizeof(int32_t)) != cudaSuccess) {
         if (h->d_err) cudaFree(h->d_err);
@@ -359,7 +427,8 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
     if (v != GEMM_OK || M == 0 || N == 0) return v;
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
-    return launch(h, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype, static_cast<cudaStream_t>(stream));
+    return launch_gemm(h->opts, h->dev, &h->tmaps, h->d_err, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype,
+                       static_cast<cudaStream_t>(stream));
 }
 
 gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,
@@ -403,7 +472,8 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
             cudaSuccess)
             return GEMM_ERR_CUDA;
     }
-    const gemm_status_t st = launch(h, dA, dB, dC, M, N, K, dlda, dldb, dldc, layout, dtype, s);
+    const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->tmaps, h->d_err, dA, dB, dC, M, N, K, dlda, dldb,
+                                         dldc, layout, dtype, s);
     if (st != GEMM_OK) return st;
     if (cudaMemcpy2DAsync(C, ldc * 2, dC, dldc * 2, N * 2, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -428,27 +498,29 @@ gemm_status_t gemm_error_info(gemm_handle_t h, int32_t info[4])
 gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
 {
     if (!h) return GEMM_ERR_INVALID_ARG;
+    LaunchOptions& o = h->opts;
     switch (opt) {
     case GEMM_OPT_CONFIG:
-        if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128)
-            return value == GEMM_CONFIG_256x256 ? GEMM_ERR_UNSUPPORTED : GEMM_ERR_INVALID_ARG;
-        h->config = value;
+        if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128 &&
+            value != GEMM_CONFIG_256x256)
+            return GEMM_ERR_INVALID_ARG;
+        o.config = value;
         return GEMM_OK;
     case GEMM_OPT_TIMEOUT_NS:
         if (value < 1000000) return GEMM_ERR_INVALID_ARG;
-        h->timeout_ns = value;
+        o.timeout_ns = value;
         return GEMM_OK;
     case GEMM_OPT_MAX_CTAS:
         if (value < 0) return GEMM_ERR_INVALID_ARG;
-        h->max_ctas = value;
+        o.max_ctas = value;
         return GEMM_OK;
     case GEMM_OPT_RASTER_GROUP:
         if (value < 1 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
-        h->raster_group = value;
+        o.raster_group = value;
         return GEMM_OK;
     case GEMM_OPT_FAULT_INJECT:
         if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
-        h->fault_inject = value;
+        o.fault_inject = value;
         return GEMM_OK;
     default:
         return GEMM_ERR_INVALID_ARG;
@@ -458,12 +530,13 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
 gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value)
 {
     if (!h || !value) return GEMM_ERR_INVALID_ARG;
+    const LaunchOptions& o = h->opts;
     switch (opt) {
-    case GEMM_OPT_CONFIG: *value = h->config; return GEMM_OK;
-    case GEMM_OPT_TIMEOUT_NS: *value = h->timeout_ns; return GEMM_OK;
-    case GEMM_OPT_MAX_CTAS: *value = h->max_ctas; return GEMM_OK;
-    case GEMM_OPT_RASTER_GROUP: *value = h->raster_group; return GEMM_OK;
-    case GEMM_OPT_FAULT_INJECT: *value = h->fault_inject; return GEMM_OK;
+    case GEMM_OPT_CONFIG: *value = o.config; return GEMM_OK;
+    case GEMM_OPT_TIMEOUT_NS: *value = o.timeout_ns; return GEMM_OK;
+    case GEMM_OPT_MAX_CTAS: *value = o.max_ctas; return GEMM_OK;
+    case GEMM_OPT_RASTER_GROUP: *value = o.raster_group; return GEMM_OK;
+    case GEMM_OPT_FAULT_INJECT: *value = o.fault_inject; return GEMM_OK;
     default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -474,8 +547,14 @@ gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     if (!h || !plan || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
     if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
-    const KernelChoice kc = kernel_choice(pick_config(h, M, N), dtype, layout);
-    fill_plan(h, M, N, K, kc, plan);
+    const int config = pick_config(h->opts, h->dev, M, N);
+    const KernelChoice kc = kernel_choice(config, dtype, layout);
+    const int slot = slot_of(config, dtype, layout);
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);
+    if (ready != GEMM_OK) return ready;
+    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], M, N, K, kc, plan);
     return GEMM_OK;
 }
 
@@ -520,8 +599,8 @@ int32_t gemm_api_version(void) { return GEMM_API_VERSION; }
 // array below instead.  Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 namespace {
 
-constexpr size_t kNoallocScratchBytes = 256;                    // stated maximum
-constexpr size_t kNoallocRecordBytes = 4 * sizeof(int32_t);     // what the kernel writes
+constexpr size_t kNoallocScratchBytes = 256;                 // stated maximum
+constexpr size_t kNoallocRecordBytes = 4 * sizeof(int32_t);  // what the kernel writes
 constexpr int kNoallocMaxDevices = 64;
 
 // One copy per device, kept until the process exits.  On the host this name is only a
@@ -532,9 +611,7 @@ struct NoallocDevice {
     std::once_flag once;
     gemm_status_t setup = GEMM_ERR_CUDA;
     int32_t* scratch = nullptr;  // device address of g_noalloc_scratch on this device
-    int num_sms = 0;
-    std::mutex mu;               // guards attrs_set
-    bool attrs_set[8] = {false, false, false, false, false, false, false, false};
+    DeviceState dev;
 };
 
 NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
@@ -542,41 +619,17 @@ NoallocDevice g_noalloc_devices[kNoallocMaxDevices];
 // Runs once per device, with that device current (the caller's current device).
 void noalloc_setup(NoallocDevice& d, int device)
 {
-    int major = 0, minor = 0, sms = 0;
-    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, device) != cudaSuccess ||
-        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, device) != cudaSuccess) {
-        d.setup = GEMM_ERR_CUDA;
-        return;
-    }
-    if (major != 10 || minor != 3) {
-        d.setup = GEMM_ERR_ARCH;
-        return;
-    }
+    int sms = 0;
+    d.setup = query_device(device, &sms);
+    if (d.setup != GEMM_OK) return;
     void* addr = nullptr;
     if (cudaGetSymbolAddress(&addr, g_noalloc_scratch) != cudaSuccess || addr == nullptr) {
         d.setup = GEMM_ERR_CUDA;
         return;
     }
     d.scratch = static_cast<int32_t*>(addr);
-    d.num_sms = sms;
+    d.dev.num_sms = sms;
     d.setup = GEMM_OK;
-}
-
-// Tensor-map encoding without the handle's cache (host-only work, no allocation).
-bool encode_tmap_uncached(const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-                          uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out)
-{
-    if (!load_encode_fn()) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {pitch_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
-    return g_encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                    CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 }  // namespace
@@ -600,62 +653,10 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     // The record keeps the previous call's contents: clear it before this launch.
     if (cudaMemsetAsync(d.scratch, 0, kNoallocRecordBytes, s) != cudaSuccess) return GEMM_ERR_CUDA;
-
-    if (K == 0) {
-        int blocks = static_cast<int>(cdiv(M * N, 256));
-        if (blocks > d.num_sms * 8) blocks = d.num_sms * 8;
-        if (dtype == GEMM_DTYPE_BF16)
-            dtg::zero_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, s>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc);
-        else
-            dtg::zero_fill_kernel<__half><<<blocks, 256, 0, s>>>(static_cast<__half*>(C), M, N, ldc);
-        if (cudaPeekAtLastError() != cudaSuccess) return GEMM_ERR_CUDA;
-    } else {
-        gemm_handle_s opts;  // default options; only num_sms is read by the planners
-        opts.num_sms = d.num_sms;
-        const int config = pick_config(&opts, M, N);
-        const KernelChoice kc = kernel_choice(config, dtype, layout);
-        gemm_plan_t plan;
-        fill_plan(&opts, M, N, K, kc, &plan);
-
-        CUtensorMap tA, tB, tC;
-        const bool nn = layout == GEMM_LAYOUT_NN;
-        if (!encode_tmap_uncached(A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
-        if (nn ? !encode_tmap_uncached(B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)
-               : !encode_tmap_uncached(B, K, N, ldb * 2, dtg::kBK, kc.bn, dtype, &tB))
-            return GEMM_ERR_CUDA;
-        if (!encode_tmap_uncached(C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
-        {
-            std::lock_guard<std::mutex> lock(d.mu);
-            const int slot = attr_slot(kc, dtype, layout);
-            if (!d.attrs_set[slot]) {
-                if (cudaFuncSetAttribute(kc.fn, cudaFuncAttributeMaxDynamicSharedMemorySize, kc.smem) != cudaSuccess)
-                    return GEMM_ERR_CUDA;
-                d.attrs_set[slot] = true;
-            }
-        }
-        KernelParams kp;
-        kp.M = static_cast<int32_t>(M);
-        kp.N = static_cast<int32_t>(N);
-        kp.K = static_cast<int32_t>(K);
-        kp.tiles_m = static_cast<int32_t>(plan.tiles_m);
-        kp.tiles_n = static_cast<int32_t>(plan.tiles_n);
-        kp.num_kb = static_cast<int32_t>(plan.k_blocks);
-        kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
-        kp.group_m = static_cast<int32_t>(opts.raster_group);
-        kp.fault_inject = 0;
-        kp.timeout_ns = static_cast<uint64_t>(opts.timeout_ns);
-        kp.err = d.scratch;
-        kp.C = C;
-        kp.ldc = ldc;
-        void* args[] = {&tA, &tB, &tC, &kp};
-        cudaLaunchConfig_t cfg;
-        std::memset(&cfg, 0, sizeof(cfg));
-        cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
-        cfg.blockDim = dim3(dtg::kThreads, 1, 1);
-        cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
-        cfg.stream = s;
-        if (cudaLaunchKernelExC(&cfg, kc.fn, args) != cudaSuccess) return GEMM_ERR_CUDA;
-    }
+    const LaunchOptions defaults;
+    const gemm_status_t st =
+        launch_gemm(defaults, d.dev, nullptr, d.scratch, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype, s);
+    if (st != GEMM_OK) return st;
 
     if (watchdog_info) {
         int32_t info[4] = {0, 0, 0, 0};

@@ -128,10 +128,12 @@ __host__ __device__ constexpr uint32_t idesc_f16()
 struct Watchdog {
     volatile int32_t* abort_flag;  // shared memory
     const KernelParams* p;
+    uint32_t peer_abort = 0;       // shared::cluster address of the peer CTA's flag (CTA pairs), or 0
 
     __device__ __forceinline__ void fail(int role, int64_t tile, int kb) const
     {
         *abort_flag = 1;
+        if (peer_abort) ptx::st_shared_cluster_u32(peer_abort, 1u);
         if (atomicCAS(p->err, 0, 1) == 0) {
             p->err[1] = role;
             p->err[2] = static_cast<int32_t>(blockIdx.x);
@@ -183,6 +185,65 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
         __half2 v = __floats2half2_rn(lo, hi);
         return *reinterpret_cast<uint32_t*>(&v);
     }
+}
+
+// Write the 32-row x 64-column box of C at (row y, column x) that this warp holds (lane =
+// row, v = the 64 fp32 accumulator bit patterns of that row).  Normally the box goes
+// through a 128-byte-swizzled staging buffer and one TMA store, which drops rows >= M and
+// columns >= N (the masked write-back of "NineToothed GEMM 语法入门" §5).  A TMA store clips the inner dimension only
+// to 16-byte granules, so when N is not a multiple of 8 the box that straddles column N
+// is written with plain masked stores instead.  Returns true if the staging buffer was
+// used (the caller then alternates buffers).
+template <bool BF16>
+__device__ __forceinline__ bool store_box(const uint32_t (&v)[64], int32_t x, int32_t y, int lane,
+                                          uint32_t stg, const CUtensorMap* tmC, const KernelParams& p)
+{
+    if ((p.N & 7) != 0 && x + kEpiCols > p.N) {
+        const int64_t row = static_cast<int64_t>(y) + lane;
+        if (row < p.M && x < p.N) {
+            uint16_t* crow = static_cast<uint16_t*>(p.C) + row * p.ldc;
+#pragma unroll
+            for (int ch = 0; ch < 8; ++ch) {
+                const int32_t col = x + ch * 8;
+                if (col + 8 <= p.N) {  // a whole 16-byte chunk: one vector store
+                    uint4 q;
+                    q.x = pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]);
+                    q.y = pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]);
+                    q.z = pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]);
+                    q.w = pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]);
+                    *reinterpret_cast<uint4*>(crow + col) = q;
+                } else {
+#pragma unroll
+                    for (int e = 0; e < 8; e += 2) {
+                        const uint32_t two = pack2<BF16>(v[8 * ch + e], v[8 * ch + e + 1]);
+                        if (col + e < p.N) crow[col + e] = static_cast<uint16_t>(two & 0xFFFFu);
+                        if (col + e + 1 < p.N) crow[col + e + 1] = static_cast<uint16_t>(two >> 16);
+                    }
+                }
+            }
+        }
+        return false;
+    }
+    // The staging buffer is reusable once the store issued from it two boxes ago has
+    // finished reading it.
+    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    __syncwarp();
+    const uint32_t row = stg + lane * 128;
+#pragma unroll
+    for (int ch = 0; ch < 8; ++ch) {
+        // 16-byte chunk ch of this row lands at chunk (ch ^ row%8): the 128-byte swizzle
+        // the TMA store expects.
+        const uint32_t addr = row + ((ch ^ (lane & 7)) << 4);
+        ptx::st_shared_v4(addr, pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]), pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]),
+                          pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]), pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]));
+    }
+    ptx::fence_proxy_async_smem();
+    __syncwarp();
+    if (lane == 0) {
+        if (x < p.N && y < p.M) ptx::tma_store_2d(tmC, stg, x, y);
+        ptx::bulk_commit_group();
+    }
+    return true;
 }
 
 template <int BN, int STAGES, bool BF16, bool B_MN_MAJOR>
@@ -276,6 +337,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         stage = 0;
                         phase ^= 1u;
                     }
+                }
+            }
+            // Tail: wait (bounded) until the MMA thread has released every stage this
+            // producer filled, so no tcgen05.commit arrival is still heading for this
+            // CTA's barriers when it leaves.
+            for (int i = 0; i < STAGES; ++i) {
+                if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, -1, i)) break;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
                 }
             }
         producer_done:
@@ -383,57 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int i = 0; i < 64; ++i) v[i] = 0u;  // K == 0: the empty sum
                 }
                 const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                if ((p.N & 7) != 0 && x + kEpiCols > p.N) {
-                    // Ragged right edge with N not a multiple of 8: a TMA store clips only at
-                    // 16-byte granularity and would write C's row padding, so this box is
-                    // written with plain masked stores (one row per thread).
-                    const int64_t row = static_cast<int64_t>(y) + lane;
-                    if (row < p.M && x < p.N) {
-                        uint16_t* crow = static_cast<uint16_t*>(p.C) + row * p.ldc;
-#pragma unroll
-                        for (int ch = 0; ch < 8; ++ch) {
-                            const int32_t col = x + ch * 8;
-                            if (col + 8 <= p.N) {  // a whole 16-byte chunk: one vector store
-                                uint4 q;
-                                q.x = pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]);
-                                q.y = pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]);
-                                q.z = pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]);
-                                q.w = pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]);
-                                *reinterpret_cast<uint4*>(crow + col) = q;
-                            } else {
-#pragma unroll
-                                for (int e = 0; e < 8; e += 2) {
-                                    const uint32_t two = pack2<BF16>(v[8 * ch + e], v[8 * ch + e + 1]);
-                                    if (col + e < p.N) crow[col + e] = static_cast<uint16_t>(two & 0xFFFFu);
-                                    if (col + e + 1 < p.N) crow[col + e + 1] = static_cast<uint16_t>(two >> 16);
-                                }
-                            }
-                        }
-                    }
-                    continue;
-                }
-                // The staging buffer is reusable once the store issued from it two boxes
-                // ago has finished reading it.
-                if (lane == 0) ptx::bulk_wait_group_read<1>();
-                __syncwarp();
-                const uint32_t row = stg0 + sbuf * kStgBytes + lane * 128;
-#pragma unroll
-                for (int ch = 0; ch < 8; ++ch) {
-                    // 16-byte chunk ch of this row lands at chunk (ch ^ row%8): the
-                    // 128-byte swizzle the TMA store expects.
-                    const uint32_t addr = row + ((ch ^ (lane & 7)) << 4);
-                    ptx::st_shared_v4(addr, pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]),
-                                      pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]),
-                                      pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]),
-                                      pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]));
-                }
-                ptx::fence_proxy_async_smem();
-                __syncwarp();
-                if (lane == 0) {
-                    if (x < p.N && y < p.M) ptx::tma_store_2d(&tmC, stg0 + sbuf * kStgBytes, x, y);
-                    ptx::bulk_commit_group();
-                }
-                sbuf ^= 1;
+                if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
             }
             if (num_kb > 0 && ++acc == 2) {
                 acc = 0;

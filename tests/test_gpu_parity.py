@@ -129,12 +129,17 @@ def test_small_workloads_full(g, name, dist):
 
 @pytest.mark.parametrize("name", ["c3", "c4", "c5"])
 @pytest.mark.parametrize("dist", ["workload", "int"])
-def test_full_size_workloads_sampled(g, name, dist):
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256])
+def test_full_size_workloads_sampled(g, name, dist, config):
     w = WORKLOADS[name]
     if dist == "int":
         w = w.with_dist("int")
     A, B = workload_inputs(w)
-    got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    g.set_option(native.OPT_CONFIG, config)
+    try:
+        got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
     rows = sample_rows(w.M, 24 if w.M * w.N * w.K < 2**40 else 12, seed=w.seed)
     ref, _, _ = oracle.gemm_rows(A, B, w.layout, w.dtype, rows)
     if dist == "int":
@@ -155,7 +160,7 @@ SHAPES = [(1, 1, 1), (1, 8, 3), (3, 5, 7), (8, 8, 8), (17, 9, 33), (64, 64, 64),
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128])
+@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256])
 def test_ragged_shapes(g, layout, dtype, config):
     g.set_option(native.OPT_CONFIG, config)
     try:
@@ -237,19 +242,34 @@ def native_dtype(dtype):
     return {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
 
 
-def test_several_tiles_per_cta_and_raster_groups(g):
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256])
+@pytest.mark.parametrize("layout", ["TN", "NN"])
+def test_several_tiles_per_cta_and_raster_groups(g, config, layout):
     M, N, K = 1000, 1000, 520
-    A, B = make_inputs(M, N, K, "TN", "f16", "int", seed=5)
-    ref = oracle.gemm(A, B, "TN", "f16")
+    A, B = make_inputs(M, N, K, layout, "f16", "int", seed=5)
+    ref = oracle.gemm(A, B, layout, "f16")
+    g.set_option(native.OPT_CONFIG, config)
     try:
-        for max_ctas, group in [(1, 16), (3, 1), (7, 3), (0, 64), (5, 1000)]:
+        for max_ctas, group in [(1, 16), (3, 1), (7, 3), (0, 64), (5, 1000), (2, 2)]:
             g.set_option(native.OPT_MAX_CTAS, max_ctas)
             g.set_option(native.OPT_RASTER_GROUP, group)
-            got, _ = gpu_gemm(g, A, B, "TN", "f16")
-            assert_exact(got, ref, f"max_ctas={max_ctas} group={group}")
+            got, _ = gpu_gemm(g, A, B, layout, "f16")
+            assert_exact(got, ref, f"cfg{config} max_ctas={max_ctas} group={group}")
     finally:
         g.set_option(native.OPT_MAX_CTAS, 0)
         g.set_option(native.OPT_RASTER_GROUP, 16)
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+
+
+def test_plan_reports_pair_clusters(g):
+    g.set_option(native.OPT_CONFIG, native.CONFIG_256x256)
+    try:
+        pl = g.plan(8192, 8192, 8192, "TN", "bf16")
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+    assert pl["cluster"] == 2 and pl["bm"] == 256 and pl["bn"] == 256
+    assert pl["grid"] % 2 == 0 and 2 <= pl["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count
+    assert pl["tiles_m"] == 32 and pl["tiles_n"] == 32 and pl["k_blocks"] == 128
 
 
 def test_large_extents(g):
@@ -302,11 +322,13 @@ def test_run_host_matches_oracle(g):
     assert_close(codes(C), oracle.gemm(A, B, w.layout, w.dtype), w.dtype, "run_host")
 
 
-def test_watchdog_timeout_is_reported_and_context_survives(g):
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256])
+def test_watchdog_timeout_is_reported_and_context_survives(g, config):
     # One ring stage is left unarmed in CTA 0: the MMA thread's wait on it must run out,
     # the kernel must leave cleanly, and the host must read GEMM_ERR_TIMEOUT.
     w = WORKLOADS["c2"].with_dist("int")
     A, B = workload_inputs(w)
+    g.set_option(native.OPT_CONFIG, config)
     g.set_option(native.OPT_TIMEOUT_NS, 50_000_000)
     g.set_option(native.OPT_FAULT_INJECT, 1)
     try:
@@ -322,5 +344,8 @@ def test_watchdog_timeout_is_reported_and_context_survives(g):
         g.set_option(native.OPT_FAULT_INJECT, 0)
         g.set_option(native.OPT_TIMEOUT_NS, 2_000_000_000)
     # The context is still usable and the next run is correct.
-    got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    try:
+        got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
     assert_exact(got, oracle.gemm(A, B, w.layout, w.dtype), "after timeout")
