@@ -49,6 +49,8 @@ constexpr int kEpiWarps = 4;
 constexpr int kEpiCols = 64;                        // columns per staged TMA store box
 constexpr int kStgBytes = 32 * kEpiCols * 2;        // one warp's 32 x 64 box, 4 KB
 
+constexpr uint32_t kWaitSleepNs = 20000;           // longest single suspension of a waiting thread
+
 // Error-word roles.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3;
 
@@ -148,14 +150,14 @@ struct Watchdog {
     {
         if (ptx::mbar_try_wait(bar, parity)) return true;
         const uint64_t t0 = ptx::globaltimer_ns();
-        for (uint32_t n = 1;; ++n) {
-            if (ptx::mbar_try_wait(bar, parity)) return true;
-            if ((n & 15u) == 0) {
-                if (*abort_flag) return false;
-                if (ptx::globaltimer_ns() - t0 > p->timeout_ns) {
-                    fail(role, tile, kb);
-                    return false;
-                }
+        for (;;) {
+            // Sleep until the phase completes (or kWaitSleepNs passes): a waiting warp must
+            // not take issue slots from the producer and MMA warps on its scheduler.
+            if (ptx::mbar_try_wait_sleep(bar, parity, kWaitSleepNs)) return true;
+            if (*abort_flag) return false;
+            if (ptx::globaltimer_ns() - t0 > p->timeout_ns) {
+                fail(role, tile, kb);
+                return false;
             }
         }
     }
