@@ -5,7 +5,8 @@ The compute path is the CUDA library ``libdtgemm.so`` behind the C ABI in
 memory and streams only.
 """
 from .native import (CONFIG_128x128, CONFIG_128x256, CONFIG_256x256, CONFIG_AUTO, Gemm, GemmError, LAYOUT_NN,
-                     LAYOUT_TN, OPT_CONFIG, OPT_FAULT_INJECT, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_TIMEOUT_NS,
+                     LAYOUT_TN, OPT_CONFIG, OPT_FAULT_INJECT, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_STREAM_K,
+                     OPT_TIMEOUT_NS,
                      empty_output, load, matmul)
 
 __all__ = ["Gemm", "GemmError", "matmul", "load", "empty_output", "LAYOUT_NN", "LAYOUT_TN", "OPT_CONFIG",

@@ -1,6 +1,6 @@
 // Host side of the C ABI declared in include/gemm.h: argument validation, TMA tensor-map
 // encoding, the choice of kernel configuration and the launch.  All arithmetic runs in
-// the kernels of gemm_kernel.cuh / gemm_kernel_pair.cuh.
+// the kernels of gemm_kernel.cuh.
 #include <cuda.h>
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
@@ -13,7 +13,6 @@
 
 #include "gemm.h"
 #include "gemm_kernel.cuh"
-#include "gemm_kernel_pair.cuh"
 
 namespace {
 
@@ -24,6 +23,7 @@ constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int kPairStages = 6;
 constexpr int kNumSlots = 12;  // 3 configurations x 2 dtypes x 2 layouts
+constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -65,6 +65,7 @@ struct LaunchOptions {
     int64_t max_ctas = 0;
     int64_t raster_group = kGroupDefault;
     int64_t fault_inject = 0;
+    int64_t stream_k = 1;
 };
 
 // Per-device facts and lazily-set per-kernel state.  Guarded by `mu`.
@@ -86,6 +87,14 @@ struct KernelChoice {
     int smem;
 };
 
+// Stream-K workspace: fp32 partial sums and arrival counters (see gemm_kernel.cuh).
+struct Workspace {
+    float* partials = nullptr;
+    int32_t* counters = nullptr;
+    size_t partial_floats = 0;  // capacity
+    int64_t counter_count = 0;  // capacity
+};
+
 }  // namespace
 
 struct gemm_handle_s {
@@ -94,6 +103,7 @@ struct gemm_handle_s {
     int32_t last_info[4] = {0, 0, 0, 0};
     LaunchOptions opts;
     DeviceState dev;
+    Workspace ws;
     std::vector<TmapEntry> tmaps;
     // gemm_run_host staging
     void* d_stage = nullptr;
@@ -155,16 +165,16 @@ template <int BN, int STAGES, bool BF16, bool NN>
 KernelChoice one_cta_choice(int config)
 {
     return {config, dtg::kBM, BN, BN, STAGES, 1,
-            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN>),
+            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN, false>),
             dtg::Smem<BN, STAGES>::kAlloc};
 }
 
 template <bool BF16, bool NN>
 KernelChoice pair_choice()
 {
-    return {GEMM_CONFIG_256x256, dtg::kPairBM, dtg::kPairBN, 128, kPairStages, 2,
-            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_pair_kernel<kPairStages, BF16, NN>),
-            dtg::PairSmem<kPairStages>::kAlloc};
+    return {GEMM_CONFIG_256x256, 2 * dtg::kBM, 256, 128, kPairStages, 2,
+            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<256, kPairStages, BF16, NN, true>),
+            dtg::Smem<128, kPairStages>::kAlloc};
 }
 
 template <bool BF16, bool NN>
@@ -202,6 +212,13 @@ gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int 
             cfg.gridDim = dim3(static_cast<unsigned>(kc.cluster * (dev.num_sms / kc.cluster)), 1, 1);
             cfg.blockDim = dim3(dtg::kThreads, 1, 1);
             cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
+            cudaLaunchAttribute attr;
+            attr.id = cudaLaunchAttributeClusterDimension;
+            attr.val.clusterDim.x = static_cast<unsigned>(kc.cluster);
+            attr.val.clusterDim.y = 1;
+            attr.val.clusterDim.z = 1;
+            cfg.attrs = &attr;
+            cfg.numAttrs = 1;
             int n = 0;
             if (cudaOccupancyMaxActiveClusters(&n, kc.fn, &cfg) != cudaSuccess || n <= 0) return GEMM_ERR_CUDA;
             dev.max_clusters[slot] = n;
@@ -225,8 +242,17 @@ int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64
     return GEMM_CONFIG_128x256;
 }
 
-void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters, int64_t M, int64_t N, int64_t K,
-               const KernelChoice& kc, gemm_plan_t* plan)
+// Workspace a stream-K plan with `units` work units needs (see the kernel's slot layout).
+size_t sk_partial_floats(int64_t units, const KernelChoice& kc)
+{
+    return static_cast<size_t>(2 * units) * static_cast<size_t>(kc.cluster) * dtg::kBM * static_cast<size_t>(kc.bn);
+}
+
+int64_t sk_counter_count(int64_t sk_tiles, const KernelChoice& kc) { return sk_tiles * kc.cluster; }
+
+// `ws` == nullptr: no workspace, every tile is done whole (data-parallel).
+void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters, const Workspace* ws, int64_t M,
+               int64_t N, int64_t K, const KernelChoice& kc, gemm_plan_t* plan)
 {
     std::memset(plan, 0, sizeof(*plan));
     plan->config = kc.config;
@@ -246,8 +272,23 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
         const int64_t cap = o.max_ctas / kc.cluster;
         units = cap < 1 ? 1 : (cap < units ? cap : units);
     }
-    if (tiles < units) units = tiles;
     if (units < 1) units = 1;
+    plan->dp_tiles = tiles;
+    // Stream-K when whole tiles would leave the last wave part-empty: every unit does
+    // (full waves - 1) whole tiles, then an equal share of the K blocks of the rest.
+    if (ws && o.stream_k && tiles % units != 0) {
+        const int64_t dp = tiles >= units ? (tiles / units - 1) * units : 0;
+        const int64_t sk_tiles = tiles - dp;
+        const int64_t sk_blocks = sk_tiles * plan->k_blocks;
+        const int64_t base = sk_blocks / units;
+        if (base >= kMinStreamKBlocks && sk_partial_floats(units, kc) <= ws->partial_floats &&
+            sk_counter_count(sk_tiles, kc) <= ws->counter_count) {
+            plan->dp_tiles = dp;
+            plan->sk_base = base;
+            plan->sk_extra = sk_blocks % units;
+        }
+    }
+    if (plan->dp_tiles == tiles && tiles < units) units = tiles;  // whole tiles only: no idle units
     plan->grid = units * kc.cluster;
     plan->threads = dtg::kThreads;
     plan->smem_bytes = kc.smem;
@@ -286,7 +327,9 @@ gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void
 }
 
 // Enqueue C = A·B (arguments already validated, M, N > 0) on the current device.
-gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, std::vector<TmapEntry>* cache, int32_t* err,
+// `ws` == nullptr restricts the schedule to whole tiles (no stream-K workspace).
+gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Workspace* ws,
+                          std::vector<TmapEntry>* cache, int32_t* err,
                           const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
                           int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream)
 {
@@ -307,7 +350,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, std::vector<
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
     if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
-    fill_plan(o, dev, dev.max_clusters[slot], M, N, K, kc, &plan);
+    fill_plan(o, dev, dev.max_clusters[slot], ws, M, N, K, kc, &plan);
 
     CUtensorMap tA, tB, tC;
     const bool nn = layout == GEMM_LAYOUT_NN;
@@ -333,6 +376,11 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, std::vector<
     kp.err = err;
     kp.C = C;
     kp.ldc = ldc;
+    kp.dp_tiles = static_cast<int32_t>(plan.dp_tiles);
+    kp.sk_base = plan.sk_base;
+    kp.sk_extra = plan.sk_extra;
+    kp.ws = ws ? ws->partials : nullptr;
+    kp.counters = ws ? ws->counters : nullptr;
 
     void* args[] = {&tA, &tB, &tC, &kp};
     cudaLaunchConfig_t cfg;
@@ -341,6 +389,15 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, std::vector<
     cfg.blockDim = dim3(dtg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
     cfg.stream = stream;
+    cudaLaunchAttribute attr;
+    if (kc.cluster > 1) {
+        attr.id = cudaLaunchAttributeClusterDimension;
+        attr.val.clusterDim.x = static_cast<unsigned>(kc.cluster);
+        attr.val.clusterDim.y = 1;
+        attr.val.clusterDim.z = 1;
+        cfg.attrs = &attr;
+        cfg.numAttrs = 1;
+    }
     if (cudaLaunchKernelExC(&cfg, kc.fn, args) != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_OK;
 }
@@ -354,6 +411,11 @@ gemm_status_t read_error_word(gemm_handle_t h, cudaStream_t stream)
     if (info[0] != 0) {
         std::memcpy(h->last_info, info, sizeof(info));
         if (cudaMemsetAsync(h->d_err, 0, sizeof(info), stream) != cudaSuccess) return GEMM_ERR_CUDA;
+        // An abandoned launch may have left stream-K arrival counters part-way.
+        if (h->ws.counters &&
+            cudaMemsetAsync(h->ws.counters, 0, static_cast<size_t>(h->ws.counter_count) * sizeof(int32_t), stream) !=
+                cudaSuccess)
+            return GEMM_ERR_CUDA;
         if (cudaStreamSynchronize(stream) != cudaSuccess) return GEMM_ERR_CUDA;
         return GEMM_ERR_TIMEOUT;
     }
@@ -395,9 +457,19 @@ gemm_status_t gemm_create(gemm_handle_t* out, int device)
     if (!h) return GEMM_ERR_CUDA;
     h->device = device;
     h->dev.num_sms = sms;
+    // Stream-K workspace, sized for the largest plan any configuration makes on this
+    // device: 2 slots per work unit of 128 x 256 fp32 per CTA, and an arrival counter per
+    // stream-K tile (at most two waves of tiles) and CTA.
+    h->ws.partial_floats = static_cast<size_t>(2 * sms) * dtg::kBM * 256;
+    h->ws.counter_count = 4 * static_cast<int64_t>(sms);
     if (cudaMalloc(&h->d_err, 4 * sizeof(int32_t)) != cudaSuccess ||
-        cudaMemset(h->d_err, 0, 4 * sizeof(int32_t)) != cudaSuccess) {
+        cudaMemset(h->d_err, 0, 4 * sizeof(int32_t)) != cudaSuccess ||
+        cudaMalloc(&h->ws.partials, h->ws.partial_floats * sizeof(float)) != cudaSuccess ||
+        cudaMalloc(&h->ws.counters, static_cast<size_t>(h->ws.counter_count) * sizeof(int32_t)) != cudaSuccess ||
+        cudaMemset(h->ws.counters, 0, static_cast<size_t>(h->ws.counter_count) * sizeof(int32_t)) != cudaSuccess) {
         if (h->d_err) cudaFree(h->d_err);
+        if (h->ws.partials) cudaFree(h->ws.partials);
+        if (h->ws.counters) cudaFree(h->ws.counters);
         delete h;
         return GEMM_ERR_CUDA;
     }
@@ -414,6 +486,8 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
         if (cudaDeviceSynchronize() != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->d_err && cudaFree(h->d_err) != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->d_stage && cudaFree(h->d_stage) != cudaSuccess) st = GEMM_ERR_CUDA;
+        if (h->ws.partials && cudaFree(h->ws.partials) != cudaSuccess) st = GEMM_ERR_CUDA;
+        if (h->ws.counters && cudaFree(h->ws.counters) != cudaSuccess) st = GEMM_ERR_CUDA;
     }
     delete h;
     return st;
@@ -427,7 +501,7 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
     if (v != GEMM_OK || M == 0 || N == 0) return v;
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
-    return launch_gemm(h->opts, h->dev, &h->tmaps, h->d_err, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype,
+    return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype,
                        static_cast<cudaStream_t>(stream));
 }
 
@@ -472,8 +546,8 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
             cudaSuccess)
             return GEMM_ERR_CUDA;
     }
-    const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->tmaps, h->d_err, dA, dB, dC, M, N, K, dlda, dldb,
-                                         dldc, layout, dtype, s);
+    const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, dA, dB, dC, M, N, K, dlda,
+                                         dldb, dldc, layout, dtype, s);
     if (st != GEMM_OK) return st;
     if (cudaMemcpy2DAsync(C, ldc * 2, dC, dldc * 2, N * 2, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
         return GEMM_ERR_CUDA;
@@ -522,6 +596,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
         if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
         o.fault_inject = value;
         return GEMM_OK;
+    case GEMM_OPT_STREAM_K:
+        if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+        o.stream_k = value;
+        return GEMM_OK;
     default:
         return GEMM_ERR_INVALID_ARG;
     }
@@ -537,6 +615,7 @@ gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value
     case GEMM_OPT_MAX_CTAS: *value = o.max_ctas; return GEMM_OK;
     case GEMM_OPT_RASTER_GROUP: *value = o.raster_group; return GEMM_OK;
     case GEMM_OPT_FAULT_INJECT: *value = o.fault_inject; return GEMM_OK;
+    case GEMM_OPT_STREAM_K: *value = o.stream_k; return GEMM_OK;
     default: return GEMM_ERR_INVALID_ARG;
     }
 }
@@ -554,7 +633,7 @@ gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
     if (!g.ok) return GEMM_ERR_CUDA;
     const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);
     if (ready != GEMM_OK) return ready;
-    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], M, N, K, kc, plan);
+    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], &h->ws, M, N, K, kc, plan);
     return GEMM_OK;
 }
 
@@ -655,7 +734,7 @@ extern "C" gemm_status_t gemm_run_noalloc(const void* A, const void* B, void* C,
     if (cudaMemsetAsync(d.scratch, 0, kNoallocRecordBytes, s) != cudaSuccess) return GEMM_ERR_CUDA;
     const LaunchOptions defaults;
     const gemm_status_t st =
-        launch_gemm(defaults, d.dev, nullptr, d.scratch, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype, s);
+        launch_gemm(defaults, d.dev, nullptr, nullptr, d.scratch, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype, s);
     if (st != GEMM_OK) return st;
 
     if (watchdog_info) {

@@ -10,23 +10,44 @@
 //                 outside the tensor are zero-filled by the TMA unit ("NineToothed GEMM
 //                 语法入门" §5: out-of-range reads contribute 0).
 //   warp 1        MMA issuer (one thread): per K block, BK/16 tcgen05.mma into the TMEM
-//                 accumulator, then tcgen05.commit releases the stage; after the tile's
-//                 last K block a commit marks the accumulator full.  The first MMA of a
-//                 tile overwrites (the zero-filled accumulator of §2), later ones add.
+//                 accumulator, then tcgen05.commit releases the stage; after the item's
+//                 last K block a commit marks the accumulator full.  The first MMA of an
+//                 item overwrites (the zero-filled accumulator of §2), later ones add.
 //   warps 2..5    epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
 //                 of its lane quadrant), fp32 -> fp16/bf16 round-to-nearest-even, staging
 //                 in 128-byte-swizzled shared memory and a TMA store that drops elements
 //                 outside M x N (§5: masked write-back).
 //
-// The accumulator is double-buffered in TMEM (2 x BN fp32 columns), so the epilogue of
-// tile t overlaps the main loop of tile t+1.  Tiles are walked persistently: CTA b takes
-// tiles b, b + gridDim.x, ... in a grouped raster order (tile_coord).
+// The accumulator is double-buffered in TMEM (2 x BN fp32 columns), so the epilogue of one
+// item overlaps the main loop of the next.
+//
+// CTA pairs (PAIR = true): a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// tcgen05.mma.cta_group::2 (M = 256).  This is the two-warpgroup kernel of the same page
+// (two workers share one B tile, each takes its own rows of A) moved to the SM level:
+// CTA r loads rows [128 r, 128 r + 128) of the A tile and B rows/columns
+// [r BN/2, (r + 1) BN/2) into its own shared memory; one thread of the leader CTA (rank 0)
+// issues the pair MMA, which reads both CTAs' halves and writes each CTA's 128 accumulator
+// rows into that CTA's TMEM.  Per SM this halves the shared-memory bytes of B per MMA.
+//   full[s]      lives in the leader, armed with both CTAs' bytes; both CTAs' TMA loads
+//                complete on it (.cta_group::2 loads may signal the peer's barrier).
+//   empty[s], acc_full[b]  in both CTAs; the leader's commits arrive on both (multicast).
+//   acc_empty[b] lives in the leader and counts the epilogue warps of both CTAs.
+//
+// Work schedule ("NineToothed GEMM 语法入门" §4: output tiles are independent, the K loop
+// of one tile needs a merge if it is split).  Tiles are numbered in a grouped raster order
+// (tile_coord).  With W work units (CTAs, or CTA pairs) running at once, tiles
+// [0, dp_tiles) are taken whole, unit u doing tiles u, u + W, ...; the K blocks of the
+// remaining tiles are dealt out as W contiguous ranges (stream-K), so every unit does the
+// same amount of work instead of a last wave running part-empty.  A unit whose range covers
+// only part of a tile writes its fp32 partial sums to a workspace slot and counts itself
+// in; the last part to arrive adds all parts in K order (deterministic, whatever the
+// arrival order) and writes C.  No unit ever waits for another.
 //
 // Every mbarrier wait is bounded (a watchdog on %globaltimer): on expiry the waiting
-// thread records the place in the device error word, raises a CTA-wide abort flag, and
-// all roles leave their loops; the producer then waits (bounded) for its in-flight
-// loads, the MMA thread for its in-flight MMAs, the epilogue for its stores, and the
-// TMEM is freed before the CTA exits.  No trap, no unbounded spin.
+// thread records the place in the device error word and raises the abort flag of its CTA
+// (and of the peer CTA); all roles leave their loops; the producer then waits (bounded)
+// for its in-flight loads, the MMA thread for its in-flight MMAs, the epilogue for its
+// stores, and the TMEM is freed before the CTA exits.  No trap, no unbounded spin.
 #pragma once
 #include <cuda.h>
 #include <cuda_bf16.h>
@@ -38,7 +59,7 @@
 
 namespace dtg {
 
-constexpr int kBM = 128;          // rows per tile (= MMA M, one TMEM lane per row)
+constexpr int kBM = 128;          // accumulator rows per CTA (one TMEM lane per row)
 constexpr int kBK = 64;           // K per ring stage: 64 x 2 B = one 128-byte swizzle row
 constexpr int kUmmaK = 16;        // K per tcgen05.mma of kind::f16
 constexpr int kThreads = 192;     // 6 warps
@@ -48,8 +69,8 @@ constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
 constexpr int kEpiCols = 64;                        // columns per staged TMA store box
 constexpr int kStgBytes = 32 * kEpiCols * 2;        // one warp's 32 x 64 box, 4 KB
-
 constexpr uint32_t kWaitSleepNs = 20000;           // longest single suspension of a waiting thread
+constexpr int kEpiBarrier = 1;                      // named barrier of the 4 epilogue warps
 
 // Error-word roles.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3;
@@ -63,6 +84,12 @@ struct KernelParams {
     int32_t* err;                // device error word [4]
     void* C;                     // output base, for the ragged-N edge written without TMA
     int64_t ldc;                 // output row pitch (elements)
+    // stream-K schedule (dp_tiles == num_tiles: every tile whole, no workspace used)
+    int32_t dp_tiles;            // tiles [0, dp_tiles) are done whole, round robin
+    int64_t sk_base, sk_extra;   // K-block ranges over the rest: the first sk_extra units
+                                 // take sk_base + 1 blocks, the others sk_base
+    float* ws;                   // partial sums: [2 * units][ranks][BN / 4][128] float4
+    int32_t* counters;           // arrivals per stream-K tile and CTA rank (kept at zero)
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -80,10 +107,58 @@ __host__ __device__ __forceinline__ void tile_coord(int64_t t, int64_t tiles_m, 
     tn = r / rows;
 }
 
-template <int BN, int STAGES>
+// First stream-K K-block (relative to the stream-K region) of work unit u.
+__host__ __device__ __forceinline__ int64_t sk_start(int64_t sk_base, int64_t sk_extra, int64_t u)
+{
+    return u * sk_base + (u < sk_extra ? u : sk_extra);
+}
+
+// Work unit whose stream-K range holds K-block x of the stream-K region.
+__host__ __device__ __forceinline__ int64_t sk_owner(int64_t sk_base, int64_t sk_extra, int64_t x)
+{
+    const int64_t big = sk_extra * (sk_base + 1);
+    return x < big ? x / (sk_base + 1) : sk_extra + (x - big) / sk_base;
+}
+
+// The work items of one unit, in order: (tile, first K block, end K block).
+struct WorkIter {
+    int64_t next_dp, step, u, u_end;
+
+    __device__ __forceinline__ WorkIter(const KernelParams& p, int64_t unit, int64_t units)
+        : next_dp(unit), step(units), u(0), u_end(0)
+    {
+        if (p.dp_tiles < p.num_tiles) {
+            u = sk_start(p.sk_base, p.sk_extra, unit);
+            u_end = sk_start(p.sk_base, p.sk_extra, unit + 1);
+        }
+    }
+
+    __device__ __forceinline__ bool next(const KernelParams& p, int64_t& tile, int& kb0, int& kb1)
+    {
+        if (next_dp < p.dp_tiles) {
+            tile = next_dp;
+            kb0 = 0;
+            kb1 = p.num_kb;
+            next_dp += step;
+            return true;
+        }
+        if (u < u_end) {
+            const int64_t tr = u / p.num_kb;
+            kb0 = static_cast<int>(u - tr * p.num_kb);
+            const int64_t end = kb0 + (u_end - u);
+            kb1 = static_cast<int>(end < p.num_kb ? end : p.num_kb);
+            tile = p.dp_tiles + tr;
+            u += kb1 - kb0;
+            return true;
+        }
+        return false;
+    }
+};
+
+template <int B_ROWS, int STAGES>
 struct Smem {
     static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = BN * kBK * 2;
+    static constexpr int kBBytes = B_ROWS * kBK * 2;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRing = STAGES * kStageBytes;
     static constexpr int kStgOff = kRing;
@@ -91,13 +166,9 @@ struct Smem {
     static constexpr int kBarOff = kStgOff + kStg;
     static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
-    static constexpr int kTotal = kMiscOff + 16;     // tmem slot, abort flag
+    static constexpr int kTotal = kMiscOff + 16;     // tmem slot, abort flag, stream-K "last" flag
     static constexpr int kAlloc = kTotal + 1024;     // slack for aligning the base to 1 KB
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
-    static constexpr int kTmemCols = 2 * BN;         // two accumulator buffers
-    static_assert(kTmemCols == 32 || kTmemCols == 64 || kTmemCols == 128 || kTmemCols == 256 ||
-                      kTmemCols == 512,
-                  "TMEM allocations are powers of two");
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
@@ -192,10 +263,10 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
 // Write the 32-row x 64-column box of C at (row y, column x) that this warp holds (lane =
 // row, v = the 64 fp32 accumulator bit patterns of that row).  Normally the box goes
 // through a 128-byte-swizzled staging buffer and one TMA store, which drops rows >= M and
-// columns >= N (the masked write-back of "NineToothed GEMM 语法入门" §5).  A TMA store clips the inner dimension only
-// to 16-byte granules, so when N is not a multiple of 8 the box that straddles column N
-// is written with plain masked stores instead.  Returns true if the staging buffer was
-// used (the caller then alternates buffers).
+// columns >= N (the masked write-back of "NineToothed GEMM 语法入门" §5).  A TMA store
+// clips the inner dimension only to 16-byte granules, so when N is not a multiple of 8
+// the box that straddles column N is written with plain masked stores instead.  Returns
+// true if the staging buffer was used (the caller then alternates buffers).
 template <bool BF16>
 __device__ __forceinline__ bool store_box(const uint32_t (&v)[64], int32_t x, int32_t y, int lane,
                                           uint32_t stg, const CUtensorMap* tmC, const KernelParams& p)
@@ -248,13 +319,55 @@ __device__ __forceinline__ bool store_box(const uint32_t (&v)[64], int32_t x, in
     return true;
 }
 
-template <int BN, int STAGES, bool BF16, bool B_MN_MAJOR>
+__device__ __forceinline__ void epilogue_bar_sync()
+{
+    asm volatile("bar.sync %0, %1;" ::"n"(kEpiBarrier), "n"(kEpiWarps * 32) : "memory");
+}
+
+// Barrier of the 4 epilogue warps that also ANDs a flag over their 128 threads: the
+// epilogue warps use it to agree on leaving their loop, so they always execute the same
+// iterations (and therefore the same named barriers).
+__device__ __forceinline__ bool epilogue_bar_and(bool v)
+{
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred pi, po;\n\t"
+        "setp.ne.u32 pi, %1, 0;\n\t"
+        "bar.red.and.pred po, %2, %3, pi;\n\t"
+        "selp.u32 %0, 1, 0, po;\n\t}\n"
+        : "=r"(r)
+        : "r"(v ? 1u : 0u), "n"(kEpiBarrier), "n"(kEpiWarps * 32)
+        : "memory");
+    return r != 0;
+}
+
+// Stream-K bookkeeping for stream-K tile tr (relative to the stream-K region): the first
+// unit with a part of it and the number of parts.
+__device__ __forceinline__ void sk_parts(const KernelParams& p, int64_t tr, int64_t& first_unit, int64_t& parts)
+{
+    first_unit = sk_owner(p.sk_base, p.sk_extra, tr * p.num_kb);
+    parts = sk_owner(p.sk_base, p.sk_extra, (tr + 1) * p.num_kb - 1) - first_unit + 1;
+}
+
+// Workspace slot of unit u's part of stream-K tile tr: each unit has two slots, for the
+// tile its range starts in (0) and the tile it ends in (1).
+__device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int64_t tr)
+{
+    return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
+}
+
+template <int BN, int STAGES, bool BF16, bool NN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
-    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA,
-                        const __grid_constant__ CUtensorMap tmB,
+    gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
-    using L = Smem<BN, STAGES>;
+    constexpr int kRanks = PAIR ? 2 : 1;
+    constexpr int kTileM = kBM * kRanks;       // output rows per tile
+    constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
+    constexpr uint32_t kTmemCols = 2 * BN;     // two accumulator buffers
+    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
+    using L = Smem<kBRows, STAGES>;
+
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1 KB (128-byte swizzle atoms repeat every 8 rows).
     const uint32_t raw_addr = ptx::smem_addr(smem_raw);
@@ -269,9 +382,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int32_t* const abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMiscOff + 4);
+    volatile int32_t* const last_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMiscOff + 8);
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0: leader (issues the MMAs)
+    const bool leader = rank == 0;
+    const int64_t unit = PAIR ? static_cast<int64_t>(ptx::cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
+    const int64_t units = PAIR ? static_cast<int64_t>(ptx::num_clusters_x()) : static_cast<int64_t>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -280,60 +398,81 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
-            ptx::mbar_init(acce_bar(b), kEpiWarps);
+            ptx::mbar_init(acce_bar(b), kEpiWarps * kRanks);
         }
         ptx::mbar_init(drain_bar, 1);
         *abort_flag = 0;
+        *last_flag = 0;
         ptx::fence_mbar_init();
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmC);
     }
     if (warp == kMmaWarp) {
-        ptx::tmem_alloc(ptx::smem_addr(tmem_slot), L::kTmemCols);
-        ptx::tmem_relinquish();
+        if constexpr (PAIR) {
+            ptx::tmem_alloc_pair(ptx::smem_addr(tmem_slot), kTmemCols);
+            ptx::tmem_relinquish_pair();
+        } else {
+            ptx::tmem_alloc(ptx::smem_addr(tmem_slot), kTmemCols);
+            ptx::tmem_relinquish();
+        }
     }
     ptx::tc_fence_before_sync();
-    __syncthreads();
+    if constexpr (PAIR)
+        ptx::cluster_sync();  // both CTAs' barriers initialised and TMEM allocated
+    else
+        __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
 
-    const Watchdog wd{abort_flag, &p};
-    const int num_kb = p.num_kb;
+    Watchdog wd{abort_flag, &p};
+    if constexpr (PAIR) wd.peer_abort = ptx::mapa_shared(ptx::smem_addr(const_cast<int32_t*>(abort_flag)), rank ^ 1u);
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
             // ---------------------------------------------------------------- producer
-            uint32_t armed_mask = 0, armed_parity = 0;  // per stage: armed at least once, last parity
+            uint32_t armed_mask = 0, armed_parity = 0;  // leader: stages armed, last parity
             int stage = 0;
             uint32_t phase = 0;
-            bool injected = false;
-            for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+            int64_t loaded = 0;
+            WorkIter it(p, unit, units);
+            int64_t tile;
+            int kb0, kb1;
+            while (it.next(p, tile, kb0, kb1)) {
                 int64_t tm, tn;
-                tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                const int32_t y_a = static_cast<int32_t>(tm * kBM);
-                const int32_t n0 = static_cast<int32_t>(tn * BN);
-                for (int kb = 0; kb < num_kb; ++kb) {
-                    if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, t, kb)) goto producer_done;
-                    if (p.fault_inject && !injected && blockIdx.x == 0 && kb == (num_kb > 1 ? 1 : 0)) {
-                        injected = true;  // leave this stage unarmed: its consumer must time out
+                tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                const int32_t y_a = static_cast<int32_t>(tm * kTileM + rank * kBM);
+                const int32_t n_b = static_cast<int32_t>(tn * BN + rank * kBRows);
+                for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
+                    if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
+                    if (p.fault_inject && leader && unit == 0 && loaded == 1) {
+                        // Test hook: leave this stage unarmed so the MMA thread's wait on it
+                        // runs out and the watchdog path is exercised.
                     } else {
                         const uint32_t sa = base + stage * L::kStageBytes;
                         const uint32_t sb = sa + L::kABytes;
                         const int32_t k0 = kb * kBK;
-                        ptx::mbar_arrive_expect_tx(full_bar(stage), L::kStageBytes);
-                        ptx::tma_load_2d(sa, &tmA, k0, y_a, full_bar(stage));
-                        if constexpr (B_MN_MAJOR) {
-                            // B stored K x N: BN/64 boxes of 64 (N) x 64 (K), each 8 KB.
-#pragma unroll
-                            for (int q = 0; q < BN / 64; ++q)
-                                ptx::tma_load_2d(sb + q * (64 * kBK * 2), &tmB, n0 + q * 64, k0, full_bar(stage));
-                        } else {
-                            // B stored N x K: one box of 64 (K) x BN (N rows).
-                            ptx::tma_load_2d(sb, &tmB, k0, n0, full_bar(stage));
+                        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                        if (leader) {
+                            ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes);
+                            armed_mask |= 1u << stage;
+                            armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         }
-                        armed_mask |= 1u << stage;
-                        armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
+                        auto load = [&](uint32_t dst, const CUtensorMap* tm_, int32_t x, int32_t y) {
+                            if constexpr (PAIR)
+                                ptx::tma_load_2d_pair(dst, tm_, x, y, fb);
+                            else
+                                ptx::tma_load_2d(dst, tm_, x, y, fb);
+                        };
+                        load(sa, &tmA, k0, y_a);
+                        if constexpr (NN) {
+                            // B stored K x N: kBRows / 64 boxes of 64 (N) x 64 (K), 8 KB each.
+#pragma unroll
+                            for (int q = 0; q < kBRows / 64; ++q) load(sb + q * (64 * kBK * 2), &tmB, n_b + q * 64, k0);
+                        } else {
+                            // B stored N x K: one box of 64 (K) x kBRows (N rows).
+                            load(sb, &tmB, k0, n_b);
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -352,67 +491,84 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         producer_done:
-            // Wait (bounded) for every load this thread issued, so none is in flight at exit.
-            for (int s = 0; s < STAGES; ++s)
-                if (armed_mask & (1u << s)) wd.drain(full_bar(s), (armed_parity >> s) & 1u);
+            // The leader's full barriers count every load of the CTA (pair): waiting on them
+            // (bounded) covers every load still in flight.
+            if (leader)
+                for (int s = 0; s < STAGES; ++s)
+                    if (armed_mask & (1u << s)) wd.drain(full_bar(s), (armed_parity >> s) & 1u);
         }
     } else if (warp == kMmaWarp) {
-        if (lane == 0) {
+        if (lane == 0 && leader) {
             // ---------------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_f16<BF16, B_MN_MAJOR, kBM, BN>();
+            constexpr uint32_t idesc = idesc_f16<BF16, NN, kTileM, BN>();
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
             uint32_t acc_phase = 0;
             bool aborted = false;
-            if (num_kb > 0) {
-                for (int64_t t = blockIdx.x; t < p.num_tiles && !aborted; t += gridDim.x) {
-                    if (!wd.wait(acce_bar(acc), acc_phase ^ 1u, kRoleMma, t, -1)) {
+            WorkIter it(p, unit, units);
+            int64_t tile;
+            int kb0, kb1;
+            while (!aborted && it.next(p, tile, kb0, kb1)) {
+                if (!wd.wait(acce_bar(acc), acc_phase ^ 1u, kRoleMma, tile, -1)) {
+                    aborted = true;
+                    break;
+                }
+                ptx::tc_fence_after_sync();
+                const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
+                for (int kb = kb0; kb < kb1; ++kb) {
+                    if (!wd.wait(full_bar(stage), phase, kRoleMma, tile, kb)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                    for (int kb = 0; kb < num_kb; ++kb) {
-                        if (!wd.wait(full_bar(stage), phase, kRoleMma, t, kb)) {
-                            aborted = true;
-                            break;
-                        }
-                        ptx::tc_fence_after_sync();
-                        const uint32_t sa = base + stage * L::kStageBytes;
-                        const uint32_t sb = sa + L::kABytes;
+                    const uint32_t sa = base + stage * L::kStageBytes;
+                    const uint32_t sb = sa + L::kABytes;
 #pragma unroll
-                        for (int k = 0; k < kBK / kUmmaK; ++k) {
-                            // A (K-major, 128B swizzle): the k-th 16-column slice starts 32 B
-                            // further along each 128-byte row; 8-row groups are 1 KB apart.
-                            const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
-                            uint64_t bdesc;
-                            if constexpr (B_MN_MAJOR) {
-                                // B (N-major): rows are K; the k-th slice is 16 rows (2 KB) on;
-                                // 64-wide N blocks are 8 KB apart (LBO), 8-row K groups 1 KB (SBO).
-                                bdesc = smem_desc_sw128(sb + k * 2048, 64 * kBK * 2, 1024);
-                            } else {
-                                bdesc = smem_desc_sw128(sb + k * 32, 16, 1024);
-                            }
-                            ptx::mma_f16_cta1(d_tmem, adesc, bdesc, idesc, (kb | k) != 0 ? 1u : 0u);
+                    for (int k = 0; k < kBK / kUmmaK; ++k) {
+                        // A (K-major, 128B swizzle): the k-th 16-column slice starts 32 B further
+                        // along each 128-byte row; 8-row groups are 1 KB apart (SBO).
+                        const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
+                        uint64_t bdesc;
+                        if constexpr (NN) {
+                            // B (N-major): rows are K; the k-th slice is 16 rows (2 KB) on; 64-wide
+                            // N blocks are 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO).
+                            bdesc = smem_desc_sw128(sb + k * 2048, 64 * kBK * 2, 1024);
+                        } else {
+                            bdesc = smem_desc_sw128(sb + k * 32, 16, 1024);
                         }
-                        ptx::mma_commit_cta1(empty_bar(stage));  // stage free once these MMAs finish
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
+                        const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
+                        if constexpr (PAIR)
+                            ptx::mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                        else
+                            ptx::mma_f16_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
                     }
-                    if (aborted) break;
-                    ptx::mma_commit_cta1(accf_bar(acc));  // accumulator complete
-                    if (++acc == 2) {
-                        acc = 0;
-                        acc_phase ^= 1u;
+                    // The stage is free once these MMAs finish (in both CTAs of a pair).
+                    if constexpr (PAIR)
+                        ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
+                    else
+                        ptx::mma_commit_cta1(empty_bar(stage));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
                     }
+                }
+                if (aborted) break;
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair_mc(accf_bar(acc), 0x3);  // accumulator complete
+                else
+                    ptx::mma_commit_cta1(accf_bar(acc));
+                if (++acc == 2) {
+                    acc = 0;
+                    acc_phase ^= 1u;
                 }
             }
             if (aborted) {
                 // Let every MMA issued so far finish before the TMEM is released.
-                ptx::mma_commit_cta1(drain_bar);
+                if constexpr (PAIR)
+                    ptx::mma_commit_pair_mc(drain_bar, 0x1);
+                else
+                    ptx::mma_commit_cta1(drain_bar);
                 wd.drain(drain_bar, 0);
             }
         }
@@ -421,44 +577,151 @@ __global__ void __launch_bounds__(kThreads, 1)
         // -------------------------------------------------------------------- epilogue
         const int ew = warp - kEpiWarp0;            // 0..3: staging buffers
         const int quad = warp & 3;                  // TMEM lane quadrant this warp may read
+        const int row_in_cta = quad * 32 + lane;    // accumulator row of this thread
         const uint32_t stg0 = base + L::kStgOff + ew * 2 * kStgBytes;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
         int sbuf = 0;
-        for (int64_t t = blockIdx.x; t < p.num_tiles; t += gridDim.x) {
+        WorkIter it(p, unit, units);
+        int64_t tile;
+        int kb0, kb1;
+        auto release_acc = [&]() {
+            // Whole accumulator read: hand the buffer back to the MMA thread.
+            ptx::tc_fence_before_sync();
+            __syncwarp();
+            if (lane == 0) {
+                if constexpr (PAIR)
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0));
+                else
+                    ptx::mbar_arrive(acce_bar(acc));
+            }
+        };
+        while (it.next(p, tile, kb0, kb1)) {
             int64_t tm, tn;
-            tile_coord(t, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            if (num_kb > 0) {
-                const bool ok = wd.wait(accf_bar(acc), acc_phase, kRoleEpilogue, t, -1);
-                if (!__all_sync(0xffffffffu, ok)) break;
-                ptx::tc_fence_after_sync();
-            }
-            const int32_t y = static_cast<int32_t>(tm * kBM + quad * 32);
+            tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            const bool ok = wd.wait(accf_bar(acc), acc_phase, kRoleEpilogue, tile, -1);
+            if (!epilogue_bar_and(ok)) break;  // all four epilogue warps leave together
+            ptx::tc_fence_after_sync();
+            const int32_t y = static_cast<int32_t>(tm * kTileM + rank * kBM + quad * 32);
+            const uint32_t tacc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
+            if (kb0 == 0 && kb1 == p.num_kb) {
+                // Whole tile: convert and store.
 #pragma unroll 1
-            for (int c = 0; c < BN / kEpiCols; ++c) {
-                uint32_t v[64];
-                if (num_kb > 0) {
-                    const uint32_t ta = tmem_base + lane_off + static_cast<uint32_t>(acc * BN + c * kEpiCols);
-                    uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-                    uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-                    ptx::tmem_ld_32x32b_x32(ta, v0);
-                    ptx::tmem_ld_32x32b_x32(ta + 32, v1);
+                for (int c = 0; c < BN / kEpiCols; ++c) {
+                    uint32_t v[64];
+                    uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                    uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                    ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols, v0);
+                    ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols + 32, v1);
                     ptx::tmem_wait_ld();
-                    if (c == BN / kEpiCols - 1) {
-                        // Whole accumulator read: hand the buffer back to the MMA warp.
-                        ptx::tc_fence_before_sync();
-                        __syncwarp();
-                        if (lane == 0) ptx::mbar_arrive(acce_bar(acc));
-                    }
-                } else {
-#pragma unroll
-                    for (int i = 0; i < 64; ++i) v[i] = 0u;  // K == 0: the empty sum
+                    if (c == BN / kEpiCols - 1) release_acc();
+                    const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
+                    if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
                 }
-                const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+            } else {
+                // Part of a stream-K tile: park the fp32 partial sums in this unit's slot.
+                // A slot holds float4 column groups group-major, rows inner, so each warp
+                // store / load moves 512 contiguous bytes (32 rows of one column group).
+                const int64_t tr = tile - p.dp_tiles;
+                constexpr size_t kSlotF4 = static_cast<size_t>(kBM) * BN / 4;
+                auto slot_f4 = [&](int64_t slot) {
+                    return reinterpret_cast<float4*>(p.ws) + (static_cast<size_t>(slot) * kRanks + rank) * kSlotF4 +
+                           row_in_cta;
+                };
+                int64_t first_unit, parts;
+                sk_parts(p, tr, first_unit, parts);
+                const int64_t my_part = unit - first_unit;
+                int32_t* counter = p.counters + tr * kRanks + rank;
+                // Sum all parts in K order (so the result does not depend on who arrives
+                // last) and store.  With own_in_tmem this part's sums are read from TMEM at
+                // its place in the order instead of from the workspace.
+                auto reduce_and_store = [&](bool own_in_tmem) {
+#pragma unroll 1
+                    for (int c = 0; c < BN / kEpiCols; ++c) {
+                        float s[64];
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) s[i] = 0.0f;
+#pragma unroll 2
+                        for (int64_t part = 0; part < parts; ++part) {
+                            if (own_in_tmem && part == my_part) {
+                                uint32_t v[64];
+                                uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                                uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                                ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols, v0);
+                                ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols + 32, v1);
+                                ptx::tmem_wait_ld();
+#pragma unroll
+                                for (int i = 0; i < 64; ++i) s[i] += __uint_as_float(v[i]);
+                            } else {
+                                const float4* s4 = slot_f4(sk_slot(p, first_unit + part, tr)) + c * 16 * kBM;
+                                float4 f[16];
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) f[q] = __ldcg(s4 + q * kBM);
+#pragma unroll
+                                for (int q = 0; q < 16; ++q) {
+                                    s[4 * q] += f[q].x;
+                                    s[4 * q + 1] += f[q].y;
+                                    s[4 * q + 2] += f[q].z;
+                                    s[4 * q + 3] += f[q].w;
+                                }
+                            }
+                        }
+                        if (own_in_tmem && c == BN / kEpiCols - 1) release_acc();
+                        uint32_t v[64];
+#pragma unroll
+                        for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(s[i]);
+                        const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
+                        if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+                    }
+                };
+                // Are all the other parts in already?  Then this part is the last: it skips
+                // parking its own sums.  (Each other part parked its sums before counting
+                // itself in, so what the count shows is visible.)
+                if (ew == 0 && lane == 0) {
+                    const bool last = atomicAdd(counter, 0) == parts - 1;
+                    if (last) {
+                        *counter = 0;  // every other part has counted itself in: ready for reuse
+                        __threadfence();
+                    }
+                    *last_flag = last ? 1 : 0;
+                }
+                epilogue_bar_sync();
+                if (*last_flag) {
+                    reduce_and_store(true);
+                } else {
+                    float4* mine = slot_f4(sk_slot(p, unit, tr));
+#pragma unroll 1
+                    for (int c = 0; c < BN / kEpiCols; ++c) {
+                        uint32_t v[64];
+                        uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                        uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                        ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols, v0);
+                        ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols + 32, v1);
+                        ptx::tmem_wait_ld();
+                        if (c == BN / kEpiCols - 1) release_acc();
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            mine[(c * 16 + q) * kBM] = make_float4(__uint_as_float(v[4 * q]), __uint_as_float(v[4 * q + 1]),
+                                                                   __uint_as_float(v[4 * q + 2]),
+                                                                   __uint_as_float(v[4 * q + 3]));
+                    }
+                    // Count this part in; if it turns out to be the last, sum every part.
+                    __threadfence();
+                    epilogue_bar_sync();
+                    if (ew == 0 && lane == 0) {
+                        const bool last = atomicAdd(counter, 1) == parts - 1;
+                        if (last) {
+                            *counter = 0;
+                            __threadfence();
+                        }
+                        *last_flag = last ? 1 : 0;
+                    }
+                    epilogue_bar_sync();
+                    if (*last_flag) reduce_and_store(false);
+                }
             }
-            if (num_kb > 0 && ++acc == 2) {
+            if (++acc == 2) {
                 acc = 0;
                 acc_phase ^= 1u;
             }
@@ -469,9 +732,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     ptx::tc_fence_before_sync();
     __syncthreads();
+    if constexpr (PAIR) ptx::cluster_sync();  // neither CTA exits or frees TMEM while the peer may use it
     if (warp == kMmaWarp) {
         ptx::tc_fence_after_sync();
-        ptx::tmem_dealloc(tmem_base, L::kTmemCols);
+        if constexpr (PAIR)
+            ptx::tmem_dealloc_pair(tmem_base, kTmemCols);
+        else
+            ptx::tmem_dealloc(tmem_base, kTmemCols);
     }
 }
 

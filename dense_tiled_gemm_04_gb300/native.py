@@ -20,7 +20,7 @@ DTYPES = {"f16": DTYPE_F16, "bf16": DTYPE_BF16}
 TORCH_TO_DTYPE = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
-OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT = range(5)
+OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT, OPT_STREAM_K = range(6)
 CONFIG_AUTO, CONFIG_128x256, CONFIG_128x128, CONFIG_256x256 = range(4)
 
 
@@ -28,7 +28,8 @@ class gemm_plan_t(ctypes.Structure):
     _fields_ = [("config", ctypes.c_int32), ("bm", ctypes.c_int32), ("bn", ctypes.c_int32),
                 ("bk", ctypes.c_int32), ("stages", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
-                ("grid", ctypes.c_int64), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32)]
+                ("grid", ctypes.c_int64), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
+                ("dp_tiles", ctypes.c_int64), ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64)]
 
 
 class GemmError(RuntimeError):

@@ -67,9 +67,13 @@ enum {
     GEMM_OPT_MAX_CTAS = 2,     /* cap on persistent CTAs (0 = one per SM); tests use it to
                                   make each CTA walk several tiles                            */
     GEMM_OPT_RASTER_GROUP = 3, /* output-tile raster: M tiles per group (L2 reuse), >= 1      */
-    GEMM_OPT_FAULT_INJECT = 4  /* test hook: 1 = CTA 0's producer leaves one ring stage unarmed,
+    GEMM_OPT_FAULT_INJECT = 4, /* test hook: 1 = CTA 0's producer leaves one ring stage unarmed,
                                   so a consumer wait runs out and the watchdog path returns
                                   GEMM_ERR_TIMEOUT through gemm_sync_status (no GPU fault)   */
+    GEMM_OPT_STREAM_K = 5      /* 1 (default): when whole tiles would leave the last wave
+                                  part-empty, share the K blocks of the last tiles evenly
+                                  between CTAs (partial sums merged in K order, so results
+                                  are deterministic); 0: whole tiles only                     */
 };
 
 typedef int32_t gemm_config_t;
@@ -90,6 +94,9 @@ typedef struct {
     int64_t grid;       /* CTAs launched (persistent)                                        */
     int32_t threads;    /* threads per CTA                                                   */
     int32_t smem_bytes; /* dynamic shared memory per CTA                                     */
+    int64_t dp_tiles;   /* tiles done whole; the rest are shared out by K blocks (stream-K) */
+    int64_t sk_base;    /* stream-K K blocks per work unit (the first sk_extra units: +1)    */
+    int64_t sk_extra;
 } gemm_plan_t;
 
 /* Create a handle bound to CUDA device `device`.  Checks that the device is sm_103,

@@ -339,7 +339,8 @@ def test_watchdog_timeout_is_reported_and_context_survives(g, config):
         assert st == native.OK
         assert g.sync_status() == native.ERR_TIMEOUT
         info = g.error_info()
-        assert info[0] == 1 and info[2] == 0, info  # timeout, in CTA 0
+        # A timeout, first seen in the first CTA (or, for CTA pairs, either CTA of the first pair).
+        assert info[0] == 1 and info[2] in ((0, 1) if config == native.CONFIG_256x256 else (0,)), info
     finally:
         g.set_option(native.OPT_FAULT_INJECT, 0)
         g.set_option(native.OPT_TIMEOUT_NS, 2_000_000_000)
