@@ -30,16 +30,18 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor roofline"
 WORKLOAD = "c4"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
-KERNEL_SOURCES = ["dense_tiled_gemm_04_gb300/csrc/gemm_kernel.cuh", "dense_tiled_gemm_04_gb300/csrc/gemm_kernel_pair.cuh",
-                  "dense_tiled_gemm_04_gb300/csrc/sm103_ptx.cuh",
-                  "dense_tiled_gemm_04_gb300/csrc/gemm_api.cu"]
+KERNEL_DIR = os.path.join("dense_tiled_gemm_04_gb300", "csrc")
 
 
 def kernel_fingerprint() -> str:
+    """Hash of the library sources; a stored ncu traffic figure is only reported for the
+    sources it was measured on."""
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+    d = os.path.join(ROOT, KERNEL_DIR)
+    for name in sorted(os.listdir(d)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            with open(os.path.join(d, name), "rb") as f:
+                h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
 
 

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cstdint>
 #include <cstring>
 #include <mutex>
@@ -18,7 +19,7 @@ namespace {
 
 using dtg::KernelParams;
 
-constexpr int kGroupDefault = 16;
+constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int kPairStages = 6;
@@ -87,6 +88,16 @@ struct KernelChoice {
     int smem;
 };
 
+// Streams and events of gemm_run_host's copy/compute pipeline (created on first use).
+struct HostPipe {
+    static constexpr int kMaxChunks = 8;
+    static constexpr int kChunksWanted = 4;
+    bool ready = false;
+    cudaStream_t in[2] = {nullptr, nullptr}, out = nullptr;
+    cudaEvent_t start = nullptr, b[2] = {nullptr, nullptr}, done = nullptr;
+    cudaEvent_t a[kMaxChunks] = {}, c[kMaxChunks] = {};
+};
+
 // Stream-K workspace: fp32 partial sums and arrival counters (see gemm_kernel.cuh).
 struct Workspace {
     float* partials = nullptr;
@@ -105,9 +116,10 @@ struct gemm_handle_s {
     DeviceState dev;
     Workspace ws;
     std::vector<TmapEntry> tmaps;
-    // gemm_run_host staging
+    // gemm_run_host staging and pipeline
     void* d_stage = nullptr;
     size_t stage_bytes = 0;
+    HostPipe pipe;
 };
 
 namespace {
@@ -488,6 +500,14 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
         if (h->d_stage && cudaFree(h->d_stage) != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->ws.partials && cudaFree(h->ws.partials) != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->ws.counters && cudaFree(h->ws.counters) != cudaSuccess) st = GEMM_ERR_CUDA;
+        if (h->pipe.ready) {
+            for (cudaStream_t q : {h->pipe.in[0], h->pipe.in[1], h->pipe.out}) cudaStreamDestroy(q);
+            for (cudaEvent_t e : {h->pipe.start, h->pipe.b[0], h->pipe.b[1], h->pipe.done}) cudaEventDestroy(e);
+            for (int i = 0; i < HostPipe::kMaxChunks; ++i) {
+                cudaEventDestroy(h->pipe.a[i]);
+                cudaEventDestroy(h->pipe.c[i]);
+            }
+        }
     }
     delete h;
     return st;
@@ -514,6 +534,18 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    HostPipe& hp = h->pipe;
+    if (!hp.ready) {
+        for (cudaStream_t* q : {&hp.in[0], &hp.in[1], &hp.out})
+            if (cudaStreamCreateWithFlags(q, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
+        for (cudaEvent_t* e : {&hp.start, &hp.b[0], &hp.b[1], &hp.done})
+            if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
+        for (int i = 0; i < HostPipe::kMaxChunks; ++i)
+            if (cudaEventCreateWithFlags(&hp.a[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.c[i], cudaEventDisableTiming) != cudaSuccess)
+                return GEMM_ERR_CUDA;
+        hp.ready = true;
+    }
     // Device copies are packed: ld rounded up to 8 elements (16 bytes) keeps TMA alignment.
     auto r8 = [](int64_t x) { return (x + 7) & ~int64_t(7); };
     auto r256 = [](size_t x) { return (x + 255) & ~size_t(255); };
@@ -539,17 +571,52 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
     char* dA = static_cast<char*>(h->d_stage);
     char* dB = dA + bytes_a;
     char* dC = dB + bytes_b;
+    const char* hA = static_cast<const char*>(A);
+    const char* hB = static_cast<const char*>(B);
+    char* hC = static_cast<char*>(C);
+
+    // Pipeline: B first (its two halves on two copy streams), then A in row chunks
+    // alternating between the copy streams; the GEMM of a chunk starts on `stream` once B
+    // and the chunk's rows are in, and the chunk's rows of C go back on a third stream
+    // while later chunks compute.  Chunks are whole multiples of 256 rows.
+    const int64_t chunk = std::max<int64_t>(2048, ((M + HostPipe::kChunksWanted - 1) / HostPipe::kChunksWanted + 255) /
+                                                      256 * 256);
+    const int nchunks = static_cast<int>(std::min<int64_t>((M + chunk - 1) / chunk, HostPipe::kMaxChunks));
+    const int64_t rows_per = (M + nchunks - 1) / nchunks;
+    if (cudaEventRecord(hp.start, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    for (cudaStream_t q : {hp.in[0], hp.in[1], hp.out})
+        if (cudaStreamWaitEvent(q, hp.start, 0) != cudaSuccess) return GEMM_ERR_CUDA;
     if (K > 0) {
-        if (cudaMemcpy2DAsync(dA, dlda * 2, A, lda * 2, K * 2, M, cudaMemcpyHostToDevice, s) != cudaSuccess)
+        const int64_t half = b_rows / 2;
+        if (half > 0 && cudaMemcpy2DAsync(dB, dldb * 2, hB, ldb * 2, b_cols * 2, half, cudaMemcpyHostToDevice,
+                                          hp.in[0]) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (cudaMemcpy2DAsync(dB, dldb * 2, B, ldb * 2, b_cols * 2, b_rows, cudaMemcpyHostToDevice, s) !=
-            cudaSuccess)
+        if (cudaMemcpy2DAsync(dB + half * dldb * 2, dldb * 2, hB + half * ldb * 2, ldb * 2, b_cols * 2,
+                              b_rows - half, cudaMemcpyHostToDevice, hp.in[1]) != cudaSuccess)
             return GEMM_ERR_CUDA;
     }
-    const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, dA, dB, dC, M, N, K, dlda,
-                                         dldb, dldc, layout, dtype, s);
-    if (st != GEMM_OK) return st;
-    if (cudaMemcpy2DAsync(C, ldc * 2, dC, dldc * 2, N * 2, M, cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    if (cudaEventRecord(hp.b[0], hp.in[0]) != cudaSuccess || cudaEventRecord(hp.b[1], hp.in[1]) != cudaSuccess ||
+        cudaStreamWaitEvent(s, hp.b[0], 0) != cudaSuccess || cudaStreamWaitEvent(s, hp.b[1], 0) != cudaSuccess)
+        return GEMM_ERR_CUDA;
+    for (int i = 0; i < nchunks; ++i) {
+        const int64_t r0 = i * rows_per, rows = std::min(rows_per, M - r0);
+        if (rows <= 0) break;
+        cudaStream_t qin = hp.in[i & 1];
+        if (K > 0 && cudaMemcpy2DAsync(dA + r0 * dlda * 2, dlda * 2, hA + r0 * lda * 2, lda * 2, K * 2, rows,
+                                       cudaMemcpyHostToDevice, qin) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaEventRecord(hp.a[i], qin) != cudaSuccess || cudaStreamWaitEvent(s, hp.a[i], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, dA + r0 * dlda * 2, dB,
+                                             dC + r0 * dldc * 2, rows, N, K, dlda, dldb, dldc, layout, dtype, s);
+        if (st != GEMM_OK) return st;
+        if (cudaEventRecord(hp.c[i], s) != cudaSuccess || cudaStreamWaitEvent(hp.out, hp.c[i], 0) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+        if (cudaMemcpy2DAsync(hC + r0 * ldc * 2, ldc * 2, dC + r0 * dldc * 2, dldc * 2, N * 2, rows,
+                              cudaMemcpyDeviceToHost, hp.out) != cudaSuccess)
+            return GEMM_ERR_CUDA;
+    }
+    if (cudaEventRecord(hp.done, hp.out) != cudaSuccess || cudaStreamWaitEvent(s, hp.done, 0) != cudaSuccess)
         return GEMM_ERR_CUDA;
     return read_error_word(h, s);
 }

@@ -322,6 +322,26 @@ def test_run_host_matches_oracle(g):
     assert_close(codes(C), oracle.gemm(A, B, w.layout, w.dtype), w.dtype, "run_host")
 
 
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_run_host_pipelined_chunks_and_padding(g, layout):
+    # 5000 rows go through the host path in several row chunks (copy / compute / copy back
+    # overlapped); host buffers have padded rows whose padding must be left alone.
+    M, N, K = 5000, 1000, 520
+    A, B = make_inputs(M, N, K, layout, "bf16", "int", seed=12, lda=K + 8, ldb=(N if layout == "NN" else K) + 16)
+    Ah = A.as_strided((M, A.stride(0)), (A.stride(0), 1)).pin_memory()[:, :K]
+    rows_b = B.shape[0]
+    Bh = B.as_strided((rows_b, B.stride(0)), (B.stride(0), 1)).pin_memory()[:, :B.shape[1]]
+    ldc = N + 24
+    Cbuf = torch.full((M, ldc), 0, dtype=torch.int16).view(torch.bfloat16).pin_memory()
+    Cbuf.view(torch.int16).fill_(SENTINEL)
+    C = Cbuf[:, :N]
+    st = g.run_host(Ah, Bh, C, layout)
+    assert st == native.OK, native.status_string(st)
+    got = Cbuf.view(torch.int16).numpy().view(np.uint16)
+    assert_guard(got, M, N)
+    assert_exact(got[:, :N], oracle.gemm(A, B, layout, "bf16"), "run_host chunks")
+
+
 @pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256])
 def test_watchdog_timeout_is_reported_and_context_survives(g, config):
     # One ring stage is left unarmed in CTA 0: the MMA thread's wait on it must run out,
