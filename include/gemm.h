@@ -23,10 +23,13 @@
  * pitches): A, B, C must be 16-byte aligned and lda, ldb, ldc multiples of 8 elements,
  * otherwise GEMM_ERR_UNSUPPORTED.  There is no fallback path.
  *
- * Ownership.  The caller owns A, B, C and the stream; the handle owns a small device
- * workspace (the watchdog's error word), a cache of tensor-map descriptors and, after
- * the first gemm_run_host, device staging buffers.  A handle may be used from one host
- * thread at a time.  Aliasing C with A or B is undefined.
+ * Ownership.  The caller owns A, B, C and the stream; the handle owns the watchdog's
+ * 16-byte error word, a stream-K workspace (fp32 partial sums and arrival counters, about
+ * 40 MB on a 152-SM GPU, allocated by gemm_create), a cache of tensor-map descriptors and,
+ * after the first gemm_run_host, device staging buffers plus that path's streams and
+ * events.  A handle may be used from one host thread at a time, and its launches must not
+ * overlap on the GPU (they share the workspace): enqueue them on one stream or order them.
+ * Aliasing C with A or B is undefined.
  *
  * Errors.  Every entry point returns a status; nothing throws across the ABI.
  */
@@ -100,7 +103,7 @@ typedef struct {
 } gemm_plan_t;
 
 /* Create a handle bound to CUDA device `device`.  Checks that the device is sm_103,
- * reads its SM count and allocates the 16-byte device error word.
+ * reads its SM count and allocates the device error word and the stream-K workspace.
  * Returns INVALID_ARG (out == NULL or no such device), ARCH, or CUDA. */
 gemm_status_t gemm_create(gemm_handle_t* out, int device);
 
