@@ -68,6 +68,9 @@ def _load():
     lib.oracle_gemm_rows.restype = ctypes.c_int
     lib.oracle_gemm_elems.argtypes = [p, p, i64, i64, i64, ctypes.c_int, ctypes.c_int, p, p, i64, p, p]
     lib.oracle_gemm_elems.restype = ctypes.c_int
+    lib.oracle_gemm_rows_axpby.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_double, p, i64, p, p, i64, ctypes.c_int]
+    lib.oracle_gemm_rows_axpby.restype = ctypes.c_int
     lib.oracle_decode_array.argtypes = [p, p, i64, ctypes.c_int]
     lib.oracle_decode_array.restype = None
     lib.oracle_encode_array.argtypes = [p, p, i64, ctypes.c_int]
@@ -188,8 +191,36 @@ def gemm_elems(A, B, layout: str, dtype: str, ms, ns, want_f64: bool = False):
     return (out16, out64) if want_f64 else out16
 
 
+def gemm_axpby(A, B, layout: str, dtype: str, alpha: float, beta: float, Cin=None, rows=None,
+               want_f64: bool = False, nthreads: int = 0):
+    """alpha * (A·B) + beta * Cin (Cin: the logical M x N input codes, row-major; ignored when
+    beta == 0).  Returns rounded codes for `rows` (default all), or ``(codes, f64)``."""
+    lib = _load()
+    A, B = _codes(A), _codes(B)
+    M, N, K = _shape_check(A, B, layout)
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    rows = np.ascontiguousarray(rows.astype(np.int64))
+    if beta != 0.0:
+        Cin = np.ascontiguousarray(_codes(Cin))
+        if Cin.shape != (M, N):
+            raise ValueError(f"Cin must be {M} x {N}")
+        cptr, ldcin = Cin.ctypes.data, max(N, 1)
+    else:
+        cptr, ldcin = None, 1
+    out16 = np.zeros((rows.size, N), dtype=np.uint16)
+    out64 = np.zeros((rows.size, N), dtype=np.float64) if want_f64 else None
+    used = lib.oracle_gemm_rows_axpby(A.ctypes.data, B.ctypes.data, cptr, N, K, _ld(A), _ld(B), ldcin,
+                                      LAYOUTS[layout], DTYPES[dtype], float(alpha), float(beta), rows.ctypes.data,
+                                      rows.size, out16.ctypes.data,
+                                      out64.ctypes.data if out64 is not None else None, N, int(nthreads))
+    if used < 0:
+        raise MemoryError("oracle allocation failed")
+    return (out16, out64) if want_f64 else out16
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "max_threads", "LAYOUTS", "DTYPES"]
+__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "max_threads", "LAYOUTS",
+           "DTYPES"]

@@ -261,3 +261,55 @@ void oracle_encode_array(const double* in, uint16_t* out, int64_t n, int dtype)
     for (int64_t i = 0; i < n; ++i)
         out[i] = (dtype == OR_BF16) ? oracle_f64_to_bf16(in[i]) : oracle_f64_to_f16(in[i]);
 }
+
+/* C = alpha * (A·B) + beta * Cin, the accumulating form of the contraction ("张量缩并：mma
+ * 语法" introduces it as C += A × B; alpha = 1, beta = 1 is that form, alpha = 1, beta = 0
+ * the plain product).  Same sum as oracle_gemm_rows, then out = alpha * sum + beta * Cin in
+ * fp64 and one rounding.  Cin is the logical M x N input, row-major with leading dimension
+ * ldcin; with beta == 0 it is not read (may be NULL).  Rows `rows[i]` of the result are
+ * written row-major at out16/out64 + i*ldo. */
+int oracle_gemm_rows_axpby(const uint16_t* A, const uint16_t* B, const uint16_t* Cin, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldcin, int layout, int dtype, double alpha,
+                           double beta, const int64_t* rows, int64_t nrows, uint16_t* out16, double* out64,
+                           int64_t ldo, int nthreads)
+{
+    double* T = (double*)malloc(65536 * sizeof(double));
+    if (!T) return -1;
+    build_table(T, dtype);
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+        double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t i = 0; i < nrows; ++i) {
+            row_f64(T, A, B, rows[i], N, K, lda, ldb, layout, acc);
+            for (int64_t n = 0; n < N; ++n) {
+                double v = alpha * acc[n];
+                if (beta != 0.0) v += beta * T[Cin[rows[i] * ldcin + n]];
+                if (out64) out64[i * ldo + n] = v;
+                if (out16) out16[i * ldo + n] = (dtype == OR_BF16) ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+            }
+        }
+        free(acc);
+    }
+#else
+    (void)nthreads;
+    double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+    for (int64_t i = 0; i < nrows; ++i) {
+        row_f64(T, A, B, rows[i], N, K, lda, ldb, layout, acc);
+        for (int64_t n = 0; n < N; ++n) {
+            double v = alpha * acc[n];
+            if (beta != 0.0) v += beta * T[Cin[rows[i] * ldcin + n]];
+            if (out64) out64[i * ldo + n] = v;
+            if (out16) out16[i * ldo + n] = (dtype == OR_BF16) ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+        }
+    }
+    free(acc);
+#endif
+    free(T);
+    return used;
+}

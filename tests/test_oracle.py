@@ -263,3 +263,49 @@ def test_overflow_rounds_to_inf():
     B = torch.full((4, 1), 200.0, dtype=torch.float16)  # 4 * 40000 = 160000 > 65504
     C = oracle.decode(oracle.gemm(A, B, "NN", "f16"), "f16")
     assert np.isposinf(C[0, 0])
+
+
+# ------------------------------------------------------------------ alpha / beta (C = alpha A·B + beta C)
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_axpby_closed_forms(layout, dtype):
+    M, N, K = 33, 47, 29
+    A, B = make_inputs(M, N, K, layout, dtype, "int", seed=31)
+    Cin, _ = make_inputs(M, N, N, "NN", dtype, "normal", seed=32)  # any M x N codes
+    plain = oracle.gemm(A, B, layout, dtype)
+    # alpha = 1, beta = 0 is the plain product (Cin not read: pass garbage-free None)
+    assert np.array_equal(oracle.gemm_axpby(A, B, layout, dtype, 1.0, 0.0), plain)
+    # alpha = 0, beta = 1 returns Cin unchanged (every code re-rounds to itself)
+    assert np.array_equal(oracle.gemm_axpby(A, B, layout, dtype, 0.0, 1.0, Cin), oracle._codes(Cin))
+    # alpha = 2 doubles the exact sum (a power-of-two scale is exact before the rounding)
+    codes, f64 = oracle.gemm_axpby(A, B, layout, dtype, 2.0, 0.0, want_f64=True)
+    _, base = oracle.gemm(A, B, layout, dtype, want_f64=True)
+    assert np.array_equal(f64, 2.0 * base) and np.array_equal(codes, oracle.encode(2.0 * base, dtype))
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+def test_axpby_accumulate_form_against_numpy(dtype):
+    """C += A·B (alpha = beta = 1) twice, against an independent numpy fp64 evaluation;
+    small integers keep every value exact, so the codes must match bit for bit."""
+    M, N, K = 40, 24, 12
+    A, B = make_inputs(M, N, K, "TN", dtype, "int", seed=33)
+    C0, _ = make_inputs(M, N, N, "NN", dtype, "int", seed=34)
+    A64, B64 = A.to(torch.float64).numpy(), B.to(torch.float64).numpy().T
+    C1 = oracle.gemm_axpby(A, B, "TN", dtype, 1.0, 1.0, C0)
+    C2 = oracle.gemm_axpby(A, B, "TN", dtype, 1.0, 1.0, C1)
+    ref2 = 2.0 * (A64 @ B64) + C0.to(torch.float64).numpy()
+    assert np.array_equal(oracle.decode(C2, dtype), ref2)
+    # beta = -1 with Cin = A·B cancels exactly
+    AB = oracle.gemm(A, B, "TN", dtype)
+    assert np.all(oracle.decode(oracle.gemm_axpby(A, B, "TN", dtype, 1.0, -1.0, AB), dtype) == 0.0)
+
+
+def test_axpby_general_scalars_match_numpy_within_rounding():
+    M, N, K = 20, 30, 50
+    A, B = make_inputs(M, N, K, "NN", "f16", "normal", seed=35)
+    Cin, _ = make_inputs(M, N, N, "NN", "f16", "normal", seed=36)
+    _, f64 = oracle.gemm_axpby(A, B, "NN", "f16", 0.75, -1.25, Cin, want_f64=True)
+    ref = 0.75 * (A.to(torch.float64).numpy() @ B.to(torch.float64).numpy()) - 1.25 * Cin.to(torch.float64).numpy()
+    np.testing.assert_allclose(f64, ref, rtol=1e-13, atol=1e-13)
