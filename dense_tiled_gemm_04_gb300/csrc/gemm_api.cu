@@ -7,6 +7,7 @@
 
 #include <algorithm>
 #include <cstdint>
+#include <cmath>
 #include <cstring>
 #include <mutex>
 #include <new>
@@ -47,11 +48,19 @@ struct TmapKey {
     uint64_t inner, outer, pitch_bytes;
     uint32_t box_inner, box_outer;
     int32_t dtype;
+    int32_t swizzle;
     bool operator==(const TmapKey& o) const
     {
         return ptr == o.ptr && inner == o.inner && outer == o.outer && pitch_bytes == o.pitch_bytes &&
-               box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype;
+               box_inner == o.box_inner && box_outer == o.box_outer && dtype == o.dtype && swizzle == o.swizzle;
     }
+};
+
+// Epilogue of a launch: C = alpha * A·B + beta * C, C row-major or column-major.
+struct Epilogue {
+    float alpha = 1.0f;
+    float beta = 0.0f;
+    int32_t col_major = 0;
 };
 
 struct TmapEntry {
@@ -141,12 +150,13 @@ struct DeviceGuard {
 };
 
 // Encode a 2-D row-major tensor map: `inner` contiguous elements per row, `outer` rows
-// `pitch_bytes` apart, box = box_inner x box_outer, 128-byte swizzle, zero fill outside.
-// With a cache (a handle's), identical requests reuse the earlier encoding.
+// `pitch_bytes` apart, box = box_inner x box_outer, 128-byte swizzle (or none), zero fill
+// outside.  With a cache (a handle's), identical requests reuse the earlier encoding.
 bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, uint64_t outer, uint64_t pitch_bytes,
-              uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out)
+              uint32_t box_inner, uint32_t box_outer, int32_t dtype, CUtensorMap* out,
+              CUtensorMapSwizzle swizzle = CU_TENSOR_MAP_SWIZZLE_128B)
 {
-    const TmapKey key{ptr, inner, outer, pitch_bytes, box_inner, box_outer, dtype};
+    const TmapKey key{ptr, inner, outer, pitch_bytes, box_inner, box_outer, dtype, static_cast<int32_t>(swizzle)};
     if (cache)
         for (const TmapEntry& e : *cache)
             if (e.key == key) {
@@ -161,8 +171,7 @@ bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, ui
     const CUtensorMapDataType dt =
         dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
     if (g_encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                 CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-                 CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
+                 swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
     if (cache) {
         if (static_cast<int>(cache->size()) >= kTmapCacheMax) cache->clear();
@@ -306,14 +315,16 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     plan->smem_bytes = kc.smem;
 }
 
+// c_col_major: C is stored N x M (C[m, n] at C + n * ldc + m), so ldc must cover M.
 gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
-                            int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype)
+                            int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
+                            bool c_col_major = false)
 {
     if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
     if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
-    if (!C || ldc < N) return GEMM_ERR_INVALID_ARG;
+    if (!C || ldc < (c_col_major ? M : N)) return GEMM_ERR_INVALID_ARG;
     if (K > 0) {
         if (!A || !B) return GEMM_ERR_INVALID_ARG;
         if (lda < K) return GEMM_ERR_INVALID_ARG;
@@ -343,16 +354,18 @@ gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void
 gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Workspace* ws,
                           std::vector<TmapEntry>* cache, int32_t* err,
                           const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                          int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream)
+                          int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream,
+                          const Epilogue& ep = Epilogue())
 {
     if (K == 0) {
         int blocks = static_cast<int>(cdiv(M * N, 256));
         const int cap = dev.num_sms * 8;
         if (blocks > cap) blocks = cap;
+        uint16_t* c16 = static_cast<uint16_t*>(C);
         if (dtype == GEMM_DTYPE_BF16)
-            dtg::zero_fill_kernel<__nv_bfloat16><<<blocks, 256, 0, stream>>>(static_cast<__nv_bfloat16*>(C), M, N, ldc);
+            dtg::scale_c_kernel<true><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
         else
-            dtg::zero_fill_kernel<__half><<<blocks, 256, 0, stream>>>(static_cast<__half*>(C), M, N, ldc);
+            dtg::scale_c_kernel<false><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
         return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
@@ -372,7 +385,13 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     } else {
         if (!get_tmap(cache, B, K, N, ldb * 2, dtg::kBK, kc.b_box, dtype, &tB)) return GEMM_ERR_CUDA;
     }
-    if (!get_tmap(cache, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) return GEMM_ERR_CUDA;
+    if (ep.col_major) {
+        // C stored N x M: boxes of 32 (M, contiguous) x 64 (N), unswizzled.
+        if (!get_tmap(cache, C, M, N, ldc * 2, 32, dtg::kEpiCols, dtype, &tC, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_ERR_CUDA;
+    } else if (!get_tmap(cache, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) {
+        return GEMM_ERR_CUDA;
+    }
 
     KernelParams kp;
     kp.M = static_cast<int32_t>(M);
@@ -393,6 +412,9 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.sk_extra = plan.sk_extra;
     kp.ws = ws ? ws->partials : nullptr;
     kp.counters = ws ? ws->counters : nullptr;
+    kp.alpha = ep.alpha;
+    kp.beta = ep.beta;
+    kp.c_col_major = ep.col_major;
 
     void* args[] = {&tA, &tB, &tC, &kp};
     cudaLaunchConfig_t cfg;
@@ -523,6 +545,25 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
     if (!g.ok) return GEMM_ERR_CUDA;
     return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, A, B, C, M, N, K, lda, ldb, ldc, layout, dtype,
                        static_cast<cudaStream_t>(stream));
+}
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream)
+{
+    if (!h || !args) return GEMM_ERR_INVALID_ARG;
+    const gemm_args_t& a = *args;
+    if (a.c_col_major != 0 && a.c_col_major != 1) return GEMM_ERR_INVALID_ARG;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.beta)) return GEMM_ERR_INVALID_ARG;
+    const gemm_status_t v =
+        validate_args(a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb, a.ldc, a.layout, a.dtype, a.c_col_major != 0);
+    if (v != GEMM_OK || a.M == 0 || a.N == 0) return v;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    Epilogue ep;
+    ep.alpha = a.alpha;
+    ep.beta = a.beta;
+    ep.col_major = a.c_col_major;
+    return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb,
+                       a.ldc, a.layout, a.dtype, static_cast<cudaStream_t>(stream), ep);
 }
 
 gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,

@@ -90,6 +90,10 @@ struct KernelParams {
                                  // take sk_base + 1 blocks, the others sk_base
     float* ws;                   // partial sums: [2 * units][ranks][BN / 4][128] float4
     int32_t* counters;           // arrivals per stream-K tile and CTA rank (kept at zero)
+    // epilogue: C = alpha * A·B + beta * C (C read only when beta != 0); C stored row-major,
+    // or column-major (C[m, n] at C + n * ldc + m) with c_col_major
+    float alpha, beta;
+    int32_t c_col_major;
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -260,19 +264,80 @@ __device__ __forceinline__ uint32_t pack2(uint32_t lo_bits, uint32_t hi_bits)
     }
 }
 
-// Write the 32-row x 64-column box of C at (row y, column x) that this warp holds (lane =
-// row, v = the 64 fp32 accumulator bit patterns of that row).  Normally the box goes
-// through a 128-byte-swizzled staging buffer and one TMA store, which drops rows >= M and
-// columns >= N (the masked write-back of "NineToothed GEMM 语法入门" §5).  A TMA store
-// clips the inner dimension only to 16-byte granules, so when N is not a multiple of 8
-// the box that straddles column N is written with plain masked stores instead.  Returns
-// true if the staging buffer was used (the caller then alternates buffers).
 template <bool BF16>
-__device__ __forceinline__ bool store_box(const uint32_t (&v)[64], int32_t x, int32_t y, int lane,
-                                          uint32_t stg, const CUtensorMap* tmC, const KernelParams& p)
+__device__ __forceinline__ float load16(const uint16_t* src)
 {
+    const uint16_t b = *src;
+    if constexpr (BF16)
+        return __bfloat162float(__ushort_as_bfloat16(b));
+    else
+        return __half2float(__ushort_as_half(b));
+}
+
+template <bool BF16>
+__device__ __forceinline__ uint16_t cvt16(uint32_t f_bits)
+{
+    if constexpr (BF16)
+        return __bfloat16_as_ushort(__float2bfloat16_rn(__uint_as_float(f_bits)));
+    else
+        return __half_as_ushort(__float2half_rn(__uint_as_float(f_bits)));
+}
+
+// Write the 32-row x 64-column box of C at (row y, column x) that this warp holds (lane =
+// row, v = the 64 fp32 accumulator bit patterns of that row; v is scaled in place).
+//  * C = alpha * acc + beta * C: "张量缩并：mma 语法" states the contraction as C += A × B
+//    (alpha = beta = 1); the existing C is read only when beta != 0.
+//  * Row-major C: the box goes through a 128-byte-swizzled staging buffer and one TMA store,
+//    which drops rows >= M and columns >= N (the masked write-back of "NineToothed GEMM 语法
+//    入门" §5).  A TMA store clips the inner dimension only to 16-byte granules, so when N
+//    is not a multiple of 8 the box that straddles column N is written with plain masked
+//    stores instead.
+//  * Column-major C (the same page's transposed store, mma.store.transp): the box is staged
+//    transposed (64 rows of n, 32 m values each) and stored through a tensor map of C's
+//    storage; a box straddling a ragged M (M % 8 != 0) is written with plain stores.
+// Returns true if the staging buffer was used (the caller then alternates buffers).
+template <bool BF16>
+__device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t y, int lane, uint32_t stg,
+                                          const CUtensorMap* tmC, const KernelParams& p)
+{
+    const int64_t row = static_cast<int64_t>(y) + lane;  // this thread's output row m
+    if (p.alpha != 1.0f || p.beta != 0.0f) {
+        const uint16_t* c16 = static_cast<const uint16_t*>(p.C);
+#pragma unroll
+        for (int i = 0; i < 64; ++i) {
+            float f = p.alpha * __uint_as_float(v[i]);
+            const int64_t col = static_cast<int64_t>(x) + i;
+            if (p.beta != 0.0f && row < p.M && col < p.N)
+                f = fmaf(p.beta, load16<BF16>(p.c_col_major ? c16 + col * p.ldc + row : c16 + row * p.ldc + col),
+                         f);
+            v[i] = __float_as_uint(f);
+        }
+    }
+    if (p.c_col_major) {
+        if ((p.M & 7) != 0 && y + 32 > p.M) {
+            if (row < p.M) {
+                uint16_t* c16 = static_cast<uint16_t*>(p.C);
+#pragma unroll
+                for (int i = 0; i < 64; ++i)
+                    if (x + i < p.N) c16[static_cast<int64_t>(x + i) * p.ldc + row] = cvt16<BF16>(v[i]);
+            }
+            return false;
+        }
+        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        __syncwarp();
+        // Dense staging box: (n, m) at n * 64 B + m * 2 B.
+#pragma unroll
+        for (int i = 0; i < 64; ++i)
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stg + i * 64 + lane * 2), "h"(cvt16<BF16>(v[i])) : "memory");
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            if (x < p.N && y < p.M) ptx::tma_store_2d(tmC, stg, y, x);
+            ptx::bulk_commit_group();
+        }
+        return true;
+    }
     if ((p.N & 7) != 0 && x + kEpiCols > p.N) {
-        const int64_t row = static_cast<int64_t>(y) + lane;
         if (row < p.M && x < p.N) {
             uint16_t* crow = static_cast<uint16_t*>(p.C) + row * p.ldc;
 #pragma unroll
@@ -301,12 +366,12 @@ __device__ __forceinline__ bool store_box(const uint32_t (&v)[64], int32_t x, in
     // finished reading it.
     if (lane == 0) ptx::bulk_wait_group_read<1>();
     __syncwarp();
-    const uint32_t row = stg + lane * 128;
+    const uint32_t srow = stg + lane * 128;
 #pragma unroll
     for (int ch = 0; ch < 8; ++ch) {
         // 16-byte chunk ch of this row lands at chunk (ch ^ row%8): the 128-byte swizzle
         // the TMA store expects.
-        const uint32_t addr = row + ((ch ^ (lane & 7)) << 4);
+        const uint32_t addr = srow + ((ch ^ (lane & 7)) << 4);
         ptx::st_shared_v4(addr, pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]), pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]),
                           pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]), pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]));
     }
@@ -742,15 +807,18 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-// C[M x N] = 0 for the K == 0 case (the empty sum).  Grid-stride over rows and columns.
-template <typename T>
-__global__ void zero_fill_kernel(T* C, int64_t M, int64_t N, int64_t ldc)
+// The K == 0 case: A·B is the empty sum, so C = beta * C (C = 0 when beta == 0, without
+// reading C).  Grid-stride over the M x N elements, row-major or column-major storage.
+template <bool BF16>
+__global__ void scale_c_kernel(uint16_t* C, int64_t M, int64_t N, int64_t ldc, int32_t col_major, float beta)
 {
     const int64_t total = M * N;
     for (int64_t i = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; i < total;
          i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
         const int64_t m = i / N, n = i - m * N;
-        C[m * ldc + n] = T(0.0f);
+        uint16_t* c = col_major ? C + n * ldc + m : C + m * ldc + n;
+        const float f = beta != 0.0f ? beta * load16<BF16>(c) : 0.0f;
+        *c = cvt16<BF16>(__float_as_uint(f));
     }
 }
 

@@ -32,6 +32,14 @@ class gemm_plan_t(ctypes.Structure):
                 ("dp_tiles", ctypes.c_int64), ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64)]
 
 
+class gemm_args_t(ctypes.Structure):
+    _fields_ = [("A", ctypes.c_void_p), ("B", ctypes.c_void_p), ("C", ctypes.c_void_p),
+                ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
+                ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
+                ("layout", ctypes.c_int32), ("dtype", ctypes.c_int32),
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("c_col_major", ctypes.c_int32)]
+
+
 class GemmError(RuntimeError):
     def __init__(self, status: int, what: str = ""):
         self.status = status
@@ -59,6 +67,7 @@ def load() -> ctypes.CDLL:
         "gemm_destroy": ([p], i32),
         "gemm_run": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
         "gemm_run_host": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
+        "gemm_run_ex": ([p, ctypes.POINTER(gemm_args_t), p], i32),
         "gemm_sync_status": ([p, p], i32),
         "gemm_error_info": ([p, ctypes.POINTER(i32)], i32),
         "gemm_set_option": ([p, i32, i64], i32),
@@ -202,6 +211,13 @@ class Gemm:
         if st != OK:
             raise GemmError(st, "gemm_run")
         return C
+
+    def run_ex_raw(self, A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int, alpha: float,
+                   beta: float, c_col_major: int, stream: int) -> int:
+        """gemm_run_ex on raw device addresses: C = alpha * A·B + beta * C (row- or column-major C)."""
+        a = gemm_args_t(A or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype, alpha, beta,
+                        c_col_major)
+        return int(self._lib.gemm_run_ex(self._h, ctypes.byref(a), stream or None))
 
     def run_host(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, layout: str = "NN", stream=None) -> int:
         """gemm_run_host on CPU tensors (pin them for DMA copies); synchronous; returns the status."""

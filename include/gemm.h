@@ -119,6 +119,32 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C,
                        int64_t lda, int64_t ldb, int64_t ldc,
                        gemm_layout_t layout, gemm_dtype_t dtype, void* stream);
 
+/* The general form: C = alpha * A·B + beta * C, with C stored row-major or column-major.
+ *   - "张量缩并：mma 语法" states the contraction as C += A × B (alpha = beta = 1); its
+ *     transposed store (mma.store.transp) writes the result with rows and columns swapped,
+ *     which is c_col_major here.
+ *   - alpha, beta: finite fp32 scalars.  The result is alpha * acc + beta * C_old in fp32,
+ *     rounded once to the output type.  With beta == 0, C is not read (it may hold
+ *     anything, NaN included).  K == 0 gives C = beta * C.
+ *   - c_col_major = 0: C[m, n] at C + m * ldc + n (ldc >= N), as in gemm_run.
+ *     c_col_major = 1: C[m, n] at C + n * ldc + m (ldc >= M; C stored N x M row-major).
+ *   - A, B, layouts, alignment rules and status codes are those of gemm_run.
+ * alpha = 1, beta = 0, c_col_major = 0 is exactly gemm_run. */
+typedef struct {
+    const void* A;
+    const void* B;
+    void* C;
+    int64_t M, N, K;
+    int64_t lda, ldb, ldc;
+    gemm_layout_t layout;
+    gemm_dtype_t dtype;
+    float alpha;
+    float beta;
+    int32_t c_col_major;
+} gemm_args_t;
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream);
+
 /* Same operation on HOST buffers (pinned memory lets the copies run as DMA): copies A and
  * B to handle-owned device buffers on `stream`, runs the kernel, copies C back (only the
  * M x N window, never the row padding) and synchronises the stream.  Returns the

@@ -51,6 +51,9 @@ def test_null_handle_is_rejected_without_a_gpu(lib):
     assert so.gemm_set_option(None, 0, 0) == lib.ERR_INVALID_ARG
     assert so.gemm_destroy(None) == lib.OK
     assert so.gemm_create(None, 0) == lib.ERR_INVALID_ARG
+    assert so.gemm_run_ex(None, None, None) == lib.ERR_INVALID_ARG
+    args = lib.gemm_args_t(None, None, None, 8, 8, 8, 8, 8, 8, 0, 0, 1.0, 0.0, 0)
+    assert so.gemm_run_ex(None, args, None) == lib.ERR_INVALID_ARG
 
 
 def test_create_without_a_gpu_reports_an_error(lib):
