@@ -19,7 +19,7 @@ from dataclasses import dataclass, replace
 
 import torch
 
-TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16}
+TORCH_DTYPES = {"f16": torch.float16, "bf16": torch.bfloat16, "e4m3": torch.float8_e4m3fn, "e5m2": torch.float8_e5m2}
 
 
 @dataclass(frozen=True)
@@ -79,7 +79,7 @@ def _padded(x: torch.Tensor, ld: int | None) -> torch.Tensor:
         return x.contiguous()
     if ld < cols:
         raise ValueError(f"leading dimension {ld} < row length {cols}")
-    buf = torch.full((rows, ld), float("nan"), dtype=x.dtype)
+    buf = torch.full((rows, ld), float("nan"), dtype=torch.float32).to(x.dtype)
     buf[:, :cols] = x
     return buf[:, :cols]
 

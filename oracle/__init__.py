@@ -30,7 +30,7 @@ _SRC = os.path.join(_HERE, "gemm_oracle.c")
 _LIB = os.path.join(_HERE, "liboracle_gemm.so")
 
 LAYOUTS = {"NN": 0, "TN": 1}
-DTYPES = {"f16": 0, "bf16": 1}
+DTYPES = {"f16": 0, "bf16": 1, "e4m3": 2, "e5m2": 3}
 
 _lib = None
 
@@ -71,6 +71,13 @@ def _load():
     lib.oracle_gemm_rows_axpby.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_double, ctypes.c_double, p, i64, p, p, i64, ctypes.c_int]
     lib.oracle_gemm_rows_axpby.restype = ctypes.c_int
+    lib.oracle_gemm_rows_typed.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
+                                           ctypes.c_double, ctypes.c_double, p, i64, p, p, i64, ctypes.c_int]
+    lib.oracle_gemm_rows_typed.restype = ctypes.c_int
+    lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e4m3_to_f64.restype = ctypes.c_double
+    lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e5m2_to_f64.restype = ctypes.c_double
     lib.oracle_decode_array.argtypes = [p, p, i64, ctypes.c_int]
     lib.oracle_decode_array.restype = None
     lib.oracle_encode_array.argtypes = [p, p, i64, ctypes.c_int]
@@ -91,6 +98,9 @@ def _codes(x) -> np.ndarray:
         raise TypeError(f"unsupported numpy dtype {x.dtype}")
     import torch  # torch CPU tensors only: bit patterns are taken unchanged
 
+    if x.dtype in (torch.float8_e4m3fn, torch.float8_e5m2, torch.uint8):
+        # 8-bit codes widened to 16 bits (the C side reads the low byte)
+        return x.detach().cpu().view(torch.uint8).numpy().astype(np.uint16)
     if x.dtype not in (torch.float16, torch.bfloat16, torch.int16):
         raise TypeError(f"unsupported torch dtype {x.dtype}")
     return x.detach().cpu().view(torch.int16).numpy().view(np.uint16)
@@ -218,9 +228,38 @@ def gemm_axpby(A, B, layout: str, dtype: str, alpha: float, beta: float, Cin=Non
     return (out16, out64) if want_f64 else out16
 
 
+def gemm_typed(A, B, layout: str, in_dtype: str, out_dtype: str, alpha: float = 1.0, beta: float = 0.0, Cin=None,
+               rows=None, want_f64: bool = False, nthreads: int = 0):
+    """alpha * (A·B) + beta * Cin with inputs of type ``in_dtype`` (f16, bf16, e4m3, e5m2) and
+    the result / Cin of type ``out_dtype`` (f16, bf16).  Rounded codes for ``rows`` (default
+    all), or ``(codes, f64)``."""
+    lib = _load()
+    A, B = _codes(A), _codes(B)
+    M, N, K = _shape_check(A, B, layout)
+    A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    rows = np.ascontiguousarray(rows.astype(np.int64))
+    if beta != 0.0:
+        Cin = np.ascontiguousarray(_codes(Cin))
+        if Cin.shape != (M, N):
+            raise ValueError(f"Cin must be {M} x {N}")
+        cptr, ldcin = Cin.ctypes.data, max(N, 1)
+    else:
+        cptr, ldcin = None, 1
+    out16 = np.zeros((rows.size, N), dtype=np.uint16)
+    out64 = np.zeros((rows.size, N), dtype=np.float64) if want_f64 else None
+    used = lib.oracle_gemm_rows_typed(A.ctypes.data, B.ctypes.data, cptr, N, K, _ld(A), _ld(B), ldcin,
+                                      LAYOUTS[layout], DTYPES[in_dtype], DTYPES[out_dtype], float(alpha), float(beta),
+                                      rows.ctypes.data, rows.size, out16.ctypes.data,
+                                      out64.ctypes.data if out64 is not None else None, N, int(nthreads))
+    if used < 0:
+        raise MemoryError("oracle allocation failed")
+    return (out16, out64) if want_f64 else out16
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "max_threads", "LAYOUTS",
-           "DTYPES"]
+__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "gemm_typed", "max_threads",
+           "LAYOUTS", "DTYPES"]

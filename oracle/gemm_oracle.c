@@ -42,7 +42,7 @@
 #endif
 
 enum { OR_LAYOUT_NN = 0, OR_LAYOUT_TN = 1 };
-enum { OR_F16 = 0, OR_BF16 = 1 };
+enum { OR_F16 = 0, OR_BF16 = 1, OR_E4M3 = 2, OR_E5M2 = 3 };
 
 /* ---------------------------------------------------------------- decode */
 
@@ -73,6 +73,40 @@ double oracle_bf16_to_f64(uint16_t b)
         v = f ? NAN : INFINITY;
     else
         v = ldexp((double)(f | 0x80), e - 134); /* (128+f) * 2^(e-127-7) */
+    return sign ? -v : v;
+}
+
+/* 8-bit floats (inputs only), from their definitions:
+ *   E4M3: 1 sign, 4 exponent bits (bias 7), 3 fraction bits; no infinities; exponent and
+ *         fraction all ones (S.1111.111) is NaN; largest finite 448.
+ *   E5M2: 1 sign, 5 exponent bits (bias 15), 2 fraction bits; IEEE-style inf and NaN. */
+double oracle_e4m3_to_f64(uint8_t c)
+{
+    const int sign = (c >> 7) & 1;
+    const int e = (c >> 3) & 0xf;
+    const int f = c & 0x7;
+    double v;
+    if (e == 15 && f == 7)
+        v = NAN;
+    else if (e == 0)
+        v = ldexp((double)f, -9);             /* subnormal: f * 2^(1-7-3) */
+    else
+        v = ldexp((double)(f | 0x8), e - 10); /* (8+f) * 2^(e-7-3) */
+    return sign ? -v : v;
+}
+
+double oracle_e5m2_to_f64(uint8_t c)
+{
+    const int sign = (c >> 7) & 1;
+    const int e = (c >> 2) & 0x1f;
+    const int f = c & 0x3;
+    double v;
+    if (e == 0)
+        v = ldexp((double)f, -16);            /* subnormal: f * 2^(1-15-2) */
+    else if (e == 31)
+        v = f ? NAN : INFINITY;
+    else
+        v = ldexp((double)(f | 0x4), e - 17); /* (4+f) * 2^(e-15-2) */
     return sign ? -v : v;
 }
 
@@ -139,10 +173,17 @@ uint16_t oracle_f64_to_bf16(double x)
 
 /* ---------------------------------------------------------------- GEMM */
 
+/* Value of every input code; 8-bit formats use the low byte of the 16-bit code. */
 static void build_table(double* t, int dtype)
 {
-    for (uint32_t c = 0; c < 65536u; ++c)
-        t[c] = (dtype == OR_BF16) ? oracle_bf16_to_f64((uint16_t)c) : oracle_f16_to_f64((uint16_t)c);
+    for (uint32_t c = 0; c < 65536u; ++c) {
+        if (dtype == OR_E4M3)
+            t[c] = oracle_e4m3_to_f64((uint8_t)(c & 0xffu));
+        else if (dtype == OR_E5M2)
+            t[c] = oracle_e5m2_to_f64((uint8_t)(c & 0xffu));
+        else
+            t[c] = (dtype == OR_BF16) ? oracle_bf16_to_f64((uint16_t)c) : oracle_f16_to_f64((uint16_t)c);
+    }
 }
 
 /* One output row m of the fp64 accumulator: acc[n] for n < N. */
@@ -252,8 +293,14 @@ int oracle_max_threads(void)
 /* Batch forms of the codecs, for the exhaustive codec tests. */
 void oracle_decode_array(const uint16_t* in, double* out, int64_t n, int dtype)
 {
-    for (int64_t i = 0; i < n; ++i)
-        out[i] = (dtype == OR_BF16) ? oracle_bf16_to_f64(in[i]) : oracle_f16_to_f64(in[i]);
+    for (int64_t i = 0; i < n; ++i) {
+        if (dtype == OR_E4M3)
+            out[i] = oracle_e4m3_to_f64((uint8_t)(in[i] & 0xffu));
+        else if (dtype == OR_E5M2)
+            out[i] = oracle_e5m2_to_f64((uint8_t)(in[i] & 0xffu));
+        else
+            out[i] = (dtype == OR_BF16) ? oracle_bf16_to_f64(in[i]) : oracle_f16_to_f64(in[i]);
+    }
 }
 
 void oracle_encode_array(const double* in, uint16_t* out, int64_t n, int dtype)
@@ -311,5 +358,55 @@ int oracle_gemm_rows_axpby(const uint16_t* A, const uint16_t* B, const uint16_t*
     free(acc);
 #endif
     free(T);
+    return used;
+}
+
+/* C = alpha * (A·B) + beta * Cin with input codes of type in_dtype (f16, bf16, or an 8-bit
+ * format whose codes are passed widened to 16 bits) and output / Cin of type out_dtype
+ * (f16 or bf16).  The 8-bit contraction with scales ("张量缩并：mma 语法": each result is
+ * scaled by sc_a and sc_b after the contraction) is alpha = sc_a * sc_b (* a user alpha). */
+int oracle_gemm_rows_typed(const uint16_t* A, const uint16_t* B, const uint16_t* Cin, int64_t N, int64_t K,
+                           int64_t lda, int64_t ldb, int64_t ldcin, int layout, int in_dtype, int out_dtype,
+                           double alpha, double beta, const int64_t* rows, int64_t nrows, uint16_t* out16,
+                           double* out64, int64_t ldo, int nthreads)
+{
+    double* T = (double*)malloc(65536 * sizeof(double));
+    double* TC = (double*)malloc(65536 * sizeof(double));
+    if (!T || !TC) {
+        free(T);
+        free(TC);
+        return -1;
+    }
+    build_table(T, in_dtype);
+    build_table(TC, out_dtype);
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+#else
+    (void)nthreads;
+    {
+#endif
+        double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t i = 0; i < nrows; ++i) {
+            row_f64(T, A, B, rows[i], N, K, lda, ldb, layout, acc);
+            for (int64_t n = 0; n < N; ++n) {
+                double v = alpha * acc[n];
+                if (beta != 0.0) v += beta * TC[Cin[rows[i] * ldcin + n]];
+                if (out64) out64[i * ldo + n] = v;
+                if (out16)
+                    out16[i * ldo + n] = (out_dtype == OR_BF16) ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+            }
+        }
+        free(acc);
+    }
+    free(T);
+    free(TC);
     return used;
 }

@@ -309,3 +309,52 @@ def test_axpby_general_scalars_match_numpy_within_rounding():
     _, f64 = oracle.gemm_axpby(A, B, "NN", "f16", 0.75, -1.25, Cin, want_f64=True)
     ref = 0.75 * (A.to(torch.float64).numpy() @ B.to(torch.float64).numpy()) - 1.25 * Cin.to(torch.float64).numpy()
     np.testing.assert_allclose(f64, ref, rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ 8-bit inputs
+
+
+@pytest.mark.parametrize("fmt,tdt", [("e4m3", torch.float8_e4m3fn), ("e5m2", torch.float8_e5m2)])
+def test_fp8_decode_every_code_matches_torch(fmt, tdt):
+    codes = np.arange(256, dtype=np.uint16)
+    mine = oracle.decode(codes, fmt)
+    ref = torch.from_numpy(codes.astype(np.uint8)).view(tdt).to(torch.float64).numpy()
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(mine), nan)
+    assert np.array_equal(mine[~nan], ref[~nan])
+    assert np.array_equal(np.signbit(mine[~nan]), np.signbit(ref[~nan]))
+
+
+def test_fp8_closed_forms():
+    # E4M3 largest finite 448 (0x7e), smallest subnormal 2^-9 (0x01), NaN 0x7f; E5M2 inf 0x7c.
+    assert oracle.decode([0x7E, 0x01, 0x38], "e4m3").tolist() == [448.0, 2.0 ** -9, 1.0]
+    assert np.isnan(oracle.decode([0x7F], "e4m3")[0])
+    assert oracle.decode([0x7B, 0x01, 0x3C], "e5m2").tolist() == [57344.0, 2.0 ** -16, 1.0]
+    assert np.isposinf(oracle.decode([0x7C], "e5m2")[0])
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("out", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_fp8_gemm_equals_16bit_gemm_on_exact_values(fmt, out, layout):
+    # Integers in {-2..2} are exact in every format: the 8-bit product must equal the
+    # 16-bit product of the same values, code for code.
+    M, N, K = 37, 45, 70
+    A8, B8 = make_inputs(M, N, K, layout, fmt, "int", seed=41)
+    A16, B16 = A8.to(torch.float32).to(torch.bfloat16 if out == "bf16" else torch.float16), \
+        B8.to(torch.float32).to(torch.bfloat16 if out == "bf16" else torch.float16)
+    assert np.array_equal(oracle.gemm_typed(A8, B8, layout, fmt, out), oracle.gemm(A16, B16, layout, out))
+
+
+def test_fp8_scales_and_random_values():
+    M, N, K = 30, 40, 64
+    A, B = make_inputs(M, N, K, "TN", "e4m3", "normal", seed=42)
+    sa, sb = 0.5, 8.0  # powers of two: the scaled sum is exact before the rounding
+    codes, f64 = oracle.gemm_typed(A, B, "TN", "e4m3", "bf16", alpha=sa * sb, want_f64=True)
+    ref = A.to(torch.float64).numpy() @ B.to(torch.float64).numpy().T
+    np.testing.assert_allclose(f64, sa * sb * ref, rtol=1e-13, atol=1e-13)
+    assert np.array_equal(codes, oracle.encode(f64, "bf16"))
+    # beta folds in a 16-bit C of the output type
+    Cin, _ = make_inputs(M, N, N, "NN", "bf16", "int", seed=43)
+    _, f64b = oracle.gemm_typed(A, B, "TN", "e4m3", "bf16", alpha=1.0, beta=-1.0, Cin=Cin, want_f64=True)
+    np.testing.assert_allclose(f64b, ref - Cin.to(torch.float64).numpy(), rtol=1e-13, atol=1e-13)
