@@ -16,9 +16,13 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 LIB = os.path.join(HERE, "libdtgemm.so")
-SOURCES = [os.path.join(CSRC, "gemm_api.cu")]
-DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "sm103_ptx.cuh")] + [
+# One translation unit for the host side, one per operand type for the kernels: they
+# compile in parallel and link into one library.
+SOURCES = [os.path.join(CSRC, f) for f in ("gemm_api.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_e4m3.cu",
+                                           "kernels_e5m2.cu")]
+DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "sm103_ptx.cuh", "kernel_set.cuh")] + [
     os.path.join(INCLUDE, "gemm.h")]
+OBJ_DIR = os.path.join(HERE, "_build")
 
 ARCH_FLAGS = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
@@ -41,18 +45,39 @@ def up_to_date() -> bool:
     return all(os.path.getmtime(d) <= t for d in DEPENDS)
 
 
+def _run(cmd):
+    return subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.STDOUT, text=True)
+
+
 def build(force: bool = False, verbose: bool = False) -> str:
     if not force and up_to_date():
         return LIB
-    cmd = [nvcc_path(), *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-shared",
-           "-I", INCLUDE, "-I", CSRC, "-o", LIB + ".tmp", *SOURCES]
+    nvcc = nvcc_path()
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    common = [nvcc, *ARCH_FLAGS, "-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-I", INCLUDE, "-I", CSRC]
     if verbose:
-        cmd.insert(1, "-Xptxas=-v")
-    r = subprocess.run(cmd, capture_output=True, text=True)
+        common.insert(1, "-Xptxas=-v")
+    jobs = []
+    for src in SOURCES:
+        obj = os.path.join(OBJ_DIR, os.path.splitext(os.path.basename(src))[0] + ".o")
+        cmd = [*common, "-c", "-o", obj, src]
+        jobs.append((cmd, obj, _run(cmd)))
+    objs, logs, failed = [], [], None
+    for cmd, obj, proc in jobs:
+        out, _ = proc.communicate()
+        logs.append(out)
+        if proc.returncode != 0 and failed is None:
+            failed = (cmd, proc.returncode, out)
+        objs.append(obj)
+    if failed:
+        cmd, rc, out = failed
+        raise RuntimeError(f"nvcc failed ({rc}):\n{' '.join(cmd)}\n{out}")
+    link = [nvcc, *ARCH_FLAGS, "-shared", "-Xcompiler", "-fPIC", "-o", LIB + ".tmp", *objs]
+    r = subprocess.run(link, capture_output=True, text=True)
     if r.returncode != 0:
-        raise RuntimeError(f"nvcc failed ({r.returncode}):\n{' '.join(cmd)}\n{r.stdout}\n{r.stderr}")
+        raise RuntimeError(f"nvcc link failed ({r.returncode}):\n{' '.join(link)}\n{r.stdout}\n{r.stderr}")
     if verbose:
-        sys.stderr.write(r.stdout + r.stderr)
+        sys.stderr.write("".join(logs) + r.stdout + r.stderr)
     os.replace(LIB + ".tmp", LIB)
     return LIB
 

@@ -14,17 +14,17 @@
 #include <vector>
 
 #include "gemm.h"
-#include "gemm_kernel.cuh"
+#include "kernel_set.cuh"
 
 namespace {
 
+using dtg::KernelChoice;
 using dtg::KernelParams;
 
 constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
-constexpr int kPairStages = 6;
-constexpr int kNumSlots = 12;  // 3 configurations x 2 dtypes x 2 layouts
+constexpr int kNumSlots = 36;  // 3 configurations x 6 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -56,11 +56,13 @@ struct TmapKey {
     }
 };
 
-// Epilogue of a launch: C = alpha * A·B + beta * C, C row-major or column-major.
+// Epilogue of a launch: C = alpha * A·B + beta * C, C row-major or column-major, of
+// type `out` (< 0: the operand type).
 struct Epilogue {
     float alpha = 1.0f;
     float beta = 0.0f;
     int32_t col_major = 0;
+    gemm_dtype_t out = -1;
 };
 
 struct TmapEntry {
@@ -84,17 +86,6 @@ struct DeviceState {
     std::mutex mu;
     bool attrs_set[kNumSlots] = {};
     int max_clusters[kNumSlots] = {};  // pair kernels: co-resident clusters (0 = not yet queried)
-};
-
-// Which kernel instantiation a plan launches.
-struct KernelChoice {
-    int config;
-    int bm, bn;     // output tile of one CTA (1-CTA) or of the pair
-    int b_box;      // rows (TN) / columns (NN) of B one CTA loads per stage
-    int stages;
-    int cluster;    // CTAs per cluster
-    const void* fn;
-    int smem;
 };
 
 // Streams and events of gemm_run_host's copy/compute pipeline (created on first use).
@@ -168,8 +159,10 @@ bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, ui
     const cuuint64_t strides[1] = {pitch_bytes};
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
-    const CUtensorMapDataType dt =
-        dtype == GEMM_DTYPE_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    // 8-bit floats travel as bytes: TMA only moves them, the MMA interprets them.
+    const CUtensorMapDataType dt = dtype == GEMM_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                   : dtype == GEMM_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
+                                                             : CU_TENSOR_MAP_DATA_TYPE_UINT8;
     if (g_encode(out, dt, 2, const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                  swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) != CUDA_SUCCESS)
         return false;
@@ -182,41 +175,26 @@ bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, ui
 
 int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
-template <int BN, int STAGES, bool BF16, bool NN>
-KernelChoice one_cta_choice(int config)
+bool is_f8(gemm_dtype_t t) { return t == GEMM_DTYPE_E4M3 || t == GEMM_DTYPE_E5M2; }
+int elem_bytes(gemm_dtype_t t) { return is_f8(t) ? 1 : 2; }
+
+// `out` is the type of C: equal to `in` for 16-bit operands, F16 or BF16 for 8-bit ones.
+KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout)
 {
-    return {config, dtg::kBM, BN, BN, STAGES, 1,
-            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<BN, STAGES, BF16, NN, false>),
-            dtg::Smem<BN, STAGES>::kAlloc};
+    const bool nn = layout == GEMM_LAYOUT_NN, out_bf16 = out == GEMM_DTYPE_BF16;
+    switch (in) {
+    case GEMM_DTYPE_BF16: return dtg::choice_bf16(config, nn);
+    case GEMM_DTYPE_E4M3: return dtg::choice_e4m3(config, out_bf16, nn);
+    case GEMM_DTYPE_E5M2: return dtg::choice_e5m2(config, out_bf16, nn);
+    default: return dtg::choice_f16(config, nn);
+    }
 }
 
-template <bool BF16, bool NN>
-KernelChoice pair_choice()
-{
-    return {GEMM_CONFIG_256x256, 2 * dtg::kBM, 256, 128, kPairStages, 2,
-            reinterpret_cast<const void*>(&dtg::gemm_tcgen05_kernel<256, kPairStages, BF16, NN, true>),
-            dtg::Smem<128, kPairStages>::kAlloc};
-}
-
-template <bool BF16, bool NN>
-KernelChoice choice_typed(int config)
-{
-    if (config == GEMM_CONFIG_256x256) return pair_choice<BF16, NN>();
-    if (config == GEMM_CONFIG_128x128) return one_cta_choice<128, 6, BF16, NN>(config);
-    return one_cta_choice<256, 4, BF16, NN>(GEMM_CONFIG_128x256);
-}
-
-KernelChoice kernel_choice(int config, gemm_dtype_t dtype, gemm_layout_t layout)
-{
-    const bool bf16 = dtype == GEMM_DTYPE_BF16, nn = layout == GEMM_LAYOUT_NN;
-    if (bf16) return nn ? choice_typed<true, true>(config) : choice_typed<true, false>(config);
-    return nn ? choice_typed<false, true>(config) : choice_typed<false, false>(config);
-}
-
-int slot_of(int config, gemm_dtype_t dtype, gemm_layout_t layout)
+int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout)
 {
     const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
-    return c * 4 + (dtype == GEMM_DTYPE_BF16 ? 2 : 0) + (layout == GEMM_LAYOUT_NN ? 1 : 0);
+    const int types = is_f8(in) ? 2 + 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0) : in;
+    return (c * 6 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
 }
 
 // Opt the kernel into its shared memory and, for pair kernels, ask how many clusters can
@@ -279,12 +257,12 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     plan->config = kc.config;
     plan->bm = kc.bm;
     plan->bn = kc.bn;
-    plan->bk = dtg::kBK;
+    plan->bk = kc.stage_k;
     plan->stages = kc.stages;
     plan->cluster = kc.cluster;
     plan->tiles_m = cdiv(M, kc.bm);
     plan->tiles_n = cdiv(N, kc.bn);
-    plan->k_blocks = cdiv(K, dtg::kBK);
+    plan->k_blocks = cdiv(K, kc.stage_k);
     const int64_t tiles = plan->tiles_m * plan->tiles_n;
     // Clusters (CTA pairs, or single CTAs) that can run at once, capped by the option.
     int64_t units = kc.cluster > 1 ? (max_clusters > 0 ? max_clusters : dev.num_sms / kc.cluster)
@@ -316,12 +294,20 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
 }
 
 // c_col_major: C is stored N x M (C[m, n] at C + n * ldc + m), so ldc must cover M.
+// out_dtype < 0: gemm_run's rule, 16-bit operands and C of the same type.  Otherwise any
+// operand type, C of type out_dtype (16-bit), equal to dtype for 16-bit operands.
 gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                             int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
-                            bool c_col_major = false)
+                            bool c_col_major = false, gemm_dtype_t out_dtype = -1)
 {
     if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
-    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (out_dtype < 0) {
+        if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    } else {
+        if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16 && !is_f8(dtype)) return GEMM_ERR_INVALID_ARG;
+        if (out_dtype != GEMM_DTYPE_F16 && out_dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+        if (!is_f8(dtype) && out_dtype != dtype) return GEMM_ERR_INVALID_ARG;
+    }
     if (M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (M == 0 || N == 0) return GEMM_OK;
     if (!C || ldc < (c_col_major ? M : N)) return GEMM_ERR_INVALID_ARG;
@@ -336,7 +322,9 @@ gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t
     if (K > 0) {
         if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0)
             return GEMM_ERR_UNSUPPORTED;
-        if ((lda & 7) != 0 || (ldb & 7) != 0) return GEMM_ERR_UNSUPPORTED;
+        // Row pitches of A and B are TMA strides: multiples of 16 bytes.
+        const int64_t mask = 16 / elem_bytes(dtype) - 1;
+        if ((lda & mask) != 0 || (ldb & mask) != 0) return GEMM_ERR_UNSUPPORTED;
     }
     return GEMM_OK;
 }
@@ -357,12 +345,13 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
                           int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream,
                           const Epilogue& ep = Epilogue())
 {
+    const gemm_dtype_t out = ep.out < 0 ? dtype : ep.out;
     if (K == 0) {
         int blocks = static_cast<int>(cdiv(M * N, 256));
         const int cap = dev.num_sms * 8;
         if (blocks > cap) blocks = cap;
         uint16_t* c16 = static_cast<uint16_t*>(C);
-        if (dtype == GEMM_DTYPE_BF16)
+        if (out == GEMM_DTYPE_BF16)
             dtg::scale_c_kernel<true><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
         else
             dtg::scale_c_kernel<false><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
@@ -370,8 +359,8 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     }
 
     const int config = pick_config(o, dev, M, N);
-    const KernelChoice kc = kernel_choice(config, dtype, layout);
-    const int slot = slot_of(config, dtype, layout);
+    const KernelChoice kc = kernel_choice(config, dtype, out, layout);
+    const int slot = slot_of(config, dtype, out, layout);
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
     if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
@@ -379,17 +368,21 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
 
     CUtensorMap tA, tB, tC;
     const bool nn = layout == GEMM_LAYOUT_NN;
-    if (!get_tmap(cache, A, K, M, lda * 2, dtg::kBK, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
+    const uint64_t eb = static_cast<uint64_t>(elem_bytes(dtype));
+    const uint32_t sk = static_cast<uint32_t>(kc.stage_k);
+    if (!get_tmap(cache, A, K, M, lda * eb, sk, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
     if (nn) {
-        if (!get_tmap(cache, B, N, K, ldb * 2, 64, dtg::kBK, dtype, &tB)) return GEMM_ERR_CUDA;
+        if (!get_tmap(cache, B, N, K, ldb * eb, static_cast<uint32_t>(kc.n_block), sk, dtype, &tB))
+            return GEMM_ERR_CUDA;
     } else {
-        if (!get_tmap(cache, B, K, N, ldb * 2, dtg::kBK, kc.b_box, dtype, &tB)) return GEMM_ERR_CUDA;
+        if (!get_tmap(cache, B, K, N, ldb * eb, sk, static_cast<uint32_t>(kc.b_box), dtype, &tB))
+            return GEMM_ERR_CUDA;
     }
     if (ep.col_major) {
         // C stored N x M: boxes of 32 (M, contiguous) x 64 (N), unswizzled.
-        if (!get_tmap(cache, C, M, N, ldc * 2, 32, dtg::kEpiCols, dtype, &tC, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!get_tmap(cache, C, M, N, ldc * 2, 32, dtg::kEpiCols, out, &tC, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
-    } else if (!get_tmap(cache, C, N, M, ldc * 2, dtg::kEpiCols, 32, dtype, &tC)) {
+    } else if (!get_tmap(cache, C, N, M, ldc * 2, dtg::kEpiCols, 32, out, &tC)) {
         return GEMM_ERR_CUDA;
     }
 
@@ -552,16 +545,22 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
     if (!h || !args) return GEMM_ERR_INVALID_ARG;
     const gemm_args_t& a = *args;
     if (a.c_col_major != 0 && a.c_col_major != 1) return GEMM_ERR_INVALID_ARG;
-    if (!std::isfinite(a.alpha) || !std::isfinite(a.beta)) return GEMM_ERR_INVALID_ARG;
-    const gemm_status_t v =
-        validate_args(a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb, a.ldc, a.layout, a.dtype, a.c_col_major != 0);
+    if (a.out_dtype < 0) return GEMM_ERR_INVALID_ARG;
+    // The three factors are multiplied in fp32 before the kernel scales the accumulator.
+    const float alpha = a.alpha * a.scale_a * a.scale_b;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.beta) || !std::isfinite(a.scale_a) ||
+        !std::isfinite(a.scale_b) || !std::isfinite(alpha))
+        return GEMM_ERR_INVALID_ARG;
+    const gemm_status_t v = validate_args(a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb, a.ldc, a.layout, a.dtype,
+                                          a.c_col_major != 0, a.out_dtype);
     if (v != GEMM_OK || a.M == 0 || a.N == 0) return v;
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
     Epilogue ep;
-    ep.alpha = a.alpha;
+    ep.alpha = alpha;
     ep.beta = a.beta;
     ep.col_major = a.c_col_major;
+    ep.out = a.out_dtype;
     return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb,
                        a.ldc, a.layout, a.dtype, static_cast<cudaStream_t>(stream), ep);
 }
@@ -733,10 +732,12 @@ gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, 
 {
     if (!h || !plan || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
     if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
-    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16 && !is_f8(dtype)) return GEMM_ERR_INVALID_ARG;
+    // 8-bit operands: the plan of the bf16-output kernel (the fp16-output one is the same).
+    const gemm_dtype_t out = is_f8(dtype) ? GEMM_DTYPE_BF16 : dtype;
     const int config = pick_config(h->opts, h->dev, M, N);
-    const KernelChoice kc = kernel_choice(config, dtype, layout);
-    const int slot = slot_of(config, dtype, layout);
+    const KernelChoice kc = kernel_choice(config, dtype, out, layout);
+    const int slot = slot_of(config, dtype, out, layout);
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
     const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);

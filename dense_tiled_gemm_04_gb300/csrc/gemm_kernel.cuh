@@ -1,5 +1,5 @@
-// Persistent warp-specialised tcgen05 GEMM for sm_103a: C = A·B, fp16/bf16 in, fp32
-// accumulate in tensor memory (TMEM), fp16/bf16 out.
+// Persistent warp-specialised tcgen05 GEMM for sm_103a: C = A·B, fp16/bf16 (or E4M3/E5M2)
+// in, fp32 accumulate in tensor memory (TMEM), fp16/bf16 out.
 //
 // Structure (the four steps of "张量缩并：mma 语法" -- fill, load, multiply, store -- with
 // the load and the multiply on different warps so they overlap, which the same page
@@ -9,8 +9,9 @@
 //                 barrier with the byte count and issues the A and B tile loads.  Reads
 //                 outside the tensor are zero-filled by the TMA unit ("NineToothed GEMM
 //                 语法入门" §5: out-of-range reads contribute 0).
-//   warp 1        MMA issuer (one thread): per K block, BK/16 tcgen05.mma into the TMEM
-//                 accumulator, then tcgen05.commit releases the stage; after the item's
+//   warp 1        MMA issuer (one thread): per K block (128 bytes of K), four tcgen05.mma of
+//                 32 bytes of K each into the TMEM accumulator (kind::f16 for 16-bit operands,
+//                 kind::f8f6f4 for 8-bit ones), then tcgen05.commit releases the stage; after the item's
 //                 last K block a commit marks the accumulator full.  The first MMA of an
 //                 item overwrites (the zero-filled accumulator of §2), later ones add.
 //   warps 2..5    epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
@@ -60,8 +61,7 @@
 namespace dtg {
 
 constexpr int kBM = 128;          // accumulator rows per CTA (one TMEM lane per row)
-constexpr int kBK = 64;           // K per ring stage: 64 x 2 B = one 128-byte swizzle row
-constexpr int kUmmaK = 16;        // K per tcgen05.mma of kind::f16
+constexpr int kRowBytes = 128;    // K bytes per operand row of a ring stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;     // 6 warps
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
@@ -71,6 +71,20 @@ constexpr int kEpiCols = 64;                        // columns per staged TMA st
 constexpr int kStgBytes = 32 * kEpiCols * 2;        // one warp's 32 x 64 box, 4 KB
 constexpr uint32_t kWaitSleepNs = 20000;           // longest single suspension of a waiting thread
 constexpr int kEpiBarrier = 1;                      // named barrier of the 4 epilogue warps
+
+// Operand element types: 0 fp16, 1 bf16 (tcgen05 kind::f16), 2 E4M3, 3 E5M2 (kind::f8f6f4).
+// A ring stage always holds 128-byte rows of K (one 128-byte swizzle row), so the number of
+// K elements per stage and per MMA (32 bytes) depends on the element size; the shared-memory
+// layout, the descriptors' byte offsets and the stage sizes do not.
+template <int IN>
+struct Operand {
+    static constexpr int kBytes = IN >= 2 ? 1 : 2;
+    static constexpr int kStageK = 128 / kBytes;    // K elements per ring stage
+    static constexpr int kMmaK = 32 / kBytes;       // K elements per tcgen05.mma
+    static constexpr int kNBlock = 128 / kBytes;    // N elements per 128-byte row of an N-major B box
+    static constexpr bool kF8 = IN >= 2;
+    static constexpr uint32_t kFormat = IN >= 2 ? IN - 2 : IN;  // instruction-descriptor A/B format
+};
 
 // Error-word roles.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3;
@@ -161,8 +175,8 @@ struct WorkIter {
 
 template <int B_ROWS, int STAGES>
 struct Smem {
-    static constexpr int kABytes = kBM * kBK * 2;
-    static constexpr int kBBytes = B_ROWS * kBK * 2;
+    static constexpr int kABytes = kBM * kRowBytes;
+    static constexpr int kBBytes = B_ROWS * kRowBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRing = STAGES * kStageBytes;
     static constexpr int kStgOff = kRing;
@@ -189,14 +203,15 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     return d;
 }
 
-// Instruction descriptor of tcgen05.mma.kind::f16: D fp32, A/B fp16 or bf16, A K-major,
-// B K-major (TN) or N-major (NN), M x N shape.
-template <bool BF16, bool B_MN_MAJOR, int M, int N>
-__host__ __device__ constexpr uint32_t idesc_f16()
+// Instruction descriptor of tcgen05.mma.kind::f16 / kind::f8f6f4: D fp32, A and B of the same
+// format (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2), A K-major, B K-major (TN)
+// or N-major (NN), M x N shape.
+template <uint32_t FORMAT, bool B_MN_MAJOR, int M, int N>
+__host__ __device__ constexpr uint32_t idesc_mma()
 {
     return (1u << 4)                                  // D format: f32
-           | ((BF16 ? 1u : 0u) << 7)                  // A format: 0 f16, 1 bf16
-           | ((BF16 ? 1u : 0u) << 10)                 // B format
+           | (FORMAT << 7)                            // A format
+           | (FORMAT << 10)                           // B format
            | ((B_MN_MAJOR ? 1u : 0u) << 16)           // B major-ness
            | (static_cast<uint32_t>(N >> 3) << 17)    // N / 8
            | (static_cast<uint32_t>(M >> 4) << 24);   // M / 16
@@ -421,11 +436,13 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
     return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
 }
 
-template <int BN, int STAGES, bool BF16, bool NN, bool PAIR>
+// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).
+template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const KernelParams p)
 {
+    using T = Operand<IN>;
     constexpr int kRanks = PAIR ? 2 : 1;
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
@@ -516,7 +533,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     } else {
                         const uint32_t sa = base + stage * L::kStageBytes;
                         const uint32_t sb = sa + L::kABytes;
-                        const int32_t k0 = kb * kBK;
+                        const int32_t k0 = kb * T::kStageK;
                         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
                         if (leader) {
                             ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes);
@@ -531,11 +548,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         };
                         load(sa, &tmA, k0, y_a);
                         if constexpr (NN) {
-                            // B stored K x N: kBRows / 64 boxes of 64 (N) x 64 (K), 8 KB each.
+                            // B stored K x N: boxes of one 128-byte row of N (kNBlock elements)
+                            // by kStageK rows of K, kStageK * 128 bytes each.
 #pragma unroll
-                            for (int q = 0; q < kBRows / 64; ++q) load(sb + q * (64 * kBK * 2), &tmB, n_b + q * 64, k0);
+                            for (int q = 0; q < kBRows / T::kNBlock; ++q)
+                                load(sb + q * (T::kStageK * 128), &tmB, n_b + q * T::kNBlock, k0);
                         } else {
-                            // B stored N x K: one box of 64 (K) x kBRows (N rows).
+                            // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
                         }
                     }
@@ -565,7 +584,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0 && leader) {
             // ---------------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_f16<BF16, NN, kTileM, BN>();
+            constexpr uint32_t idesc = idesc_mma<T::kFormat, NN, kTileM, BN>();
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -590,23 +609,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
 #pragma unroll
-                    for (int k = 0; k < kBK / kUmmaK; ++k) {
-                        // A (K-major, 128B swizzle): the k-th 16-column slice starts 32 B further
-                        // along each 128-byte row; 8-row groups are 1 KB apart (SBO).
+                    for (int k = 0; k < T::kStageK / T::kMmaK; ++k) {
+                        // A (K-major, 128B swizzle): the k-th K slice starts 32 B further along
+                        // each 128-byte row; 8-row groups are 1 KB apart (SBO).
                         const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
                         uint64_t bdesc;
                         if constexpr (NN) {
-                            // B (N-major): rows are K; the k-th slice is 16 rows (2 KB) on; 64-wide
-                            // N blocks are 8 KB apart (LBO), 8-row K groups 1 KB apart (SBO).
-                            bdesc = smem_desc_sw128(sb + k * 2048, 64 * kBK * 2, 1024);
+                            // B (N-major): rows are K; the k-th slice starts kMmaK rows of 128 B
+                            // on; 128-byte-wide N blocks are kStageK rows apart (LBO), 8-row K
+                            // groups 1 KB apart (SBO).
+                            bdesc = smem_desc_sw128(sb + k * (T::kMmaK * 128), T::kStageK * 128, 1024);
                         } else {
                             bdesc = smem_desc_sw128(sb + k * 32, 16, 1024);
                         }
                         const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
-                        if constexpr (PAIR)
-                            ptx::mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
-                        else
-                            ptx::mma_f16_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
+                        if constexpr (PAIR) {
+                            if constexpr (T::kF8)
+                                ptx::mma_f8_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                            else
+                                ptx::mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
+                        } else {
+                            if constexpr (T::kF8)
+                                ptx::mma_f8_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
+                            else
+                                ptx::mma_f16_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
+                        }
                     }
                     // The stage is free once these MMAs finish (in both CTAs of a pair).
                     if constexpr (PAIR)
@@ -682,7 +709,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_wait_ld();
                     if (c == BN / kEpiCols - 1) release_acc();
                     const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                    if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+                    if (store_box<OUT_BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
                 }
             } else {
                 // Part of a stream-K tile: park the fp32 partial sums in this unit's slot.
@@ -737,7 +764,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(s[i]);
                         const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                        if (store_box<BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+                        if (store_box<OUT_BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
                     }
                 };
                 // Are all the other parts in already?  Then this part is the last: it skips

@@ -14,10 +14,12 @@ import torch
 from . import build as _build
 
 LAYOUT_NN, LAYOUT_TN = 0, 1
-DTYPE_F16, DTYPE_BF16 = 0, 1
+DTYPE_F16, DTYPE_BF16, DTYPE_E4M3, DTYPE_E5M2 = 0, 1, 2, 3
 LAYOUTS = {"NN": LAYOUT_NN, "TN": LAYOUT_TN}
-DTYPES = {"f16": DTYPE_F16, "bf16": DTYPE_BF16}
+DTYPES = {"f16": DTYPE_F16, "bf16": DTYPE_BF16, "e4m3": DTYPE_E4M3, "e5m2": DTYPE_E5M2}
 TORCH_TO_DTYPE = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
+# 8-bit operand types (gemm_run_ex only).
+TORCH_TO_DTYPE_EX = {**TORCH_TO_DTYPE, torch.float8_e4m3fn: DTYPE_E4M3, torch.float8_e5m2: DTYPE_E5M2}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
 OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT, OPT_STREAM_K = range(6)
@@ -37,7 +39,8 @@ class gemm_args_t(ctypes.Structure):
                 ("M", ctypes.c_int64), ("N", ctypes.c_int64), ("K", ctypes.c_int64),
                 ("lda", ctypes.c_int64), ("ldb", ctypes.c_int64), ("ldc", ctypes.c_int64),
                 ("layout", ctypes.c_int32), ("dtype", ctypes.c_int32),
-                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("c_col_major", ctypes.c_int32)]
+                ("alpha", ctypes.c_float), ("beta", ctypes.c_float), ("c_col_major", ctypes.c_int32),
+                ("out_dtype", ctypes.c_int32), ("scale_a", ctypes.c_float), ("scale_b", ctypes.c_float)]
 
 
 class GemmError(RuntimeError):
@@ -111,7 +114,8 @@ def _ld(t: torch.Tensor) -> int:
     if t.size(1) > 1 and t.stride(1) != 1:
         raise ValueError("expected unit stride along the last dimension (row-major)")
     if t.size(0) <= 1:
-        return max(-(-t.size(1) // 8) * 8, 8)
+        align = 16 // t.element_size()  # a TMA row pitch is a multiple of 16 bytes
+        return max(-(-t.size(1) // align) * align, align)
     return t.stride(0)
 
 
@@ -213,11 +217,41 @@ class Gemm:
         return C
 
     def run_ex_raw(self, A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int, alpha: float,
-                   beta: float, c_col_major: int, stream: int) -> int:
-        """gemm_run_ex on raw device addresses: C = alpha * A·B + beta * C (row- or column-major C)."""
+                   beta: float, c_col_major: int, stream: int, out_dtype: int | None = None, scale_a: float = 1.0,
+                   scale_b: float = 1.0) -> int:
+        """gemm_run_ex on raw device addresses:
+        C = alpha * scale_a * scale_b * A·B + beta * C (row- or column-major C)."""
         a = gemm_args_t(A or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype, alpha, beta,
-                        c_col_major)
+                        c_col_major, dtype if out_dtype is None else out_dtype, scale_a, scale_b)
         return int(self._lib.gemm_run_ex(self._h, ctypes.byref(a), stream or None))
+
+    def run_ex(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor | None = None, layout: str = "NN",
+               out_dtype: torch.dtype | None = None, alpha: float = 1.0, beta: float = 0.0, scale_a: float = 1.0,
+               scale_b: float = 1.0, c_col_major: bool = False, stream=None) -> torch.Tensor:
+        """C = alpha * scale_a * scale_b * A·B + beta * C on device tensors; A, B 16-bit or 8-bit
+        (float8_e4m3fn / float8_e5m2), C float16 or bfloat16.  With c_col_major, ``C`` is the
+        N x M row-major tensor holding C transposed.  Async on `stream`."""
+        M, K = A.shape
+        N = B.shape[1] if layout == "NN" else B.shape[0]
+        if (B.shape[0] if layout == "NN" else B.shape[1]) != K:
+            raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, layout {layout}")
+        if A.dtype != B.dtype or A.dtype not in TORCH_TO_DTYPE_EX:
+            raise TypeError("A and B must have the same 16-bit or 8-bit float type")
+        if out_dtype is None:
+            out_dtype = C.dtype if C is not None else (A.dtype if A.dtype in TORCH_TO_DTYPE else torch.bfloat16)
+        if out_dtype not in TORCH_TO_DTYPE:
+            raise TypeError("C must be float16 or bfloat16")
+        shape = (N, M) if c_col_major else (M, N)
+        if C is None:
+            C = empty_output(*shape, out_dtype, A.device)
+        if tuple(C.shape) != shape or C.dtype != out_dtype:
+            raise ValueError("C has the wrong shape or dtype")
+        st = self.run_ex_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), M, N, K, _ld(A), _ld(B), _ld(C),
+                             LAYOUTS[layout], TORCH_TO_DTYPE_EX[A.dtype], alpha, beta, int(c_col_major),
+                             _stream_ptr(stream), TORCH_TO_DTYPE[out_dtype], scale_a, scale_b)
+        if st != OK:
+            raise GemmError(st, "gemm_run_ex")
+        return C
 
     def run_host(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, layout: str = "NN", stream=None) -> int:
         """gemm_run_host on CPU tensors (pin them for DMA copies); synchronous; returns the status."""

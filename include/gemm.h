@@ -42,15 +42,18 @@
 extern "C" {
 #endif
 
-#define GEMM_API_VERSION 1
+#define GEMM_API_VERSION 2
 
 typedef struct gemm_handle_s* gemm_handle_t;
 
 typedef int32_t gemm_layout_t;
 enum { GEMM_LAYOUT_NN = 0, GEMM_LAYOUT_TN = 1 };
 
+/* Element types.  F16 and BF16 serve as operand and output types; E4M3 and E5M2 (8-bit
+ * floats: 1-4-3 with bias 7 and no infinities, 1-5-2 with bias 15) are operand types only,
+ * accepted by gemm_run_ex. */
 typedef int32_t gemm_dtype_t;
-enum { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1 };
+enum { GEMM_DTYPE_F16 = 0, GEMM_DTYPE_BF16 = 1, GEMM_DTYPE_E4M3 = 2, GEMM_DTYPE_E5M2 = 3 };
 
 typedef int32_t gemm_status_t;
 enum {
@@ -119,17 +122,25 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C,
                        int64_t lda, int64_t ldb, int64_t ldc,
                        gemm_layout_t layout, gemm_dtype_t dtype, void* stream);
 
-/* The general form: C = alpha * A·B + beta * C, with C stored row-major or column-major.
+/* The general form: C = alpha * scale_a * scale_b * A·B + beta * C, with C stored row-major
+ * or column-major and 16-bit or 8-bit operands.
  *   - "张量缩并：mma 语法" states the contraction as C += A × B (alpha = beta = 1); its
  *     transposed store (mma.store.transp) writes the result with rows and columns swapped,
- *     which is c_col_major here.
- *   - alpha, beta: finite fp32 scalars.  The result is alpha * acc + beta * C_old in fp32,
- *     rounded once to the output type.  With beta == 0, C is not read (it may hold
+ *     which is c_col_major here; its scaled form (mma.row.row.scale with sc_a, sc_b) scales
+ *     each result after the contraction, which is scale_a, scale_b here (per-tensor scales,
+ *     the usual companions of 8-bit operands).
+ *   - dtype: operand type of A and B (F16, BF16, E4M3 or E5M2).  out_dtype: type of C (F16
+ *     or BF16); for 16-bit operands it must equal dtype.
+ *   - alpha, beta, scale_a, scale_b: finite fp32 scalars.  The result is
+ *     (alpha * scale_a * scale_b) * acc + beta * C_old in fp32 (the three factors multiplied
+ *     in fp32 first), rounded once to out_dtype.  With beta == 0, C is not read (it may hold
  *     anything, NaN included).  K == 0 gives C = beta * C.
  *   - c_col_major = 0: C[m, n] at C + m * ldc + n (ldc >= N), as in gemm_run.
  *     c_col_major = 1: C[m, n] at C + n * ldc + m (ldc >= M; C stored N x M row-major).
- *   - A, B, layouts, alignment rules and status codes are those of gemm_run.
- * alpha = 1, beta = 0, c_col_major = 0 is exactly gemm_run. */
+ *   - 8-bit operands: lda and ldb must be multiples of 16 elements (16 bytes); otherwise
+ *     A, B, layouts, alignment rules and status codes are those of gemm_run.
+ * alpha = scale_a = scale_b = 1, beta = 0, c_col_major = 0, out_dtype = dtype is exactly
+ * gemm_run. */
 typedef struct {
     const void* A;
     const void* B;
@@ -141,6 +152,9 @@ typedef struct {
     float alpha;
     float beta;
     int32_t c_col_major;
+    gemm_dtype_t out_dtype;
+    float scale_a;
+    float scale_b;
 } gemm_args_t;
 
 gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream);

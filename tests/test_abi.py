@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     so = lib.load()
-    assert so.gemm_api_version() == 1
+    assert so.gemm_api_version() == 2
     for s in range(6):
         assert lib.status_string(s).startswith("GEMM_")
     assert "unknown" in lib.status_string(99)
@@ -52,8 +52,24 @@ def test_null_handle_is_rejected_without_a_gpu(lib):
     assert so.gemm_destroy(None) == lib.OK
     assert so.gemm_create(None, 0) == lib.ERR_INVALID_ARG
     assert so.gemm_run_ex(None, None, None) == lib.ERR_INVALID_ARG
-    args = lib.gemm_args_t(None, None, None, 8, 8, 8, 8, 8, 8, 0, 0, 1.0, 0.0, 0)
+    args = lib.gemm_args_t(None, None, None, 8, 8, 8, 8, 8, 8, 0, 0, 1.0, 0.0, 0, 0, 1.0, 1.0)
     assert so.gemm_run_ex(None, args, None) == lib.ERR_INVALID_ARG
+
+
+def test_args_struct_matches_the_header(lib):
+    # Field order and size of gemm_args_t as declared in the header (x86-64 and aarch64 ABI).
+    text = open(HEADER).read()
+    end = text.index("} gemm_args_t;")
+    body = text[text.rindex("typedef struct {", 0, end) + len("typedef struct {"):end]
+    body = re.sub(r"/\*.*?\*/", "", body, flags=re.S)
+    names = []
+    for decl in body.split(";"):
+        m = re.match(r"\s*(?:const\s+)?\w+\s*\*?\s*(.*)$", decl, flags=re.S)
+        if decl.strip():
+            names += [n.strip() for n in m.group(1).split(",")]
+    assert names == [f for f, _ in lib.gemm_args_t._fields_]
+    import ctypes
+    assert ctypes.sizeof(lib.gemm_args_t) == 3 * 8 + 6 * 8 + 2 * 4 + 2 * 4 + 4 + 4 + 2 * 4
 
 
 def test_create_without_a_gpu_reports_an_error(lib):
@@ -81,6 +97,7 @@ P = 1 << 20  # a 16-byte-aligned fake address: gemm_check_args never dereference
     ((P, P, P, -1, 8, 8, 8, 8, 8, 0, 0), 1),           # negative size
     ((P, P, P, 8, 8, 8, 8, 8, 8, 2, 0), 1),            # bad layout
     ((P, P, P, 8, 8, 8, 8, 8, 8, 0, 7), 1),            # bad dtype
+    ((P, P, P, 16, 16, 16, 16, 16, 16, 0, 2), 1),      # 8-bit operands: gemm_run_ex only
     ((0, P, P, 8, 8, 8, 8, 8, 8, 0, 0), 1),            # null A
     ((P, P, 0, 8, 8, 8, 8, 8, 8, 0, 0), 1),            # null C
     ((P, P, P, 8, 16, 16, 8, 16, 16, 0, 0), 1),        # lda < K
