@@ -74,6 +74,12 @@ def _load():
     lib.oracle_gemm_rows_typed.argtypes = [p, p, p, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int, ctypes.c_int,
                                            ctypes.c_double, ctypes.c_double, p, i64, p, p, i64, ctypes.c_int]
     lib.oracle_gemm_rows_typed.restype = ctypes.c_int
+    lib.oracle_gemm_rows_blockscaled.argtypes = [p, p, p, p, p, i64, i64, i64, i64, i64, i64, i64, ctypes.c_int,
+                                                 ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, p, i64,
+                                                 p, p, i64, ctypes.c_int]
+    lib.oracle_gemm_rows_blockscaled.restype = ctypes.c_int
+    lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
+    lib.oracle_e8m0_to_f64.restype = ctypes.c_double
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e4m3_to_f64.restype = ctypes.c_double
     lib.oracle_e5m2_to_f64.argtypes = [ctypes.c_uint8]
@@ -257,9 +263,57 @@ def gemm_typed(A, B, layout: str, in_dtype: str, out_dtype: str, alpha: float = 
     return (out16, out64) if want_f64 else out16
 
 
+def _scales(x, rows: int, nblocks: int, what: str) -> np.ndarray:
+    """Row-major uint8 exponent array of shape (rows, nblocks) (numpy or torch CPU)."""
+    if not isinstance(x, np.ndarray):
+        x = x.detach().cpu().numpy()
+    x = np.ascontiguousarray(x, dtype=np.uint8)
+    if x.shape != (rows, nblocks):
+        raise ValueError(f"{what} must be {rows} x {nblocks}, got {x.shape}")
+    return x
+
+
+def gemm_blockscaled(A, B, sa, sb, layout: str, in_dtype: str, out_dtype: str, alpha: float = 1.0,
+                     beta: float = 0.0, Cin=None, rows=None, want_f64: bool = False, nthreads: int = 0):
+    """alpha * sum_j 2^(sa-127) 2^(sb-127) (A·B over K block j) + beta * Cin: 8-bit operands with
+    one E8M0 scale per 32 K elements of each row of A (``sa``: M x ceil(K/32)) and of each
+    column of Beff (``sb``: N x ceil(K/32)).  Rounded codes for ``rows``, or ``(codes, f64)``."""
+    lib = _load()
+    A, B = _codes(A), _codes(B)
+    M, N, K = _shape_check(A, B, layout)
+    A, B = np.ascontiguousarray(A), np.ascontiguousarray(B)
+    nb = -(-K // 32)
+    sa = _scales(sa, M, nb, "sa")
+    sb = _scales(sb, N, nb, "sb")
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    rows = np.ascontiguousarray(rows.astype(np.int64))
+    if beta != 0.0:
+        Cin = np.ascontiguousarray(_codes(Cin))
+        if Cin.shape != (M, N):
+            raise ValueError(f"Cin must be {M} x {N}")
+        cptr, ldcin = Cin.ctypes.data, max(N, 1)
+    else:
+        cptr, ldcin = None, 1
+    out16 = np.zeros((rows.size, N), dtype=np.uint16)
+    out64 = np.zeros((rows.size, N), dtype=np.float64) if want_f64 else None
+    used = lib.oracle_gemm_rows_blockscaled(A.ctypes.data, B.ctypes.data, sa.ctypes.data, sb.ctypes.data, cptr, N, K,
+                                            _ld(A), _ld(B), max(nb, 1), max(nb, 1), ldcin, LAYOUTS[layout],
+                                            DTYPES[in_dtype], DTYPES[out_dtype], float(alpha), float(beta),
+                                            rows.ctypes.data, rows.size, out16.ctypes.data,
+                                            out64.ctypes.data if out64 is not None else None, N, int(nthreads))
+    if used < 0:
+        raise MemoryError("oracle allocation failed")
+    return (out16, out64) if want_f64 else out16
+
+
+def e8m0(e: int) -> float:
+    return float(_load().oracle_e8m0_to_f64(int(e)))
+
+
 def max_threads() -> int:
     return int(_load().oracle_max_threads())
 
 
-__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "gemm_typed", "max_threads",
+__all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "gemm_typed",
+           "gemm_blockscaled", "e8m0", "max_threads",
            "LAYOUTS", "DTYPES"]

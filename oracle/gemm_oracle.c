@@ -410,3 +410,87 @@ int oracle_gemm_rows_typed(const uint16_t* A, const uint16_t* B, const uint16_t*
     free(TC);
     return used;
 }
+
+/* ------------------------------------------------------- block-scaled 8-bit operands */
+
+/* Value of an 8-bit scale exponent (the E8M0 format of the OCP microscaling formats:
+ * 2^(e - 127), e = 255 is NaN). */
+double oracle_e8m0_to_f64(uint8_t e)
+{
+    return e == 255u ? NAN : ldexp(1.0, (int)e - 127);
+}
+
+/* C = alpha * acc + beta * Cin with per-tile scales on 8-bit operands ("张量缩并：mma 语法",
+ * quantised operands with per-tile scaling: the contraction of a tile of A with a tile of B
+ * is multiplied by the A tile's scale sc_a and the B tile's scale sc_b, and the scaled
+ * results are accumulated).  Tiles are 32 long along K and one row (A) or one column (B)
+ * wide: sa[m * ldsa + j] scales A[m, 32j .. 32j+31] and sb[n * ldsb + j] scales
+ * Beff[32j .. 32j+31, n], both E8M0 exponents.  Per output element, in this order:
+ *     part_j = sum_{k in block j} A[m,k] * Beff[k,n]             (the tile contraction)
+ *     acc    = sum_j  2^(sa - 127) * 2^(sb - 127) * part_j         (scaled, accumulated)
+ * The last block of a K that is not a multiple of 32 holds fewer terms.  Everything in fp64,
+ * rounded once to out_dtype.  Same row selection and outputs as oracle_gemm_rows_typed. */
+int oracle_gemm_rows_blockscaled(const uint16_t* A, const uint16_t* B, const uint8_t* sa, const uint8_t* sb,
+                                 const uint16_t* Cin, int64_t N, int64_t K, int64_t lda, int64_t ldb, int64_t ldsa,
+                                 int64_t ldsb, int64_t ldcin, int layout, int in_dtype, int out_dtype, double alpha,
+                                 double beta, const int64_t* rows, int64_t nrows, uint16_t* out16, double* out64,
+                                 int64_t ldo, int nthreads)
+{
+    const int64_t kBlock = 32;
+    double* T = (double*)malloc(65536 * sizeof(double));
+    double* TC = (double*)malloc(65536 * sizeof(double));
+    if (!T || !TC) {
+        free(T);
+        free(TC);
+        return -1;
+    }
+    build_table(T, in_dtype);
+    build_table(TC, out_dtype);
+    const int64_t nblocks = (K + kBlock - 1) / kBlock;
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+#else
+    (void)nthreads;
+    {
+#endif
+        const size_t n_alloc = (size_t)(N > 0 ? N : 1);
+        double* acc = (double*)malloc(n_alloc * sizeof(double));
+        double* part = (double*)malloc(n_alloc * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t m = rows[i];
+            const uint16_t* arow = A + m * lda;
+            for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+            for (int64_t j = 0; j < nblocks; ++j) {
+                const int64_t k0 = j * kBlock, k1 = (k0 + kBlock < K) ? k0 + kBlock : K;
+                for (int64_t n = 0; n < N; ++n) part[n] = 0.0;
+                for (int64_t k = k0; k < k1; ++k) {
+                    const double a = T[arow[k]];
+                    for (int64_t n = 0; n < N; ++n)
+                        part[n] += a * T[layout == OR_LAYOUT_NN ? B[k * ldb + n] : B[n * ldb + k]];
+                }
+                const double s_a = oracle_e8m0_to_f64(sa[m * ldsa + j]);
+                for (int64_t n = 0; n < N; ++n) acc[n] += s_a * oracle_e8m0_to_f64(sb[n * ldsb + j]) * part[n];
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                double v = alpha * acc[n];
+                if (beta != 0.0) v += beta * TC[Cin[m * ldcin + n]];
+                if (out64) out64[i * ldo + n] = v;
+                if (out16)
+                    out16[i * ldo + n] = (out_dtype == OR_BF16) ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+            }
+        }
+        free(acc);
+        free(part);
+    }
+    free(T);
+    free(TC);
+    return used;
+}

@@ -358,3 +358,104 @@ def test_fp8_scales_and_random_values():
     Cin, _ = make_inputs(M, N, N, "NN", "bf16", "int", seed=43)
     _, f64b = oracle.gemm_typed(A, B, "TN", "e4m3", "bf16", alpha=1.0, beta=-1.0, Cin=Cin, want_f64=True)
     np.testing.assert_allclose(f64b, ref - Cin.to(torch.float64).numpy(), rtol=1e-13, atol=1e-13)
+
+
+# ------------------------------------------------------------------ 8-bit inputs, per-tile scales
+
+
+def test_e8m0_scale_codes():
+    # E8M0 (the OCP microscaling scale format): 2^(e - 127), e = 255 is NaN.
+    assert oracle.e8m0(127) == 1.0 and oracle.e8m0(128) == 2.0 and oracle.e8m0(126) == 0.5
+    assert oracle.e8m0(0) == 2.0 ** -127 and oracle.e8m0(254) == 2.0 ** 127
+    assert np.isnan(oracle.e8m0(255))
+    if hasattr(torch, "float8_e8m0fnu"):
+        codes = torch.arange(256, dtype=torch.int32).to(torch.uint8)
+        ref = codes.view(torch.float8_e8m0fnu).to(torch.float64).numpy()
+        mine = np.array([oracle.e8m0(e) for e in range(256)])
+        nan = np.isnan(ref)
+        assert np.array_equal(np.isnan(mine), nan)
+        assert np.array_equal(mine[~nan], ref[~nan])
+
+
+def _expand(s: np.ndarray, K: int) -> np.ndarray:
+    """Per-element scale 2^(s[:, k // 32] - 127): the scales written out element by element."""
+    e = np.repeat(s.astype(np.int64), 32, axis=1)[:, :K]
+    return np.ldexp(1.0, e - 127)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_blockscaled_unit_scales_equal_the_unscaled_contraction(fmt, layout):
+    M, N, K = 19, 23, 70  # three K blocks, the last one 6 long
+    A, B = make_inputs(M, N, K, layout, fmt, "normal", seed=51)
+    nb = -(-K // 32)
+    one_a, one_b = np.full((M, nb), 127, np.uint8), np.full((N, nb), 127, np.uint8)
+    for out in ("f16", "bf16"):
+        got = oracle.gemm_blockscaled(A, B, one_a, one_b, layout, fmt, out)
+        assert np.array_equal(got, oracle.gemm_typed(A, B, layout, fmt, out))
+
+
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_blockscaled_row_and_column_scales_closed_form(layout):
+    # Scales constant along K factor out of the sum: C = 2^r_m * 2^c_n * (A·B)[m, n].
+    M, N, K = 21, 17, 96
+    A, B = make_inputs(M, N, K, layout, "e4m3", "int", seed=52)
+    rng = np.random.default_rng(53)
+    r, c = rng.integers(-3, 4, M), rng.integers(-3, 4, N)
+    sa = np.repeat((127 + r)[:, None], 3, axis=1).astype(np.uint8)
+    sb = np.repeat((127 + c)[:, None], 3, axis=1).astype(np.uint8)
+    _, f64 = oracle.gemm_blockscaled(A, B, sa, sb, layout, "e4m3", "bf16", want_f64=True)
+    a, b = A.to(torch.float64).numpy(), B.to(torch.float64).numpy()
+    ab = a @ (b if layout == "NN" else b.T)
+    assert np.array_equal(f64, np.ldexp(1.0, r)[:, None] * np.ldexp(1.0, c)[None, :] * ab)
+
+
+@pytest.mark.parametrize("fmt", ["e4m3", "e5m2"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_blockscaled_against_dequantise_then_multiply(fmt, layout):
+    # The tile-by-tile form (contract a 32-long K block, scale, accumulate) against the other
+    # way round: scale every element of A and B, then one numpy fp64 product.  M != N and a
+    # ragged last block, so an index of the wrong operand, the wrong block or a dropped tail
+    # block all show.
+    M, N, K = 27, 41, 150
+    A, B = make_inputs(M, N, K, layout, fmt, "normal", seed=54)
+    nb = -(-K // 32)
+    rng = np.random.default_rng(55)
+    sa = rng.integers(120, 135, (M, nb)).astype(np.uint8)
+    sb = rng.integers(120, 135, (N, nb)).astype(np.uint8)
+    _, f64 = oracle.gemm_blockscaled(A, B, sa, sb, layout, fmt, "f16", want_f64=True)
+    a = A.to(torch.float64).numpy() * _expand(sa, K)
+    bt = (B.to(torch.float64).numpy() if layout == "TN" else B.to(torch.float64).numpy().T) * _expand(sb, K)
+    ref = a @ bt.T
+    np.testing.assert_allclose(f64, ref, rtol=1e-12, atol=1e-30)
+
+
+def test_blockscaled_one_block_scale_changes_one_partial():
+    # Raising one A scale by one step doubles exactly that block's share of the row.
+    M, N, K = 6, 9, 96
+    A, B = make_inputs(M, N, K, "TN", "e4m3", "int", seed=56)
+    sa, sb = np.full((M, 3), 127, np.uint8), np.full((N, 3), 127, np.uint8)
+    _, base = oracle.gemm_blockscaled(A, B, sa, sb, "TN", "e4m3", "bf16", want_f64=True)
+    sa2 = sa.copy()
+    sa2[4, 1] = 128
+    _, f64 = oracle.gemm_blockscaled(A, B, sa2, sb, "TN", "e4m3", "bf16", want_f64=True)
+    a, b = A.to(torch.float64).numpy(), B.to(torch.float64).numpy()
+    block1 = a[4, 32:64] @ b[:, 32:64].T
+    expect = base.copy()
+    expect[4] += block1
+    assert np.array_equal(f64, expect)
+
+
+def test_blockscaled_nan_scale_and_epilogue():
+    M, N, K = 8, 12, 64
+    A, B = make_inputs(M, N, K, "NN", "e5m2", "int", seed=57)
+    sa, sb = np.full((M, 2), 127, np.uint8), np.full((N, 2), 127, np.uint8)
+    sa[3, 1] = 255
+    got = oracle.decode(oracle.gemm_blockscaled(A, B, sa, sb, "NN", "e5m2", "f16"), "f16")
+    assert np.all(np.isnan(got[3])) and not np.isnan(np.delete(got, 3, axis=0)).any()
+    sa[3, 1] = 127
+    Cin, _ = make_inputs(M, N, N, "NN", "f16", "int", seed=58)
+    _, f64 = oracle.gemm_blockscaled(A, B, sa, sb, "NN", "e5m2", "f16", alpha=0.5, beta=-1.0, Cin=Cin,
+                                     want_f64=True)
+    ref = 0.5 * (A.to(torch.float64).numpy() @ B.to(torch.float64).numpy()) - Cin.to(torch.float64).numpy()
+    assert np.array_equal(f64, ref)
