@@ -24,7 +24,7 @@ using dtg::KernelParams;
 constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
-constexpr int kNumSlots = 36;  // 3 configurations x 6 operand/output types x 2 layouts
+constexpr int kNumSlots = 60;  // 3 configurations x 10 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -63,6 +63,8 @@ struct Epilogue {
     float beta = 0.0f;
     int32_t col_major = 0;
     gemm_dtype_t out = -1;
+    const void* sfa = nullptr;  // block scales (8-bit operands): both set, or both null
+    const void* sfb = nullptr;
 };
 
 struct TmapEntry {
@@ -179,9 +181,11 @@ bool is_f8(gemm_dtype_t t) { return t == GEMM_DTYPE_E4M3 || t == GEMM_DTYPE_E5M2
 int elem_bytes(gemm_dtype_t t) { return is_f8(t) ? 1 : 2; }
 
 // `out` is the type of C: equal to `in` for 16-bit operands, F16 or BF16 for 8-bit ones.
-KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout)
+// `mx`: 8-bit operands with block scales (one configuration, 128 x 256).
+KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, bool mx = false)
 {
     const bool nn = layout == GEMM_LAYOUT_NN, out_bf16 = out == GEMM_DTYPE_BF16;
+    if (mx) return dtg::choice_mx(in == GEMM_DTYPE_E5M2, out_bf16, nn);
     switch (in) {
     case GEMM_DTYPE_BF16: return dtg::choice_bf16(config, nn);
     case GEMM_DTYPE_E4M3: return dtg::choice_e4m3(config, out_bf16, nn);
@@ -190,11 +194,12 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
     }
 }
 
-int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout)
+int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, bool mx = false)
 {
     const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
-    const int types = is_f8(in) ? 2 + 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0) : in;
-    return (c * 6 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
+    const int f8 = 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0);  // 0..3
+    const int types = is_f8(in) ? (mx ? 6 : 2) + f8 : in;
+    return (c * 10 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
 }
 
 // Opt the kernel into its shared memory and, for pair kernels, ask how many clusters can
@@ -358,9 +363,10 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
         return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    const int config = pick_config(o, dev, M, N);
-    const KernelChoice kc = kernel_choice(config, dtype, out, layout);
-    const int slot = slot_of(config, dtype, out, layout);
+    const bool mx = ep.sfa != nullptr;
+    const int config = mx ? GEMM_CONFIG_128x256 : pick_config(o, dev, M, N);
+    const KernelChoice kc = kernel_choice(config, dtype, out, layout, mx);
+    const int slot = slot_of(config, dtype, out, layout, mx);
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
     if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
@@ -408,6 +414,9 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.alpha = ep.alpha;
     kp.beta = ep.beta;
     kp.c_col_major = ep.col_major;
+    kp.sfa = static_cast<const uint8_t*>(ep.sfa);
+    kp.sfb = static_cast<const uint8_t*>(ep.sfb);
+    kp.sfb_blocks = static_cast<int32_t>(cdiv(N, dtg::kSfChunkRows));
 
     void* args[] = {&tA, &tB, &tC, &kp};
     cudaLaunchConfig_t cfg;
@@ -459,6 +468,25 @@ gemm_status_t query_device(int device, int* sms)
         return GEMM_ERR_CUDA;
     if (major != 10 || minor != 3) return GEMM_ERR_ARCH;
     return GEMM_OK;
+}
+
+// Block scales, row-major (src[r * ld + j]: the exponent of K block j of row r, rows x
+// kblocks) -> the chunked layout the block-scaled kernels load (dtg::kSfChunkBytes).  Rows and K
+// blocks past the end are filled with 127 (a scale of 1: padded K elements are zero and stay
+// zero).  Grid-stride over the `total` destination bytes.
+__global__ void pack_scales_kernel(const uint8_t* src, int64_t rows, int64_t kblocks, int64_t ld, uint8_t* dst,
+                                   int64_t total)
+{
+    const int64_t groups = (kblocks + 3) / 4;
+    for (int64_t o = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; o < total;
+         o += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t chunk = o / dtg::kSfChunkBytes;
+        const int within = static_cast<int>(o - chunk * dtg::kSfChunkBytes);
+        const int64_t rb = chunk / groups, g = chunk - rb * groups;
+        const int64_t r = rb * dtg::kSfChunkRows + ((within >> 2) & 3) * 32 + (within >> 4);
+        const int64_t j = g * 4 + (within & 3);
+        dst[o] = (r < rows && j < kblocks) ? src[r * ld + j] : static_cast<uint8_t>(127);
+    }
 }
 
 }  // namespace
@@ -540,10 +568,9 @@ gemm_status_t gemm_run(gemm_handle_t h, const void* A, const void* B, void* C, i
                        static_cast<cudaStream_t>(stream));
 }
 
-gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream)
+// Checks of gemm_args_t shared by gemm_run_ex and gemm_run_mx; fills the epilogue.
+static gemm_status_t validate_ex(const gemm_args_t& a, Epilogue* ep)
 {
-    if (!h || !args) return GEMM_ERR_INVALID_ARG;
-    const gemm_args_t& a = *args;
     if (a.c_col_major != 0 && a.c_col_major != 1) return GEMM_ERR_INVALID_ARG;
     if (a.out_dtype < 0) return GEMM_ERR_INVALID_ARG;
     // The three factors are multiplied in fp32 before the kernel scales the accumulator.
@@ -553,16 +580,69 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
         return GEMM_ERR_INVALID_ARG;
     const gemm_status_t v = validate_args(a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb, a.ldc, a.layout, a.dtype,
                                           a.c_col_major != 0, a.out_dtype);
+    if (v != GEMM_OK) return v;
+    ep->alpha = alpha;
+    ep->beta = a.beta;
+    ep->col_major = a.c_col_major;
+    ep->out = a.out_dtype;
+    return GEMM_OK;
+}
+
+gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream)
+{
+    if (!h || !args) return GEMM_ERR_INVALID_ARG;
+    const gemm_args_t& a = *args;
+    Epilogue ep;
+    const gemm_status_t v = validate_ex(a, &ep);
     if (v != GEMM_OK || a.M == 0 || a.N == 0) return v;
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;
-    Epilogue ep;
-    ep.alpha = alpha;
-    ep.beta = a.beta;
-    ep.col_major = a.c_col_major;
-    ep.out = a.out_dtype;
     return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb,
                        a.ldc, a.layout, a.dtype, static_cast<cudaStream_t>(stream), ep);
+}
+
+int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K)
+{
+    if (rows <= 0 || K <= 0) return 0;
+    return cdiv(rows, dtg::kSfChunkRows) * cdiv(K, 128) * dtg::kSfChunkBytes;
+}
+
+gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* sfa, const void* sfb, void* stream)
+{
+    if (!h || !args) return GEMM_ERR_INVALID_ARG;
+    const gemm_args_t& a = *args;
+    if (!is_f8(a.dtype)) return GEMM_ERR_INVALID_ARG;
+    Epilogue ep;
+    const gemm_status_t v = validate_ex(a, &ep);
+    if (v != GEMM_OK || a.M == 0 || a.N == 0) return v;
+    if (a.K > 0) {
+        if (!sfa || !sfb) return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(sfa) & 15u) != 0 || (reinterpret_cast<uintptr_t>(sfb) & 15u) != 0)
+            return GEMM_ERR_UNSUPPORTED;
+        ep.sfa = sfa;
+        ep.sfb = sfb;
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb,
+                       a.ldc, a.layout, a.dtype, static_cast<cudaStream_t>(stream), ep);
+}
+
+gemm_status_t gemm_mx_pack_scales(gemm_handle_t h, const void* src, int64_t rows, int64_t kblocks, int64_t ld,
+                                  void* dst, void* stream)
+{
+    if (!h || rows < 0 || kblocks < 0) return GEMM_ERR_INVALID_ARG;
+    if (rows == 0 || kblocks == 0) return GEMM_OK;
+    if (!src || !dst || ld < kblocks) return GEMM_ERR_INVALID_ARG;
+    const int64_t total = cdiv(rows, dtg::kSfChunkRows) * cdiv(kblocks, 4) * dtg::kSfChunkBytes;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    int blocks = static_cast<int>(cdiv(total, 256));
+    const int cap = h->dev.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    pack_scales_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint8_t*>(src), rows, kblocks, ld, static_cast<uint8_t*>(dst), total);
+    return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
 }
 
 gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C, int64_t M, int64_t N,

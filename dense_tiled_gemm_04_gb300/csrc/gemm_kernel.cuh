@@ -72,10 +72,12 @@ constexpr int kStgBytes = 32 * kEpiCols * 2;        // one warp's 32 x 64 box, 4
 constexpr uint32_t kWaitSleepNs = 20000;           // longest single suspension of a waiting thread
 constexpr int kEpiBarrier = 1;                      // named barrier of the 4 epilogue warps
 
-// Operand element types: 0 fp16, 1 bf16 (tcgen05 kind::f16), 2 E4M3, 3 E5M2 (kind::f8f6f4).
-// A ring stage always holds 128-byte rows of K (one 128-byte swizzle row), so the number of
-// K elements per stage and per MMA (32 bytes) depends on the element size; the shared-memory
-// layout, the descriptors' byte offsets and the stage sizes do not.
+// Operand element types: 0 fp16, 1 bf16 (tcgen05 kind::f16), 2 E4M3, 3 E5M2 (kind::f8f6f4),
+// 4 E4M3 and 5 E5M2 with one E8M0 scale per 32 K elements of each row of A and column of B
+// (kind::mxf8f6f4, block-scaled).  A ring stage always holds 128-byte rows of K (one 128-byte
+// swizzle row), so the number of K elements per stage and per MMA (32 bytes) depends on the
+// element size; the shared-memory layout, the descriptors' byte offsets and the stage sizes
+// do not.
 template <int IN>
 struct Operand {
     static constexpr int kBytes = IN >= 2 ? 1 : 2;
@@ -83,8 +85,19 @@ struct Operand {
     static constexpr int kMmaK = 32 / kBytes;       // K elements per tcgen05.mma
     static constexpr int kNBlock = 128 / kBytes;    // N elements per 128-byte row of an N-major B box
     static constexpr bool kF8 = IN >= 2;
-    static constexpr uint32_t kFormat = IN >= 2 ? IN - 2 : IN;  // instruction-descriptor A/B format
+    static constexpr bool kMX = IN >= 4;            // block-scaled
+    static constexpr uint32_t kFormat = IN >= 2 ? (IN - 2) & 1 : IN;  // instruction-descriptor A/B format
 };
+
+// Block scales travel in 512-byte chunks: the E8M0 exponents of 128 rows (of A, or columns
+// of B) for 4 consecutive 32-long K blocks, i.e. one ring stage of 128 K elements.  Inside a
+// chunk, row r and K block c sit at byte (r % 32) * 16 + (r / 32) * 4 + c, so that the 32
+// 16-byte lines, copied into TMEM lanes 0-31 (and replicated into the other lane quadrants),
+// put row r's four exponents in column r / 32 of lane r.  Chunk (row block rb, K group g) of
+// a matrix with G = ceil(K / 128) K groups starts at byte (rb * G + g) * 512.
+constexpr int kSfChunkBytes = 512;
+constexpr int kSfChunkRows = 128;
+constexpr int kSfTmemCol = 256;  // first TMEM column of the block scales (after one 256-column accumulator)
 
 // Error-word roles.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3;
@@ -108,6 +121,10 @@ struct KernelParams {
     // or column-major (C[m, n] at C + n * ldc + m) with c_col_major
     float alpha, beta;
     int32_t c_col_major;
+    // block scales (kind::mxf8f6f4 kernels only): chunked as kSfChunkBytes describes
+    int32_t sfb_blocks;          // ceil(N / 128)
+    const uint8_t* sfa;          // ceil(M / 128) x num_kb chunks
+    const uint8_t* sfb;          // sfb_blocks x num_kb chunks
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -173,20 +190,37 @@ struct WorkIter {
     }
 };
 
-template <int B_ROWS, int STAGES>
+// SF_BYTES: block-scale bytes per ring stage (0 without block scales); STG_BUFS: staging
+// buffers per epilogue warp.
+template <int B_ROWS, int STAGES, int SF_BYTES = 0, int STG_BUFS = 2>
 struct Smem {
     static constexpr int kABytes = kBM * kRowBytes;
     static constexpr int kBBytes = B_ROWS * kRowBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRing = STAGES * kStageBytes;
-    static constexpr int kStgOff = kRing;
-    static constexpr int kStg = kEpiWarps * 2 * kStgBytes;
+    static constexpr int kSfOff = kRing;
+    static constexpr int kSfBytes = SF_BYTES;
+    static constexpr int kStgOff = kSfOff + STAGES * SF_BYTES;
+    static constexpr int kStgBufs = STG_BUFS;
+    static constexpr int kStg = kEpiWarps * STG_BUFS * kStgBytes;
     static constexpr int kBarOff = kStgOff + kStg;
     static constexpr int kNumBars = 2 * STAGES + 5;  // full, empty, acc_full[2], acc_empty[2], drain
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kTotal = kMiscOff + 16;     // tmem slot, abort flag, stream-K "last" flag
     static constexpr int kAlloc = kTotal + 1024;     // slack for aligning the base to 1 KB
     static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(kStgOff % 1024 == 0, "the swizzled staging buffers need 1 KB alignment");
+};
+
+// Shared-memory layout of a kernel instantiation (host and device agree through this).
+// Block-scaled kernels add the scale chunks of each stage (one for A, one per 128 B rows)
+// and, to stay within 227 KB, keep one staging buffer per epilogue warp.
+template <int BN, int STAGES, int IN, bool PAIR>
+struct KernelLayout {
+    static constexpr int kBRows = BN / (PAIR ? 2 : 1);
+    static constexpr bool kMX = Operand<IN>::kMX;
+    static constexpr int kSfBytes = kMX ? kSfChunkBytes * (1 + kBRows / kSfChunkRows) : 0;
+    using S = Smem<kBRows, STAGES, kSfBytes, kMX ? 1 : 2>;
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
@@ -202,6 +236,30 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t addr, uint32_t lbo,
     d |= 2ull << 61;
     return d;
 }
+
+// tcgen05 shared-memory matrix descriptor for an unswizzled matrix of 16-byte rows: core
+// matrices of 8 rows x 16 B (128 contiguous bytes), 8-row groups `sbo` bytes apart.
+__device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;  // layout bits 61-63 = 0: no swizzle
+    return d;
+}
+
+// Instruction descriptor of tcgen05.mma.kind::mxf8f6f4.block_scale: D fp32 (implied), A and
+// B of the same 8-bit format (0 E4M3, 1 E5M2), A K-major, B K-major or N-major, scale format
+// E8M0 (bit 23), M x N shape.  Bits 29-30 / 4-5 select the byte of the TMEM words holding
+// the scales of A / B: mx_scale_ids(k) for the k-th 32-long K block of a stage.
+template <uint32_t FORMAT, bool B_MN_MAJOR, int M, int N>
+__host__ __device__ constexpr uint32_t idesc_mx()
+{
+    return (FORMAT << 7) | (FORMAT << 10) | ((B_MN_MAJOR ? 1u : 0u) << 16) |
+           (static_cast<uint32_t>(N >> 3) << 17) | (1u << 23) | (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__host__ __device__ constexpr uint32_t mx_scale_ids(uint32_t k) { return (k << 29) | (k << 4); }
 
 // Instruction descriptor of tcgen05.mma.kind::f16 / kind::f8f6f4: D fp32, A and B of the same
 // format (kind::f16: 0 fp16, 1 bf16; kind::f8f6f4: 0 E4M3, 1 E5M2), A K-major, B K-major (TN)
@@ -310,8 +368,9 @@ __device__ __forceinline__ uint16_t cvt16(uint32_t f_bits)
 //  * Column-major C (the same page's transposed store, mma.store.transp): the box is staged
 //    transposed (64 rows of n, 32 m values each) and stored through a tensor map of C's
 //    storage; a box straddling a ragged M (M % 8 != 0) is written with plain stores.
-// Returns true if the staging buffer was used (the caller then alternates buffers).
-template <bool BF16>
+// STG_BUFS: staging buffers of this warp (1 or 2).  Returns true if the staging buffer was
+// used (the caller then moves on to its next buffer).
+template <bool BF16, int STG_BUFS>
 __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t y, int lane, uint32_t stg,
                                           const CUtensorMap* tmC, const KernelParams& p)
 {
@@ -338,7 +397,7 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
             }
             return false;
         }
-        if (lane == 0) ptx::bulk_wait_group_read<1>();
+        if (lane == 0) ptx::bulk_wait_group_read<STG_BUFS - 1>();
         __syncwarp();
         // Dense staging box: (n, m) at n * 64 B + m * 2 B.
 #pragma unroll
@@ -377,9 +436,9 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
         }
         return false;
     }
-    // The staging buffer is reusable once the store issued from it two boxes ago has
+    // The staging buffer is reusable once the store issued from it STG_BUFS boxes ago has
     // finished reading it.
-    if (lane == 0) ptx::bulk_wait_group_read<1>();
+    if (lane == 0) ptx::bulk_wait_group_read<STG_BUFS - 1>();
     __syncwarp();
     const uint32_t srow = stg + lane * 128;
 #pragma unroll
@@ -446,9 +505,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kRanks = PAIR ? 2 : 1;
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
-    constexpr uint32_t kTmemCols = 2 * BN;     // two accumulator buffers
+    // Block-scaled kernels keep one accumulator and put the scales of every ring stage in
+    // the TMEM columns after it; the others double-buffer the accumulator.
+    constexpr int kAccBufs = T::kMX ? 1 : 2;
+    constexpr uint32_t kTmemCols = T::kMX ? 512 : 2 * BN;
     static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
-    using L = Smem<kBRows, STAGES>;
+    using L = typename KernelLayout<BN, STAGES, IN, PAIR>::S;
+    constexpr int kSfChunks = L::kSfBytes / kSfChunkBytes;  // per stage: A, then B
+    static_assert(!T::kMX || (!PAIR && BN <= kSfTmemCol &&
+                              kSfTmemCol + STAGES * kSfChunks * 4 <= static_cast<int>(kTmemCols)),
+                  "block-scaled kernels: one CTA, the accumulator and the scales fit in TMEM");
 
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1 KB (128-byte swizzle atoms repeat every 8 rows).
@@ -535,8 +601,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                         const uint32_t sb = sa + L::kABytes;
                         const int32_t k0 = kb * T::kStageK;
                         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                        // Block scales: the A chunk of this tile row and the B chunks of this
+                        // tile's columns that exist (a ragged N may leave out the last).
+                        int sf_b_chunks = 0;
+                        if constexpr (T::kMX) {
+                            const int64_t nb0 = tn * (BN / kSfChunkRows);
+                            sf_b_chunks = static_cast<int>(p.sfb_blocks - nb0);
+                            if (sf_b_chunks > kSfChunks - 1) sf_b_chunks = kSfChunks - 1;
+                        }
                         if (leader) {
-                            ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes);
+                            const int sf_bytes = T::kMX ? (1 + sf_b_chunks) * kSfChunkBytes : 0;
+                            ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes + sf_bytes);
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         }
@@ -556,6 +631,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                         } else {
                             // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
+                        }
+                        if constexpr (T::kMX) {
+                            const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
+                            const int64_t g = kb;
+                            ptx::bulk_load_1d(sf, p.sfa + (tm * p.num_kb + g) * kSfChunkBytes, kSfChunkBytes, fb);
+                            const int64_t nb0 = tn * (BN / kSfChunkRows);
+                            for (int j = 0; j < sf_b_chunks; ++j)
+                                ptx::bulk_load_1d(sf + (1 + j) * kSfChunkBytes,
+                                                  p.sfb + ((nb0 + j) * p.num_kb + g) * kSfChunkBytes, kSfChunkBytes,
+                                                  fb);
                         }
                     }
                     if (++stage == STAGES) {
@@ -584,7 +669,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0 && leader) {
             // ---------------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc = idesc_mma<T::kFormat, NN, kTileM, BN>();
+            constexpr uint32_t idesc =
+                T::kMX ? idesc_mx<T::kFormat, NN, kTileM, BN>() : idesc_mma<T::kFormat, NN, kTileM, BN>();
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -608,6 +694,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tc_fence_after_sync();
                     const uint32_t sa = base + stage * L::kStageBytes;
                     const uint32_t sb = sa + L::kABytes;
+                    // Block scales of this stage: shared memory -> TMEM (4 columns per chunk:
+                    // A at sf_tmem, B from sf_tmem + 4).  The copies run before the MMAs
+                    // below, which read them; the stage's commit covers both.
+                    uint32_t sf_tmem = 0;
+                    if constexpr (T::kMX) {
+                        sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSfChunks * 4);
+                        const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
+#pragma unroll
+                        for (int c = 0; c < kSfChunks; ++c)
+                            ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, smem_desc_plain(sf + c * kSfChunkBytes, 0, 128));
+                    }
 #pragma unroll
                     for (int k = 0; k < T::kStageK / T::kMmaK; ++k) {
                         // A (K-major, 128B swizzle): the k-th K slice starts 32 B further along
@@ -629,7 +726,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else
                                 ptx::mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);
                         } else {
-                            if constexpr (T::kF8)
+                            if constexpr (T::kMX)
+                                ptx::mma_mxf8_cta1(d_tmem, adesc, bdesc, idesc | mx_scale_ids(k), sf_tmem, sf_tmem + 4,
+                                                   accumulate);
+                            else if constexpr (T::kF8)
                                 ptx::mma_f8_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
                             else
                                 ptx::mma_f16_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
@@ -650,7 +750,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::mma_commit_pair_mc(accf_bar(acc), 0x3);  // accumulator complete
                 else
                     ptx::mma_commit_cta1(accf_bar(acc));
-                if (++acc == 2) {
+                if (++acc == kAccBufs) {
                     acc = 0;
                     acc_phase ^= 1u;
                 }
@@ -670,7 +770,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int ew = warp - kEpiWarp0;            // 0..3: staging buffers
         const int quad = warp & 3;                  // TMEM lane quadrant this warp may read
         const int row_in_cta = quad * 32 + lane;    // accumulator row of this thread
-        const uint32_t stg0 = base + L::kStgOff + ew * 2 * kStgBytes;
+        const uint32_t stg0 = base + L::kStgOff + ew * L::kStgBufs * kStgBytes;
         const uint32_t lane_off = static_cast<uint32_t>(quad * 32) << 16;
         int acc = 0;
         uint32_t acc_phase = 0;
@@ -709,7 +809,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     ptx::tmem_wait_ld();
                     if (c == BN / kEpiCols - 1) release_acc();
                     const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                    if (store_box<OUT_BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+                    if (store_box<OUT_BF16, L::kStgBufs>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= L::kStgBufs - 1;
                 }
             } else {
                 // Part of a stream-K tile: park the fp32 partial sums in this unit's slot.
@@ -764,7 +864,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 64; ++i) v[i] = __float_as_uint(s[i]);
                         const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
-                        if (store_box<OUT_BF16>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= 1;
+                        if (store_box<OUT_BF16, L::kStgBufs>(v, x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p)) sbuf ^= L::kStgBufs - 1;
                     }
                 };
                 // Are all the other parts in already?  Then this part is the last: it skips
@@ -813,7 +913,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (*last_flag) reduce_and_store(false);
                 }
             }
-            if (++acc == 2) {
+            if (++acc == kAccBufs) {
                 acc = 0;
                 acc_phase ^= 1u;
             }

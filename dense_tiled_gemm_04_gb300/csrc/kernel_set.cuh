@@ -1,7 +1,7 @@
 // The set of kernel instantiations the host can launch, and how it names them.
 //
 // Each operand type's instantiations live in a translation unit of their own
-// (kernels_f16.cu, kernels_bf16.cu, kernels_e4m3.cu, kernels_e5m2.cu) so that nvcc
+// (kernels_f16.cu, kernels_bf16.cu, kernels_e4m3.cu, kernels_e5m2.cu, kernels_mx.cu) so that nvcc
 // compiles them in parallel; the host reaches them through the choice_* functions below,
 // which return the kernel's address and launch shape.
 #pragma once
@@ -30,7 +30,7 @@ KernelChoice one_cta_choice(int config)
 {
     return {config, kBM, BN, BN, Operand<IN>::kStageK, Operand<IN>::kNBlock, STAGES, 1,
             reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, STAGES, IN, OUT_BF16, NN, false>),
-            Smem<BN, STAGES>::kAlloc};
+            KernelLayout<BN, STAGES, IN, false>::S::kAlloc};
 }
 
 template <int IN, bool OUT_BF16, bool NN>
@@ -39,7 +39,7 @@ KernelChoice choice_for(int config)
     if (config == 3)  // GEMM_CONFIG_256x256
         return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, kPairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kPairStages, IN, OUT_BF16, NN, true>),
-                Smem<128, kPairStages>::kAlloc};
+                KernelLayout<256, kPairStages, IN, true>::S::kAlloc};
     if (config == 2)  // GEMM_CONFIG_128x128
         return one_cta_choice<128, 6, IN, OUT_BF16, NN>(config);
     return one_cta_choice<256, 4, IN, OUT_BF16, NN>(1);  // GEMM_CONFIG_128x256
@@ -56,5 +56,7 @@ KernelChoice choice_f16(int config, bool nn);
 KernelChoice choice_bf16(int config, bool nn);
 KernelChoice choice_e4m3(int config, bool out_bf16, bool nn);
 KernelChoice choice_e5m2(int config, bool out_bf16, bool nn);
+// Block-scaled 8-bit operands: one configuration (128 x 256, one CTA).
+KernelChoice choice_mx(bool e5m2, bool out_bf16, bool nn);
 
 }  // namespace dtg

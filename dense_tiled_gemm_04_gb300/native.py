@@ -71,6 +71,9 @@ def load() -> ctypes.CDLL:
         "gemm_run": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
         "gemm_run_host": ([p, p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p], i32),
         "gemm_run_ex": ([p, ctypes.POINTER(gemm_args_t), p], i32),
+        "gemm_run_mx": ([p, ctypes.POINTER(gemm_args_t), p, p, p], i32),
+        "gemm_mx_scale_bytes": ([i64, i64], i64),
+        "gemm_mx_pack_scales": ([p, p, i64, i64, i64, p, p], i32),
         "gemm_sync_status": ([p, p], i32),
         "gemm_error_info": ([p, ctypes.POINTER(i32)], i32),
         "gemm_set_option": ([p, i32, i64], i32),
@@ -97,6 +100,11 @@ def status_string(status: int) -> str:
 def check_args(A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int) -> int:
     """gemm_check_args on raw addresses (no GPU needed)."""
     return int(load().gemm_check_args(A or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype))
+
+
+def mx_scale_bytes(rows: int, K: int) -> int:
+    """Bytes of the chunked block-scale layout for `rows` rows and K elements of K."""
+    return int(load().gemm_mx_scale_bytes(rows, K))
 
 
 def tile_coord(tile: int, tiles_m: int, tiles_n: int, group_m: int):
@@ -251,6 +259,61 @@ class Gemm:
                              _stream_ptr(stream), TORCH_TO_DTYPE[out_dtype], scale_a, scale_b)
         if st != OK:
             raise GemmError(st, "gemm_run_ex")
+        return C
+
+    def pack_scales(self, sf: torch.Tensor, K: int | None = None, stream=None) -> torch.Tensor:
+        """Row-major E8M0 exponents (rows x ceil(K/32), uint8, on the device) -> the chunked
+        layout gemm_run_mx reads, in a new uint8 tensor (gemm_mx_pack_scales, async)."""
+        if sf.dtype != torch.uint8 or sf.dim() != 2 or (sf.size(1) > 1 and sf.stride(1) != 1):
+            raise ValueError("expected a 2-D row-major uint8 tensor")
+        rows, kblocks = sf.shape
+        K = 32 * kblocks if K is None else K
+        if -(-K // 32) != kblocks:
+            raise ValueError(f"{kblocks} K blocks do not cover K = {K}")
+        out = torch.empty(max(mx_scale_bytes(rows, K), 16), dtype=torch.uint8, device=sf.device)
+        ld = sf.stride(0) if rows > 1 else max(kblocks, 1)
+        st = self._lib.gemm_mx_pack_scales(self._h, sf.data_ptr() or None, rows, kblocks, ld, out.data_ptr(),
+                                           _stream_ptr(stream))
+        if st != OK:
+            raise GemmError(st, "gemm_mx_pack_scales")
+        return out
+
+    def run_mx_raw(self, A: int, B: int, C: int, sfa: int, sfb: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int,
+                   out_dtype: int, alpha: float = 1.0, beta: float = 0.0, c_col_major: int = 0, scale_a: float = 1.0,
+                   scale_b: float = 1.0, stream: int = 0) -> int:
+        """gemm_run_mx on raw device addresses; returns the status code."""
+        a = gemm_args_t(A or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype, alpha, beta,
+                        c_col_major, out_dtype, scale_a, scale_b)
+        return int(self._lib.gemm_run_mx(self._h, ctypes.byref(a), sfa or None, sfb or None, stream or None))
+
+    def run_mx(self, A: torch.Tensor, B: torch.Tensor, sfa: torch.Tensor, sfb: torch.Tensor,
+               C: torch.Tensor | None = None, layout: str = "NN", out_dtype: torch.dtype = torch.bfloat16,
+               alpha: float = 1.0, beta: float = 0.0, scale_a: float = 1.0, scale_b: float = 1.0,
+               c_col_major: bool = False, stream=None) -> torch.Tensor:
+        """C = alpha * scale_a * scale_b * (A·B with per-tile E8M0 scales) + beta * C on device
+        tensors: A, B float8_e4m3fn / float8_e5m2; sfa, sfb the chunked scales (pack_scales).
+        Async on `stream`."""
+        M, K = A.shape
+        N = B.shape[1] if layout == "NN" else B.shape[0]
+        if (B.shape[0] if layout == "NN" else B.shape[1]) != K:
+            raise ValueError(f"shape mismatch: A {tuple(A.shape)}, B {tuple(B.shape)}, layout {layout}")
+        if A.dtype != B.dtype or A.dtype not in (torch.float8_e4m3fn, torch.float8_e5m2):
+            raise TypeError("A and B must have the same 8-bit float type")
+        if out_dtype not in TORCH_TO_DTYPE:
+            raise TypeError("C must be float16 or bfloat16")
+        for t, rows, what in ((sfa, M, "sfa"), (sfb, N, "sfb")):
+            if t.dtype != torch.uint8 or t.numel() < mx_scale_bytes(rows, K):
+                raise ValueError(f"{what} must hold {mx_scale_bytes(rows, K)} bytes of packed scales")
+        shape = (N, M) if c_col_major else (M, N)
+        if C is None:
+            C = empty_output(*shape, out_dtype, A.device)
+        if tuple(C.shape) != shape or C.dtype != out_dtype:
+            raise ValueError("C has the wrong shape or dtype")
+        st = self.run_mx_raw(A.data_ptr(), B.data_ptr(), C.data_ptr(), sfa.data_ptr(), sfb.data_ptr(), M, N, K, _ld(A),
+                             _ld(B), _ld(C), LAYOUTS[layout], TORCH_TO_DTYPE_EX[A.dtype], TORCH_TO_DTYPE[out_dtype],
+                             alpha, beta, int(c_col_major), scale_a, scale_b, _stream_ptr(stream))
+        if st != OK:
+            raise GemmError(st, "gemm_run_mx")
         return C
 
     def run_host(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, layout: str = "NN", stream=None) -> int:

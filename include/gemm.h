@@ -159,6 +159,38 @@ typedef struct {
 
 gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream);
 
+/* 8-bit operands with per-tile scales: C = alpha * scale_a * scale_b * acc + beta * C with
+ *     acc[m, n] = sum_j 2^(ea[m, j] - 127) * 2^(eb[n, j] - 127) * sum_{k in block j} A[m, k] * Beff[k, n]
+ * over K blocks j of 32 elements (the last one shorter when K % 32 != 0).  This is the scaled
+ * contraction of "张量缩并：mma 语法" (each tile's product multiplied by the A tile's scale
+ * sc_a and the B tile's scale sc_b), with tiles of one row of A, or one column of B, by 32
+ * K elements, and scales in E8M0 (8-bit exponents; 255 is NaN): tcgen05's block-scaled MMA
+ * applies them inside the contraction, so no separate dequantisation pass runs.
+ *   - args: as for gemm_run_ex, with dtype E4M3 or E5M2 (anything else: INVALID_ARG).
+ *     GEMM_OPT_CONFIG does not apply: these kernels use one 128 x 256 configuration.
+ *   - sfa: the exponents ea of A (M x ceil(K/32)), sfb: those of B (one row per column n of
+ *     Beff, N x ceil(K/32)), both device pointers, 16-byte aligned, in the chunked layout that
+ *     gemm_mx_pack_scales writes (gemm_mx_scale_bytes(M, K) and (N, K) bytes).  Unused when
+ *     K == 0; otherwise null is INVALID_ARG and misalignment UNSUPPORTED.
+ *   - Padding entries of the chunked layout must hold finite scales (the packer writes 127). */
+gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* sfa, const void* sfb,
+                          void* stream);
+
+/* Bytes of the chunked block-scale layout for `rows` rows and K elements of K:
+ * ceil(rows / 128) * ceil(K / 128) * 512 (0 when rows or K is 0).  Chunk (rb, g) covers rows
+ * [128 rb, 128 rb + 128) and K blocks [4 g, 4 g + 4) and starts at byte (rb * ceil(K/128) + g)
+ * * 512; inside it, row r and K block c of the chunk sit at byte (r % 32) * 16 + (r / 32) * 4
+ * + c. */
+int64_t gemm_mx_scale_bytes(int64_t rows, int64_t K);
+
+/* Enqueue on `stream` the rearrangement of row-major exponents src[r * ld + j] (rows x
+ * kblocks bytes, ld >= kblocks; device memory) into the chunked layout at dst (device,
+ * gemm_mx_scale_bytes(rows, 32 * kblocks) bytes), padding with 127 (a scale of 1).
+ * rows == 0 or kblocks == 0 is a no-op; negative sizes, null pointers or ld < kblocks are
+ * INVALID_ARG. */
+gemm_status_t gemm_mx_pack_scales(gemm_handle_t h, const void* src, int64_t rows, int64_t kblocks, int64_t ld,
+                                  void* dst, void* stream);
+
 /* Same operation on HOST buffers (pinned memory lets the copies run as DMA): copies A and
  * B to handle-owned device buffers on `stream`, runs the kernel, copies C back (only the
  * M x N window, never the row padding) and synchronises the stream.  Returns the

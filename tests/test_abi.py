@@ -134,3 +134,13 @@ def test_tile_coord_groups_rows(lib):
     assert coords == [(0, 0), (1, 0), (2, 0), (3, 0), (0, 1), (1, 1)]
     with pytest.raises(Exception):
         lib.tile_coord(24, 8, 3, 4)
+
+
+def test_mx_scale_bytes_without_a_gpu(lib):
+    assert lib.mx_scale_bytes(0, 64) == 0 and lib.mx_scale_bytes(5, 0) == 0
+    assert lib.mx_scale_bytes(1, 1) == 512 and lib.mx_scale_bytes(128, 128) == 512
+    assert lib.mx_scale_bytes(129, 129) == 2 * 2 * 512
+    assert lib.mx_scale_bytes(8192, 8192) == 64 * 64 * 512
+    so = lib.load()
+    assert so.gemm_mx_pack_scales(None, None, 1, 1, 1, None, None) == lib.ERR_INVALID_ARG
+    assert so.gemm_run_mx(None, None, None, None, None) == lib.ERR_INVALID_ARG
