@@ -356,23 +356,12 @@ __device__ __forceinline__ uint16_t cvt16(uint32_t f_bits)
         return __half_as_ushort(__float2half_rn(__uint_as_float(f_bits)));
 }
 
-// Write the 32-row x 64-column box of C at (row y, column x) that this warp holds (lane =
-// row, v = the 64 fp32 accumulator bit patterns of that row; v is scaled in place).
-//  * C = alpha * acc + beta * C: "张量缩并：mma 语法" states the contraction as C += A × B
-//    (alpha = beta = 1); the existing C is read only when beta != 0.
-//  * Row-major C: the box goes through a 128-byte-swizzled staging buffer and one TMA store,
-//    which drops rows >= M and columns >= N (the masked write-back of "NineToothed GEMM 语法
-//    入门" §5).  A TMA store clips the inner dimension only to 16-byte granules, so when N
-//    is not a multiple of 8 the box that straddles column N is written with plain masked
-//    stores instead.
-//  * Column-major C (the same page's transposed store, mma.store.transp): the box is staged
-//    transposed (64 rows of n, 32 m values each) and stored through a tensor map of C's
-//    storage; a box straddling a ragged M (M % 8 != 0) is written with plain stores.
-// STG_BUFS: staging buffers of this warp (1 or 2).  Returns true if the staging buffer was
-// used (the caller then moves on to its next buffer).
-template <bool BF16, int STG_BUFS>
-__device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t y, int lane, uint32_t stg,
-                                          const CUtensorMap* tmC, const KernelParams& p)
+// C = alpha * acc + beta * C on the 32-row x 64-column box of C at (row y, column x) that
+// this warp holds (lane = row, v = the 64 fp32 accumulator bit patterns of that row, scaled
+// in place).  "张量缩并：mma 语法" states the contraction as C += A × B (alpha = beta = 1);
+// the existing C is read only when beta != 0.
+template <bool BF16>
+__device__ __forceinline__ void scale_box(uint32_t (&v)[64], int32_t x, int32_t y, int lane, const KernelParams& p)
 {
     const int64_t row = static_cast<int64_t>(y) + lane;  // this thread's output row m
     if (p.alpha != 1.0f || p.beta != 0.0f) {
@@ -387,13 +376,45 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
             v[i] = __float_as_uint(f);
         }
     }
+}
+
+// Round the 64 fp32 values of a box row to 16 bits (round to nearest even), two per word:
+// element 2i in the low half of h[i].
+template <bool BF16>
+__device__ __forceinline__ void pack_box(const uint32_t (&v)[64], uint32_t (&h)[32])
+{
+#pragma unroll
+    for (int i = 0; i < 32; ++i) h[i] = pack2<BF16>(v[2 * i], v[2 * i + 1]);
+}
+
+__device__ __forceinline__ uint16_t half_of(const uint32_t (&h)[32], int i)
+{
+    return static_cast<uint16_t>((h[i >> 1] >> ((i & 1) * 16)) & 0xFFFFu);
+}
+
+// Write a box of C already rounded to 16 bits (h, as pack_box leaves it).
+//  * Row-major C: the box goes through a 128-byte-swizzled staging buffer and one TMA store,
+//    which drops rows >= M and columns >= N (the masked write-back of "NineToothed GEMM 语法
+//    入门" §5).  A TMA store clips the inner dimension only to 16-byte granules, so when N
+//    is not a multiple of 8 the box that straddles column N is written with plain masked
+//    stores instead.
+//  * Column-major C (the transposed store of "张量缩并：mma 语法", mma.store.transp): the box
+//    is staged transposed (64 rows of n, 32 m values each) and stored through a tensor map of
+//    C's storage; a box straddling a ragged M (M % 8 != 0) is written with plain stores.
+// STG_BUFS: staging buffers of this warp (1 or 2).  Returns true if the staging buffer was
+// used (the caller then moves on to its next buffer).
+template <int STG_BUFS>
+__device__ __forceinline__ bool store_packed(const uint32_t (&h)[32], int32_t x, int32_t y, int lane, uint32_t stg,
+                                             const CUtensorMap* tmC, const KernelParams& p)
+{
+    const int64_t row = static_cast<int64_t>(y) + lane;  // this thread's output row m
     if (p.c_col_major) {
         if ((p.M & 7) != 0 && y + 32 > p.M) {
             if (row < p.M) {
                 uint16_t* c16 = static_cast<uint16_t*>(p.C);
 #pragma unroll
                 for (int i = 0; i < 64; ++i)
-                    if (x + i < p.N) c16[static_cast<int64_t>(x + i) * p.ldc + row] = cvt16<BF16>(v[i]);
+                    if (x + i < p.N) c16[static_cast<int64_t>(x + i) * p.ldc + row] = half_of(h, i);
             }
             return false;
         }
@@ -402,7 +423,7 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
         // Dense staging box: (n, m) at n * 64 B + m * 2 B.
 #pragma unroll
         for (int i = 0; i < 64; ++i)
-            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stg + i * 64 + lane * 2), "h"(cvt16<BF16>(v[i])) : "memory");
+            asm volatile("st.shared.u16 [%0], %1;" ::"r"(stg + i * 64 + lane * 2), "h"(half_of(h, i)) : "memory");
         ptx::fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
@@ -418,19 +439,12 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
             for (int ch = 0; ch < 8; ++ch) {
                 const int32_t col = x + ch * 8;
                 if (col + 8 <= p.N) {  // a whole 16-byte chunk: one vector store
-                    uint4 q;
-                    q.x = pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]);
-                    q.y = pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]);
-                    q.z = pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]);
-                    q.w = pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]);
-                    *reinterpret_cast<uint4*>(crow + col) = q;
+                    *reinterpret_cast<uint4*>(crow + col) = make_uint4(h[4 * ch], h[4 * ch + 1], h[4 * ch + 2],
+                                                                       h[4 * ch + 3]);
                 } else {
 #pragma unroll
-                    for (int e = 0; e < 8; e += 2) {
-                        const uint32_t two = pack2<BF16>(v[8 * ch + e], v[8 * ch + e + 1]);
-                        if (col + e < p.N) crow[col + e] = static_cast<uint16_t>(two & 0xFFFFu);
-                        if (col + e + 1 < p.N) crow[col + e + 1] = static_cast<uint16_t>(two >> 16);
-                    }
+                    for (int e = 0; e < 8; ++e)
+                        if (col + e < p.N) crow[col + e] = half_of(h, 8 * ch + e);
                 }
             }
         }
@@ -446,8 +460,7 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
         // 16-byte chunk ch of this row lands at chunk (ch ^ row%8): the 128-byte swizzle
         // the TMA store expects.
         const uint32_t addr = srow + ((ch ^ (lane & 7)) << 4);
-        ptx::st_shared_v4(addr, pack2<BF16>(v[8 * ch + 0], v[8 * ch + 1]), pack2<BF16>(v[8 * ch + 2], v[8 * ch + 3]),
-                          pack2<BF16>(v[8 * ch + 4], v[8 * ch + 5]), pack2<BF16>(v[8 * ch + 6], v[8 * ch + 7]));
+        ptx::st_shared_v4(addr, h[4 * ch], h[4 * ch + 1], h[4 * ch + 2], h[4 * ch + 3]);
     }
     ptx::fence_proxy_async_smem();
     __syncwarp();
@@ -456,6 +469,17 @@ __device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t 
         ptx::bulk_commit_group();
     }
     return true;
+}
+
+// scale_box, pack_box and store_packed in one: the box of fp32 accumulator values v.
+template <bool BF16, int STG_BUFS>
+__device__ __forceinline__ bool store_box(uint32_t (&v)[64], int32_t x, int32_t y, int lane, uint32_t stg,
+                                          const CUtensorMap* tmC, const KernelParams& p)
+{
+    scale_box<BF16>(v, x, y, lane, p);
+    uint32_t h[32];
+    pack_box<BF16>(v, h);
+    return store_packed<STG_BUFS>(h, x, y, lane, stg, tmC, p);
 }
 
 __device__ __forceinline__ void epilogue_bar_sync()
@@ -797,7 +821,30 @@ __global__ void __launch_bounds__(kThreads, 1)
             ptx::tc_fence_after_sync();
             const int32_t y = static_cast<int32_t>(tm * kTileM + rank * kBM + quad * 32);
             const uint32_t tacc = tmem_base + lane_off + static_cast<uint32_t>(acc * BN);
-            if (kb0 == 0 && kb1 == p.num_kb) {
+            if (kAccBufs == 1 && kb0 == 0 && kb1 == p.num_kb) {
+                // Whole tile, single accumulator: read the whole row of the accumulator into
+                // registers (scaled, rounded to 16 bits) and hand the accumulator back before
+                // storing, so that the next item's MMAs run while this tile is written.
+                uint32_t h[BN / kEpiCols][32];
+#pragma unroll
+                for (int c = 0; c < BN / kEpiCols; ++c) {
+                    uint32_t v[64];
+                    uint32_t(&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+                    uint32_t(&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+                    ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols, v0);
+                    ptx::tmem_ld_32x32b_x32(tacc + c * kEpiCols + 32, v1);
+                    ptx::tmem_wait_ld();
+                    scale_box<OUT_BF16>(v, static_cast<int32_t>(tn * BN + c * kEpiCols), y, lane, p);
+                    pack_box<OUT_BF16>(v, h[c]);
+                }
+                release_acc();
+#pragma unroll
+                for (int c = 0; c < BN / kEpiCols; ++c) {
+                    const int32_t x = static_cast<int32_t>(tn * BN + c * kEpiCols);
+                    if (store_packed<L::kStgBufs>(h[c], x, y, lane, stg0 + sbuf * kStgBytes, &tmC, p))
+                        sbuf ^= L::kStgBufs - 1;
+                }
+            } else if (kb0 == 0 && kb1 == p.num_kb) {
                 // Whole tile: convert and store.
 #pragma unroll 1
                 for (int c = 0; c < BN / kEpiCols; ++c) {
