@@ -1,6 +1,10 @@
 """Benchmark: C = A·B through the library's C ABI on the square bf16 8192^3 TN GEMM.
 
-    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
+
+``--workload`` picks another row of the workload table: c1..c5 (16-bit operands),
+c4-e4m3 (8-bit operands, per-tensor scales, gemm_run_ex) or c4-mx (8-bit operands with
+E8M0 scales per 32 K elements, gemm_run_mx).
 
 One step = one full GEMM (the whole hot path: TMA ring, tcgen05 MMA, epilogue) on
 inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank runs
@@ -156,6 +160,23 @@ def barrier(world):
 # ------------------------------------------------------------------ CPU oracle timing
 
 
+def oracle_rows_fn(A, B, w):
+    """rows -> threads used, computing those rows of C with the oracle routine of the workload."""
+    import oracle
+    from dense_tiled_gemm_04_gb300.workloads import block_scales, tensor_scales
+
+    if w.elem_bytes == 2:
+        return lambda rows: oracle.gemm_rows(A, B, w.layout, w.dtype, rows)[2]
+    threads = oracle.max_threads()
+    if w.scales == "block":
+        sa, sb = block_scales(w)
+        return lambda rows: (oracle.gemm_blockscaled(A, B, sa, sb, w.layout, w.dtype, w.out_dtype, rows=rows),
+                             threads)[1]
+    s_a, s_b = tensor_scales(w)
+    return lambda rows: (oracle.gemm_typed(A, B, w.layout, w.dtype, w.out_dtype, alpha=s_a * s_b, rows=rows),
+                         threads)[1]
+
+
 def oracle_rows_sample(A, B, w, target_s: float):
     """Time the oracle on whole rows of C: calibrate on one batch, then run ~target_s."""
     import numpy as np
@@ -163,15 +184,16 @@ def oracle_rows_sample(A, B, w, target_s: float):
     import oracle
 
     threads = oracle.max_threads()
+    fn = oracle_rows_fn(A, B, w)
     rng = np.random.default_rng(0)
     calib = rng.integers(0, w.M, threads)
     t0 = time.perf_counter()
-    _, _, used = oracle.gemm_rows(A, B, w.layout, w.dtype, calib)
+    used = fn(calib)
     t_cal = time.perf_counter() - t0
     batches = max(1, int(target_s / max(t_cal, 1e-3)))
     rows = rng.integers(0, w.M, threads * batches)
     t0 = time.perf_counter()
-    _, _, used = oracle.gemm_rows(A, B, w.layout, w.dtype, rows)
+    used = fn(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows.size * w.N * w.K
     return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
@@ -192,6 +214,8 @@ def run_reference(args, w):
     oracle.build()
     A, B = workload_inputs(w)
     threads = oracle.max_threads()
+    if w.elem_bytes == 1:
+        return run_reference_rows(args, w, A, B, threads)
     rng = np.random.default_rng(1)
     # Elements per step sized so warm-up + timed steps take about a minute in total.
     probe = 64 * threads
@@ -224,7 +248,81 @@ def run_reference(args, w):
     return 0
 
 
+def run_reference_rows(args, w, A, B, threads):
+    """Reference arm for the 8-bit workloads: whole rows of C per step with the oracle."""
+    import numpy as np
+
+    fn = oracle_rows_fn(A, B, w)
+    rng = np.random.default_rng(1)
+    t0 = time.perf_counter()
+    fn(rng.integers(0, w.M, threads))
+    per_row = (time.perf_counter() - t0) / threads
+    total_steps = args.steps + args.warmup
+    nrows = int(max(threads, min(w.M, 60.0 / max(total_steps, 1) / max(per_row, 1e-9))))
+    samples = [rng.integers(0, w.M, nrows) for _ in range(total_steps)]
+    for i in range(args.warmup):
+        fn(samples[i])
+    t0 = time.perf_counter()
+    for i in range(args.warmup, total_steps):
+        fn(samples[i])
+    step_s = (time.perf_counter() - t0) / max(args.steps, 1)
+    value = 2.0 * nrows * w.N * w.K / step_s / 1e12
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": f"synthetic: seeded {w.dist} {w.dtype} inputs (torch CPU generator, seed {w.seed})",
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in_dtype": w.dtype,
+                   "out": w.out_dtype, "scales": w.scales, "sample_per_step": f"{nrows} random rows of C"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{nrows} random rows of C per step ({nrows}x{w.N} fp64 dot products of "
+                                   f"{w.K} terms)"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 # ------------------------------------------------------------------ GPU arm
+
+
+def make_step(g, native, torch, w, A, B, C, stream):
+    """The library call one step makes, for the workload's operand kind.  Returns
+    (step(), plan dict, extra device inputs, description of the kernel kind)."""
+    from dense_tiled_gemm_04_gb300.workloads import block_scales, tensor_scales
+
+    sp = stream.cuda_stream
+    lay, dt = native.LAYOUTS[w.layout], native.DTYPES[w.dtype]
+    base = (A.data_ptr(), B.data_ptr(), C.data_ptr())
+    dims = (w.M, w.N, w.K, A.stride(0), B.stride(0), C.stride(0))
+    if w.elem_bytes == 2:
+        def step():
+            st = g.run_raw(*base, *dims, lay, dt, sp)
+            if st != native.OK:
+                raise native.GemmError(st, "gemm_run")
+        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [], "kind::f16"
+    out = native.DTYPES[w.out_dtype]
+    if w.scales == "tensor":
+        s_a, s_b = tensor_scales(w)
+
+        def step():
+            st = g.run_ex_raw(*base, *dims, lay, dt, 1.0, 0.0, 0, sp, out, s_a, s_b)
+            if st != native.OK:
+                raise native.GemmError(st, "gemm_run_ex")
+        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [], "kind::f8f6f4, per-tensor scales"
+    sa, sb = block_scales(w)
+    psa = g.pack_scales(torch.from_numpy(sa).to(A.device), w.K, stream)
+    psb = g.pack_scales(torch.from_numpy(sb).to(A.device), w.K, stream)
+
+    def step():
+        st = g.run_mx_raw(*base, psa.data_ptr(), psb.data_ptr(), *dims, lay, dt, out, stream=sp)
+        if st != native.OK:
+            raise native.GemmError(st, "gemm_run_mx")
+    old = g.get_option(native.OPT_CONFIG)
+    g.set_option(native.OPT_CONFIG, native.CONFIG_128x256)  # the one block-scaled configuration
+    plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
+    g.set_option(native.OPT_CONFIG, old)
+    return step, plan, [psa, psb], "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
 
 
 def run_ours(args, w):
@@ -248,20 +346,13 @@ def run_ours(args, w):
     g.set_option(native.OPT_CONFIG, {"auto": native.CONFIG_AUTO, "128x256": native.CONFIG_128x256,
                                      "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256}[args.config])
 
+    from dense_tiled_gemm_04_gb300.workloads import TORCH_DTYPES
+
     A_cpu, B_cpu = workload_inputs(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
-    C = native.empty_output(w.M, w.N, A.dtype, dev)
+    C = native.empty_output(w.M, w.N, TORCH_DTYPES[w.out_dtype], dev)
     stream = torch.cuda.current_stream(dev)
-    sp = stream.cuda_stream
-    lay, dt = native.LAYOUTS[w.layout], native.DTYPES[w.dtype]
-    args_raw = (A.data_ptr(), B.data_ptr(), C.data_ptr(), w.M, w.N, w.K, A.stride(0), B.stride(0), C.stride(0),
-                lay, dt, sp)
-    plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
-
-    def step():
-        st = g.run_raw(*args_raw)
-        if st != native.OK:
-            raise native.GemmError(st, "gemm_run")
+    step, plan, extra, kind = make_step(g, native, torch, w, A, B, C, stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -294,7 +385,28 @@ def run_ours(args, w):
     # End to end through the public C ABI on pinned host buffers: H2D of A and B, the
     # kernel, D2H of C, synchronised every step.
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and w.elem_bytes == 1:
+        # 8-bit operands: the same library call, with the step's inputs (A, B and any block
+        # scales) copied in from pinned host memory and C copied back, every step.
+        hosts = [t.cpu().pin_memory() for t in (A, B, *extra)]
+        devs = [A, B, *extra]
+        Ch = torch.empty(C.shape, dtype=C.dtype).pin_memory()
+        e2e_steps = max(3, min(args.steps, 20))
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        for _ in range(e2e_steps):
+            for d_, h_ in zip(devs, hosts):
+                d_.copy_(h_, non_blocking=True)
+            step()
+            Ch.copy_(C, non_blocking=True)
+            stream.synchronize()
+        e2e_s = (time.perf_counter() - t0) / e2e_steps
+        e2e_s = reduce_max([e2e_s], world, dev)[0]
+        e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+               "h2d_bytes_per_step": int(sum(h_.numel() * h_.element_size() for h_ in hosts)),
+               "d2h_bytes_per_step": int(Ch.numel() * 2)}
+    elif not args.no_e2e:
         Ah, Bh = A_cpu.pin_memory(), B_cpu.pin_memory()
         Ch = torch.empty((w.M, w.N), dtype=A_cpu.dtype).pin_memory()
         e2e_steps = max(3, min(args.steps, 20))
@@ -312,15 +424,18 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
 
     peaks, peak_src = load_peaks()
-    peak = float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    # 8-bit operands: the bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25).
+    ratio = 2.0 if w.elem_bytes == 1 else 1.0
+    peak = ratio * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
+    src = f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback bf16"
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": load_traffic(args.workload),
-                "peak_source": f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback",
-                "nominal_dense_peak_tflops": 2250.0, "frac_of_nominal": achieved / 2250.0,
+                "peak_source": src + (" x 2 (nominal fp8/bf16 dense ratio)" if ratio != 1.0 else ""),
+                "nominal_dense_peak_tflops": 2250.0 * ratio, "frac_of_nominal": achieved / (2250.0 * ratio),
                 "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
     if "bf16_tflops_sustained" in peaks:
-        roofline["frac_of_sustained"] = achieved / float(peaks["bf16_tflops_sustained"])
+        roofline["frac_of_sustained"] = achieved / (ratio * float(peaks["bf16_tflops_sustained"]))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -333,10 +448,11 @@ def run_ours(args, w):
             "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": w.dtype,
             "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
-                    f"(torch CPU generator, seed {w.seed})",
+                    f"(torch CPU generator, seed {w.seed})"
+                    + (", E8M0 block scales uniform in 124..130 (numpy generator)" if w.scales == "block" else ""),
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
-                       "accumulate": "fp32", "out": w.dtype,
-                       "kernel": f"tcgen05 {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
+                       "accumulate": "fp32", "out": w.out_dtype,
+                       "kernel": f"tcgen05 {kind}, {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
                                  f"ring, {plan['grid']} persistent CTAs"
                                  + (f" in {plan['grid'] // plan['cluster']} CTA pairs (cta_group::2)"
                                     if plan["cluster"] == 2 else ""),
@@ -366,7 +482,8 @@ def main(argv=None):
     ap.add_argument("--cpu-seconds", type=float, default=10.0, help="target length of the CPU-oracle sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
-    ap.add_argument("--workload", default=WORKLOAD, help="c1..c5 (default c4, the headline workload)")
+    ap.add_argument("--workload", default=WORKLOAD,
+                    help="c1..c5, c4-e4m3, c4-mx (default c4, the headline workload)")
     ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
                     help="kernel configuration (default: the library's own choice)")
     args = ap.parse_args(argv)

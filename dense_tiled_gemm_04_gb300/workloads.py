@@ -6,7 +6,10 @@ take their inputs from it.
 
 Recipe: a CPU ``torch.Generator`` seeded with the workload's seed draws A (M x K)
 first, then B in its *stored* shape (K x N for NN, N x K for TN), in fp32; the
-values are scaled and rounded to fp16/bf16 by torch's round-to-nearest-even cast.
+values are scaled and rounded to the operand type (fp16, bf16, E4M3 or E5M2) by torch's
+round-to-nearest-even cast.  Block scales (E8M0 exponents, one per 32 K elements of each
+row of A and column of B) are drawn by a numpy generator seeded with seed + 1000,
+uniform in {124..130} (scales 1/8 .. 8).
 Distributions: ``uniform`` = U[-1, 1) (``rand*2-1``), ``normal`` = N(0, 1)
 (``randn``), ``int`` = integers uniform in {-2..2} (``randint(-2, 3)``).
 A leading dimension larger than the row length pads each row with NaN, so a
@@ -29,10 +32,20 @@ class Workload:
     N: int
     K: int
     layout: str      # "NN": B stored K x N; "TN": B stored N x K
-    dtype: str       # "f16" | "bf16" (inputs and output)
+    dtype: str       # operand type: "f16" | "bf16" | "e4m3" | "e5m2"
     dist: str        # "uniform" | "normal" | "int" | "ones"
     scale: float     # multiplies the draw (1/sqrt(K) for the normalised workloads)
     seed: int
+    out: str = ""    # type of C ("" = dtype; 8-bit operands: "f16" | "bf16")
+    scales: str = "none"  # 8-bit operands: "tensor" (scale_a = scale_b = K^-1/4) | "block" (E8M0 per 32 K)
+
+    @property
+    def out_dtype(self) -> str:
+        return self.out or self.dtype
+
+    @property
+    def elem_bytes(self) -> int:
+        return 1 if self.dtype in ("e4m3", "e5m2") else 2
 
     @property
     def flops(self) -> int:
@@ -40,8 +53,9 @@ class Workload:
 
     @property
     def algorithmic_bytes(self) -> int:
-        """Read A and B once, write C once (16-bit elements)."""
-        return 2 * (self.M * self.K + self.K * self.N + self.M * self.N)
+        """Read A and B (and their block scales) once, write the 16-bit C once."""
+        sf = (self.M + self.N) * -(-self.K // 32) if self.scales == "block" else 0
+        return self.elem_bytes * (self.M * self.K + self.K * self.N) + 2 * self.M * self.N + sf
 
     def with_dist(self, dist: str, scale: float = 1.0) -> "Workload":
         return replace(self, dist=dist, scale=scale)
@@ -54,7 +68,27 @@ WORKLOADS = {
     "c4": Workload("square bf16 TN 8192^3", 8192, 8192, 8192, "TN", "bf16", "normal", 1.0 / math.sqrt(8192), 3),
     "c5": Workload("tall-skinny fp16 TN 16384x1024x8192", 16384, 1024, 8192, "TN", "f16", "uniform",
                    1.0 / math.sqrt(8192), 4),
+    # 8-bit operands: the scaled contraction of the mma syntax page.
+    "c4-e4m3": Workload("square E4M3 TN 8192^3, bf16 C, per-tensor scales", 8192, 8192, 8192, "TN", "e4m3",
+                        "normal", 1.0, 5, out="bf16", scales="tensor"),
+    "c4-mx": Workload("square E4M3 TN 8192^3, bf16 C, E8M0 scales per 32 K", 8192, 8192, 8192, "TN", "e4m3",
+                      "normal", 1.0, 6, out="bf16", scales="block"),
 }
+
+
+def tensor_scales(w: Workload):
+    """Per-tensor scales of an 8-bit workload: K^-1/4 each, so C is of unit size."""
+    s = float(w.K) ** -0.25
+    return s, s
+
+
+def block_scales(w: Workload):
+    """(sa, sb): E8M0 exponents, M x ceil(K/32) and N x ceil(K/32) uint8 numpy arrays."""
+    import numpy as np
+
+    rng = np.random.default_rng(w.seed + 1000)
+    nb = -(-w.K // 32)
+    return (rng.integers(124, 131, (w.M, nb)).astype(np.uint8), rng.integers(124, 131, (w.N, nb)).astype(np.uint8))
 
 
 def stored_b_shape(M: int, N: int, K: int, layout: str):
