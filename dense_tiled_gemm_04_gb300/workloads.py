@@ -76,6 +76,23 @@ WORKLOADS = {
 }
 
 
+def prune_24(A: torch.Tensor, seed: int) -> torch.Tensor:
+    """A copy of A (M x K, K % 4 == 0) with a 2:4 pattern along K: in every group of four
+    consecutive elements of a row, two positions drawn uniformly from the six pairs (numpy
+    generator seeded with `seed`) keep their values and the other two become zero."""
+    import numpy as np
+
+    M, K = A.shape
+    if K % 4:
+        raise ValueError("K must be a multiple of 4")
+    pairs = np.array([[1, 1, 0, 0], [1, 0, 1, 0], [1, 0, 0, 1], [0, 1, 1, 0], [0, 1, 0, 1], [0, 0, 1, 1]], dtype=bool)
+    rng = np.random.default_rng(seed)
+    mask = pairs[rng.integers(0, 6, (M, K // 4))].reshape(M, K)
+    out = A.clone()
+    out[torch.from_numpy(~mask)] = 0
+    return out
+
+
 def tensor_scales(w: Workload):
     """Per-tensor scales of an 8-bit workload: K^-1/4 each, so C is of unit size."""
     s = float(w.K) ** -0.25

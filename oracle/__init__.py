@@ -78,6 +78,11 @@ def _load():
                                                  ctypes.c_int, ctypes.c_int, ctypes.c_double, ctypes.c_double, p, i64,
                                                  p, p, i64, ctypes.c_int]
     lib.oracle_gemm_rows_blockscaled.restype = ctypes.c_int
+    lib.oracle_sparse24_compress.argtypes = [p, i64, i64, i64, p, i64, p, i64]
+    lib.oracle_sparse24_compress.restype = i64
+    lib.oracle_gemm_rows_sparse24.argtypes = [p, p, p, p, i64, i64, i64, i64, i64, i64, ctypes.c_int, ctypes.c_int,
+                                              ctypes.c_double, ctypes.c_double, p, i64, p, p, i64, ctypes.c_int]
+    lib.oracle_gemm_rows_sparse24.restype = ctypes.c_int
     lib.oracle_e8m0_to_f64.argtypes = [ctypes.c_uint8]
     lib.oracle_e8m0_to_f64.restype = ctypes.c_double
     lib.oracle_e4m3_to_f64.argtypes = [ctypes.c_uint8]
@@ -306,6 +311,54 @@ def gemm_blockscaled(A, B, sa, sb, layout: str, in_dtype: str, out_dtype: str, a
     return (out16, out64) if want_f64 else out16
 
 
+def sparse24_compress(A):
+    """2:4 compression of a dense 16-bit A (M x K, K % 4 == 0): (Ac codes M x K/2, metadata
+    words M x ceil(K/32) uint32, number of groups with more than two non-zeros)."""
+    lib = _load()
+    A = np.ascontiguousarray(_codes(A))
+    M, K = A.shape
+    if K % 4:
+        raise ValueError("K must be a multiple of 4")
+    Ac = np.zeros((M, K // 2), dtype=np.uint16)
+    lde = max(-(-K // 32), 1)
+    E = np.zeros((M, lde), dtype=np.uint32)
+    bad = lib.oracle_sparse24_compress(A.ctypes.data, M, K, max(K, 1), Ac.ctypes.data, max(K // 2, 1), E.ctypes.data,
+                                       lde)
+    return Ac, E[:, :-(-K // 32)] if K else E[:, :0], int(bad)
+
+
+def gemm_sparse24(Ac, E, B, layout: str, dtype: str, alpha: float = 1.0, beta: float = 0.0, Cin=None, rows=None,
+                  want_f64: bool = False, nthreads: int = 0):
+    """alpha * (the sparse contraction of Ac, E with B) + beta * Cin; K = 2 * Ac's columns."""
+    lib = _load()
+    Ac = np.ascontiguousarray(_codes(Ac))
+    B = np.ascontiguousarray(_codes(B))
+    M, Kc = Ac.shape
+    K = 2 * Kc
+    N = B.shape[1] if layout == "NN" else B.shape[0]
+    if (B.shape[0] if layout == "NN" else B.shape[1]) != K:
+        raise ValueError(f"K mismatch: Ac is {Ac.shape} (K = {K}), B is {B.shape} ({layout})")
+    E = np.ascontiguousarray(np.asarray(E, dtype=np.uint32))
+    if E.shape != (M, -(-K // 32)):
+        raise ValueError(f"E must be {M} x {-(-K // 32)}")
+    rows = np.arange(M) if rows is None else np.asarray(rows)
+    rows = np.ascontiguousarray(rows.astype(np.int64))
+    if beta != 0.0:
+        Cin = np.ascontiguousarray(_codes(Cin))
+        cptr, ldcin = Cin.ctypes.data, max(N, 1)
+    else:
+        cptr, ldcin = None, 1
+    out16 = np.zeros((rows.size, N), dtype=np.uint16)
+    out64 = np.zeros((rows.size, N), dtype=np.float64) if want_f64 else None
+    used = lib.oracle_gemm_rows_sparse24(Ac.ctypes.data, E.ctypes.data, B.ctypes.data, cptr, N, K, max(Kc, 1),
+                                         max(E.shape[1], 1), _ld(B), ldcin, LAYOUTS[layout], DTYPES[dtype],
+                                         float(alpha), float(beta), rows.ctypes.data, rows.size, out16.ctypes.data,
+                                         out64.ctypes.data if out64 is not None else None, N, int(nthreads))
+    if used < 0:
+        raise MemoryError("oracle allocation failed")
+    return (out16, out64) if want_f64 else out16
+
+
 def e8m0(e: int) -> float:
     return float(_load().oracle_e8m0_to_f64(int(e)))
 
@@ -315,5 +368,5 @@ def max_threads() -> int:
 
 
 __all__ = ["build", "decode", "encode", "gemm", "gemm_rows", "gemm_elems", "gemm_axpby", "gemm_typed",
-           "gemm_blockscaled", "e8m0", "max_threads",
+           "gemm_blockscaled", "e8m0", "sparse24_compress", "gemm_sparse24", "max_threads",
            "LAYOUTS", "DTYPES"]

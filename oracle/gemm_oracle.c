@@ -494,3 +494,102 @@ int oracle_gemm_rows_blockscaled(const uint16_t* A, const uint16_t* B, const uin
     free(TC);
     return used;
 }
+
+/* ------------------------------------------------------------- 2:4 structured sparsity */
+
+/* "张量缩并：mma 语法", structured sparsity: when at most two of every four consecutive
+ * elements along K of a row of A are non-zero, A is kept as its two chosen values per group
+ * (Ac, M x K/2) plus metadata naming their positions, and the sparse contraction
+ * (mma.row.row.sp with the metadata operand me) multiplies each kept value by the B row it
+ * came from.  Metadata words: E[m * lde + j] holds groups 8j .. 8j+7 of row m, group g in
+ * bits 4(g - 8j) .. 4(g - 8j) + 3: the low two bits are the position (0..3) of the first kept
+ * element, the high two bits that of the second, first < second.
+ *
+ * Compression of a dense A (M x K, K a multiple of 4): per group the first two non-zero
+ * elements are kept (a code is zero when all bits but the sign are 0); when there are fewer,
+ * the lowest positions not yet taken complete the pair, and the pair is put in ascending
+ * order.  Returns the number of groups with more than two non-zeros (their first two are
+ * kept), 0 for a valid 2:4 matrix.  Row padding of Ac / E is not written. */
+int64_t oracle_sparse24_compress(const uint16_t* A, int64_t M, int64_t K, int64_t lda, uint16_t* Ac, int64_t ldac,
+                                 uint32_t* E, int64_t lde)
+{
+    int64_t bad = 0;
+    const int64_t groups = K / 4;
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t j = 0; j * 8 < groups; ++j) E[m * lde + j] = 0u;
+        for (int64_t g = 0; g < groups; ++g) {
+            const uint16_t* a = A + m * lda + 4 * g;
+            int pos[2], n = 0, nonzero = 0;
+            for (int i = 0; i < 4; ++i)
+                if ((a[i] & 0x7fffu) != 0u) {
+                    ++nonzero;
+                    if (n < 2) pos[n++] = i;
+                }
+            if (nonzero > 2) ++bad;
+            for (int i = 0; n < 2 && i < 4; ++i)
+                if (n == 0 || pos[0] != i) pos[n++] = i;
+            if (pos[0] > pos[1]) {
+                const int t = pos[0];
+                pos[0] = pos[1];
+                pos[1] = t;
+            }
+            Ac[m * ldac + 2 * g] = a[pos[0]];
+            Ac[m * ldac + 2 * g + 1] = a[pos[1]];
+            E[m * lde + g / 8] |= (uint32_t)(pos[0] | (pos[1] << 2)) << (4 * (g % 8));
+        }
+    }
+    return bad;
+}
+
+/* The sparse contraction, as the metadata defines it:
+ *     C[m,n] = alpha * sum_g sum_{t<2} Ac[m, 2g+t] * Beff[4g + pos_t(m,g), n] + beta * Cin[m,n]
+ * with pos_t read from E as above (K a multiple of 4, K/4 groups), summed in fp64 and rounded
+ * once.  Same row selection and outputs as oracle_gemm_rows_typed (16-bit operands). */
+int oracle_gemm_rows_sparse24(const uint16_t* Ac, const uint32_t* E, const uint16_t* B, const uint16_t* Cin,
+                              int64_t N, int64_t K, int64_t ldac, int64_t lde, int64_t ldb, int64_t ldcin, int layout,
+                              int dtype, double alpha, double beta, const int64_t* rows, int64_t nrows,
+                              uint16_t* out16, double* out64, int64_t ldo, int nthreads)
+{
+    double* T = (double*)malloc(65536 * sizeof(double));
+    if (!T) return -1;
+    build_table(T, dtype);
+    const int64_t groups = K / 4;
+    int used = 1;
+#ifdef _OPENMP
+    if (nthreads <= 0) nthreads = omp_get_max_threads();
+#pragma omp parallel num_threads(nthreads)
+    {
+#pragma omp single
+        used = omp_get_num_threads();
+#else
+    (void)nthreads;
+    {
+#endif
+        double* acc = (double*)malloc((size_t)(N > 0 ? N : 1) * sizeof(double));
+#ifdef _OPENMP
+#pragma omp for schedule(dynamic, 1)
+#endif
+        for (int64_t i = 0; i < nrows; ++i) {
+            const int64_t m = rows[i];
+            for (int64_t n = 0; n < N; ++n) acc[n] = 0.0;
+            for (int64_t g = 0; g < groups; ++g) {
+                const uint32_t nib = (E[m * lde + g / 8] >> (4 * (g % 8))) & 0xfu;
+                for (int t = 0; t < 2; ++t) {
+                    const int64_t k = 4 * g + ((nib >> (2 * t)) & 3u);
+                    const double a = T[Ac[m * ldac + 2 * g + t]];
+                    for (int64_t n = 0; n < N; ++n)
+                        acc[n] += a * T[layout == OR_LAYOUT_NN ? B[k * ldb + n] : B[n * ldb + k]];
+                }
+            }
+            for (int64_t n = 0; n < N; ++n) {
+                double v = alpha * acc[n];
+                if (beta != 0.0) v += beta * T[Cin[m * ldcin + n]];
+                if (out64) out64[i * ldo + n] = v;
+                if (out16) out16[i * ldo + n] = (dtype == OR_BF16) ? oracle_f64_to_bf16(v) : oracle_f64_to_f16(v);
+            }
+        }
+        free(acc);
+    }
+    free(T);
+    return used;
+}

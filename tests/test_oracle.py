@@ -459,3 +459,78 @@ def test_blockscaled_nan_scale_and_epilogue():
                                      want_f64=True)
     ref = 0.5 * (A.to(torch.float64).numpy() @ B.to(torch.float64).numpy()) - Cin.to(torch.float64).numpy()
     assert np.array_equal(f64, ref)
+
+
+# ------------------------------------------------------------------ 2:4 structured sparsity
+from dense_tiled_gemm_04_gb300.workloads import prune_24  # noqa: E402
+
+
+def _f16_codes(vals):
+    return torch.tensor(vals, dtype=torch.float16).view(torch.int16).numpy().view(np.uint16)
+
+
+def test_sparse24_compress_closed_forms():
+    # Groups: [0,5,0,7] -> (1,3); all zero -> (0,1); [3,0,0,0] -> (0,1); [0,0,0,9] -> (0,3);
+    # [-0,0,6,0] -> (0,2) (negative zero is zero); [1,2,3,4] -> (0,1), counted as a violation;
+    # [0,8,2,0] -> (1,2); [0,0,4,4] -> (2,3).
+    row = [0, 5, 0, 7, 0, 0, 0, 0, 3, 0, 0, 0, 0, 0, 0, 9, -0.0, 0, 6, 0, 1, 2, 3, 4, 0, 8, 2, 0, 0, 0, 4, 4,
+           0, 0, 1, 0]
+    A = _f16_codes([row])
+    Ac, E, bad = oracle.sparse24_compress(A)
+    assert bad == 1
+    assert oracle.decode(Ac, "f16").tolist() == [[5, 7, 0, 0, 3, 0, 0, 9, -0.0, 6, 1, 2, 8, 2, 4, 4, 0, 1]]
+    pairs = [(1, 3), (0, 1), (0, 1), (0, 3), (0, 2), (0, 1), (1, 2), (2, 3), (0, 2)]
+    nibbles = [a | (b << 2) for a, b in pairs]
+    words = [sum(n << (4 * i) for i, n in enumerate(nibbles[:8])), nibbles[8]]
+    assert E.tolist() == [words]
+    assert E.dtype == np.uint32 and words[0] == 0xE948C44D  # nibbles D,4,4,C,8,4,9,E from the low end
+
+
+@pytest.mark.parametrize("dtype", ["f16", "bf16"])
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_sparse24_contraction_equals_dense_product(layout, dtype):
+    # The sparse form (kept values times the B rows the metadata names) against the plain
+    # dense product of the 2:4 matrix: integer data is exact in fp64 whatever the order.
+    M, N, K = 33, 47, 100  # 25 groups: the last metadata word holds one group
+    A, B = make_inputs(M, N, K, layout, dtype, "int", seed=91)
+    A = prune_24(A, seed=92)
+    Ac, E, bad = oracle.sparse24_compress(A)
+    assert bad == 0 and Ac.shape == (M, K // 2) and E.shape == (M, 4)
+    codes, f64 = oracle.gemm_sparse24(Ac, E, B, layout, dtype, want_f64=True)
+    dense = oracle.gemm_rows(A, B, layout, dtype, np.arange(M), want_f64=True)
+    assert np.array_equal(codes, dense[0])
+    assert np.array_equal(f64, dense[1])
+    a, b = A.to(torch.float64).numpy(), B.to(torch.float64).numpy()
+    assert np.array_equal(f64, a @ (b if layout == "NN" else b.T))
+
+
+def test_sparse24_normal_values_and_epilogue():
+    M, N, K = 40, 24, 64
+    A, B = make_inputs(M, N, K, "TN", "bf16", "normal", seed=93)
+    A = prune_24(A, seed=94)
+    Ac, E, _ = oracle.sparse24_compress(A)
+    Cin, _ = make_inputs(M, N, N, "NN", "bf16", "int", seed=95)
+    _, f64 = oracle.gemm_sparse24(Ac, E, B, "TN", "bf16", alpha=0.5, beta=-2.0, Cin=Cin, want_f64=True)
+    ref = 0.5 * (A.to(torch.float64).numpy() @ B.to(torch.float64).numpy().T) - 2.0 * Cin.to(torch.float64).numpy()
+    np.testing.assert_allclose(f64, ref, rtol=1e-13, atol=1e-13)
+
+
+def test_sparse24_metadata_selects_the_b_row():
+    # One kept 1.0 at K position 4g + i of row m: row m of C is row 4g + i of B (NN).
+    M, N, K = 4, 16, 64
+    _, B = make_inputs(M, N, K, "NN", "f16", "int", seed=96)
+    for m, k in [(0, 0), (1, 5), (2, 42), (3, 63)]:
+        A = torch.zeros((M, K), dtype=torch.float16)
+        A[m, k] = 1.0
+        Ac, E, bad = oracle.sparse24_compress(A)
+        assert bad == 0
+        got = oracle.gemm_sparse24(Ac, E, B, "NN", "f16")
+        assert np.array_equal(got[m], B[k].view(torch.int16).numpy().view(np.uint16))
+
+
+def test_sparse24_violation_keeps_the_first_two():
+    A = _f16_codes([[1, 2, 3, 0, 0, 0, 0, 0]])
+    B = _f16_codes([[1], [10], [100], [1000], [0], [0], [0], [0]])
+    Ac, E, bad = oracle.sparse24_compress(A)
+    assert bad == 1
+    assert oracle.decode(oracle.gemm_sparse24(Ac, E, B, "NN", "f16"), "f16").tolist() == [[21.0]]
