@@ -19,7 +19,7 @@ LIB = os.path.join(HERE, "libdtgemm.so")
 # One translation unit for the host side, one per operand type for the kernels: they
 # compile in parallel and link into one library.
 SOURCES = [os.path.join(CSRC, f) for f in ("gemm_api.cu", "kernels_f16.cu", "kernels_bf16.cu", "kernels_e4m3.cu",
-                                           "kernels_e5m2.cu", "kernels_mx.cu")]
+                                           "kernels_e5m2.cu", "kernels_mx.cu", "kernels_sparse.cu")]
 DEPENDS = SOURCES + [os.path.join(CSRC, f) for f in ("gemm_kernel.cuh", "sm103_ptx.cuh", "kernel_set.cuh")] + [
     os.path.join(INCLUDE, "gemm.h")]
 OBJ_DIR = os.path.join(HERE, "_build")

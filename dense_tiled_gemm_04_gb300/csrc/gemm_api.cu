@@ -24,7 +24,7 @@ using dtg::KernelParams;
 constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
-constexpr int kNumSlots = 60;  // 3 configurations x 10 operand/output types x 2 layouts
+constexpr int kNumSlots = 72;  // 3 configurations x 12 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -65,6 +65,7 @@ struct Epilogue {
     gemm_dtype_t out = -1;
     const void* sfa = nullptr;  // block scales (8-bit operands): both set, or both null
     const void* sfb = nullptr;
+    const void* meta = nullptr;  // 2:4 sparsity metadata: A is the compressed (M x K/2) matrix
 };
 
 struct TmapEntry {
@@ -180,12 +181,16 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool is_f8(gemm_dtype_t t) { return t == GEMM_DTYPE_E4M3 || t == GEMM_DTYPE_E5M2; }
 int elem_bytes(gemm_dtype_t t) { return is_f8(t) ? 1 : 2; }
 
+// Kernel families beyond the dense one: block-scaled 8-bit operands, 2:4-sparse A.  Both run
+// one configuration (128 x 256, one CTA).
+enum Family { kDense = 0, kBlockScaled = 1, kSparse24 = 2 };
+
 // `out` is the type of C: equal to `in` for 16-bit operands, F16 or BF16 for 8-bit ones.
-// `mx`: 8-bit operands with block scales (one configuration, 128 x 256).
-KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, bool mx = false)
+KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
     const bool nn = layout == GEMM_LAYOUT_NN, out_bf16 = out == GEMM_DTYPE_BF16;
-    if (mx) return dtg::choice_mx(in == GEMM_DTYPE_E5M2, out_bf16, nn);
+    if (family == kBlockScaled) return dtg::choice_mx(in == GEMM_DTYPE_E5M2, out_bf16, nn);
+    if (family == kSparse24) return dtg::choice_sparse(in == GEMM_DTYPE_BF16, nn);
     switch (in) {
     case GEMM_DTYPE_BF16: return dtg::choice_bf16(config, nn);
     case GEMM_DTYPE_E4M3: return dtg::choice_e4m3(config, out_bf16, nn);
@@ -194,12 +199,12 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
     }
 }
 
-int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, bool mx = false)
+int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
     const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
     const int f8 = 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0);  // 0..3
-    const int types = is_f8(in) ? (mx ? 6 : 2) + f8 : in;
-    return (c * 10 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
+    const int types = family == kSparse24 ? 10 + in : (is_f8(in) ? (family == kBlockScaled ? 6 : 2) + f8 : in);
+    return (c * 12 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
 }
 
 // Opt the kernel into its shared memory and, for pair kernels, ask how many clusters can
@@ -301,9 +306,10 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
 // c_col_major: C is stored N x M (C[m, n] at C + n * ldc + m), so ldc must cover M.
 // out_dtype < 0: gemm_run's rule, 16-bit operands and C of the same type.  Otherwise any
 // operand type, C of type out_dtype (16-bit), equal to dtype for 16-bit operands.
+// sparse_a: A is the compressed 2:4 matrix, K / 2 columns (K a multiple of 4).
 gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,
                             int64_t lda, int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype,
-                            bool c_col_major = false, gemm_dtype_t out_dtype = -1)
+                            bool c_col_major = false, gemm_dtype_t out_dtype = -1, bool sparse_a = false)
 {
     if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
     if (out_dtype < 0) {
@@ -318,11 +324,12 @@ gemm_status_t validate_args(const void* A, const void* B, const void* C, int64_t
     if (!C || ldc < (c_col_major ? M : N)) return GEMM_ERR_INVALID_ARG;
     if (K > 0) {
         if (!A || !B) return GEMM_ERR_INVALID_ARG;
-        if (lda < K) return GEMM_ERR_INVALID_ARG;
+        if (lda < (sparse_a ? K / 2 : K)) return GEMM_ERR_INVALID_ARG;
         if (ldb < (layout == GEMM_LAYOUT_NN ? N : K)) return GEMM_ERR_INVALID_ARG;
     }
     const int64_t lim = (int64_t(1) << 31) - 1;
     if (M > lim || N > lim || K > lim) return GEMM_ERR_UNSUPPORTED;
+    if (sparse_a && K % 4 != 0) return GEMM_ERR_UNSUPPORTED;
     if ((reinterpret_cast<uintptr_t>(C) & 15u) != 0 || (ldc & 7) != 0) return GEMM_ERR_UNSUPPORTED;
     if (K > 0) {
         if ((reinterpret_cast<uintptr_t>(A) & 15u) != 0 || (reinterpret_cast<uintptr_t>(B) & 15u) != 0)
@@ -363,10 +370,10 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
         return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
     }
 
-    const bool mx = ep.sfa != nullptr;
-    const int config = mx ? GEMM_CONFIG_128x256 : pick_config(o, dev, M, N);
-    const KernelChoice kc = kernel_choice(config, dtype, out, layout, mx);
-    const int slot = slot_of(config, dtype, out, layout, mx);
+    const int family = ep.sfa ? kBlockScaled : (ep.meta ? kSparse24 : kDense);
+    const int config = family != kDense ? GEMM_CONFIG_128x256 : pick_config(o, dev, M, N);
+    const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
+    const int slot = slot_of(config, dtype, out, layout, family);
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
     if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
@@ -376,7 +383,12 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     const bool nn = layout == GEMM_LAYOUT_NN;
     const uint64_t eb = static_cast<uint64_t>(elem_bytes(dtype));
     const uint32_t sk = static_cast<uint32_t>(kc.stage_k);
-    if (!get_tmap(cache, A, K, M, lda * eb, sk, dtg::kBM, dtype, &tA)) return GEMM_ERR_CUDA;
+    // A: K elements per row, or K / 2 for the compressed 2:4 matrix (64-byte stage rows,
+    // 64-byte swizzle).
+    const bool a_sw64 = static_cast<uint64_t>(kc.a_stage_k) * eb == 64;
+    if (!get_tmap(cache, A, family == kSparse24 ? K / 2 : K, M, lda * eb, static_cast<uint32_t>(kc.a_stage_k), dtg::kBM,
+                  dtype, &tA, a_sw64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+        return GEMM_ERR_CUDA;
     if (nn) {
         if (!get_tmap(cache, B, N, K, ldb * eb, static_cast<uint32_t>(kc.n_block), sk, dtype, &tB))
             return GEMM_ERR_CUDA;
@@ -417,6 +429,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.sfa = static_cast<const uint8_t*>(ep.sfa);
     kp.sfb = static_cast<const uint8_t*>(ep.sfb);
     kp.sfb_blocks = static_cast<int32_t>(cdiv(N, dtg::kSfChunkRows));
+    kp.meta = static_cast<const uint8_t*>(ep.meta);
 
     void* args[] = {&tA, &tB, &tC, &kp};
     cudaLaunchConfig_t cfg;
@@ -486,6 +499,83 @@ __global__ void pack_scales_kernel(const uint8_t* src, int64_t rows, int64_t kbl
         const int64_t r = rb * dtg::kSfChunkRows + ((within >> 2) & 3) * 32 + (within >> 4);
         const int64_t j = g * 4 + (within & 3);
         dst[o] = (r < rows && j < kblocks) ? src[r * ld + j] : static_cast<uint8_t>(127);
+    }
+}
+
+// Metadata word of row r for groups [8 j, 8 j + 8) (K [32 j, 32 j + 32)) and the kept values:
+// per group of four the first two non-zero codes (a code is zero when all bits but the sign
+// are 0) are kept, the lowest free positions complete the pair, the pair is put in ascending
+// order; Ac gets the two values.  Groups past K and rows past M get the pattern (0, 1) and no
+// values.  Returns the number of groups with more than two non-zeros.
+__device__ int32_t sparse24_word(const uint16_t* A, int64_t M, int64_t K, int64_t lda, uint16_t* Ac, int64_t ldac,
+                                 int64_t r, int64_t j, uint32_t* word)
+{
+    const int64_t groups = K / 4;
+    uint32_t w = 0;
+    int32_t nbad = 0;
+    for (int q = 0; q < 8; ++q) {
+        const int64_t g = 8 * j + q;
+        uint32_t nib = 0x4u;  // positions (0, 1)
+        if (r < M && g < groups) {
+            const uint16_t* a = A + r * lda + 4 * g;
+            int p0 = -1, p1 = -1, nonzero = 0;
+            for (int i = 0; i < 4; ++i)
+                if ((a[i] & 0x7fffu) != 0u) {
+                    ++nonzero;
+                    if (p0 < 0)
+                        p0 = i;
+                    else if (p1 < 0)
+                        p1 = i;
+                }
+            if (nonzero > 2) ++nbad;
+            for (int i = 0; p1 < 0 && i < 4; ++i)
+                if (p0 < 0)
+                    p0 = i;
+                else if (i != p0)
+                    p1 = i;
+            if (p0 > p1) {
+                const int tmp = p0;
+                p0 = p1;
+                p1 = tmp;
+            }
+            Ac[r * ldac + 2 * g] = a[p0];
+            Ac[r * ldac + 2 * g + 1] = a[p1];
+            nib = static_cast<uint32_t>(p0 | (p1 << 2));
+        }
+        w |= nib << (4 * q);
+    }
+    *word = w;
+    return nbad;
+}
+
+// 2:4 compression of a dense 16-bit A (M x K, K % 4 == 0) into Ac and the metadata chunks
+// (dtg::kMetaChunkBytes).  One thread per (row pair, ring stage of 64 K): rows r = 16 b + i
+// and r + 8 (i < 8) share TMEM words, as the sparse MMA reads them: in the half of MMA h,
+// lane r holds groups 0-3 of the MMA's 32 K for row r (low 16 bits) and for row r + 8 (high
+// 16 bits), lane r + 8 holds groups 4-7 of both rows the same way; three padding words
+// follow each word.  Groups with more than two non-zeros are counted into *bad (if not null).
+__global__ void sparse24_compress_kernel(const uint16_t* A, int64_t M, int64_t K, int64_t lda, uint16_t* Ac,
+                                         int64_t ldac, uint8_t* meta, int32_t* bad, int64_t rows_pad, int64_t stages)
+{
+    const int64_t pairs = rows_pad / 2;
+    const int64_t total = pairs * stages;
+    for (int64_t t = blockIdx.x * static_cast<int64_t>(blockDim.x) + threadIdx.x; t < total;
+         t += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t pi = t % pairs, s = t / pairs;
+        const int64_t r = 16 * (pi / 8) + pi % 8, r2 = r + 8;
+        int32_t nbad = 0;
+        uint8_t* chunk = meta + ((r / dtg::kBM) * stages + s) * dtg::kMetaChunkBytes;
+        for (int h = 0; h < 2; ++h) {
+            uint32_t w1, w2;
+            nbad += sparse24_word(A, M, K, lda, Ac, ldac, r, 2 * s + h, &w1);
+            nbad += sparse24_word(A, M, K, lda, Ac, ldac, r2, 2 * s + h, &w2);
+            uint8_t* half = chunk + h * dtg::kMetaHalfBytes;
+            *reinterpret_cast<uint4*>(half + (r % dtg::kBM) * 16) =
+                make_uint4((w1 & 0xFFFFu) | (w2 << 16), 0x44444444u, 0x44444444u, 0x44444444u);
+            *reinterpret_cast<uint4*>(half + (r2 % dtg::kBM) * 16) =
+                make_uint4((w1 >> 16) | (w2 & 0xFFFF0000u), 0x44444444u, 0x44444444u, 0x44444444u);
+        }
+        if (nbad && bad) atomicAdd(bad, nbad);
     }
 }
 
@@ -621,6 +711,63 @@ gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* 
             return GEMM_ERR_UNSUPPORTED;
         ep.sfa = sfa;
         ep.sfb = sfb;
+    }
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    return launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb,
+                       a.ldc, a.layout, a.dtype, static_cast<cudaStream_t>(stream), ep);
+}
+
+int64_t gemm_sp_meta_bytes(int64_t M, int64_t K)
+{
+    if (M <= 0 || K <= 0) return 0;
+    return cdiv(M, dtg::kBM) * cdiv(K, 64) * dtg::kMetaChunkBytes;
+}
+
+gemm_status_t gemm_sp_compress(gemm_handle_t h, const void* A, int64_t M, int64_t K, int64_t lda, gemm_dtype_t dtype,
+                               void* Ac, int64_t ldac, void* meta, int32_t* bad_groups, void* stream)
+{
+    if (!h || M < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (M == 0 || K == 0) return GEMM_OK;
+    if (K % 4 != 0) return GEMM_ERR_UNSUPPORTED;
+    if (!A || !Ac || !meta || lda < K || ldac < K / 2) return GEMM_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(meta) & 15u) != 0) return GEMM_ERR_UNSUPPORTED;
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    const int64_t rows_pad = cdiv(M, dtg::kBM) * dtg::kBM, stages = cdiv(K, 64);
+    int blocks = static_cast<int>(cdiv(rows_pad / 2 * stages, 256));
+    const int cap = h->dev.num_sms * 8;
+    if (blocks > cap) blocks = cap;
+    sparse24_compress_kernel<<<blocks, 256, 0, static_cast<cudaStream_t>(stream)>>>(
+        static_cast<const uint16_t*>(A), M, K, lda, static_cast<uint16_t*>(Ac), ldac, static_cast<uint8_t*>(meta),
+        bad_groups, rows_pad, stages);
+    return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+}
+
+gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream)
+{
+    if (!h || !args) return GEMM_ERR_INVALID_ARG;
+    const gemm_args_t& a = *args;
+    if (a.dtype != GEMM_DTYPE_F16 && a.dtype != GEMM_DTYPE_BF16) return GEMM_ERR_INVALID_ARG;
+    if (a.c_col_major != 0 && a.c_col_major != 1) return GEMM_ERR_INVALID_ARG;
+    if (a.out_dtype != a.dtype) return GEMM_ERR_INVALID_ARG;
+    const float alpha = a.alpha * a.scale_a * a.scale_b;
+    if (!std::isfinite(a.alpha) || !std::isfinite(a.beta) || !std::isfinite(a.scale_a) ||
+        !std::isfinite(a.scale_b) || !std::isfinite(alpha))
+        return GEMM_ERR_INVALID_ARG;
+    const gemm_status_t v = validate_args(a.A, a.B, a.C, a.M, a.N, a.K, a.lda, a.ldb, a.ldc, a.layout, a.dtype,
+                                          a.c_col_major != 0, a.out_dtype, true);
+    if (v != GEMM_OK || a.M == 0 || a.N == 0) return v;
+    Epilogue ep;
+    ep.alpha = alpha;
+    ep.beta = a.beta;
+    ep.col_major = a.c_col_major;
+    ep.out = a.out_dtype;
+    if (a.K > 0) {
+        if (!meta) return GEMM_ERR_INVALID_ARG;
+        if ((reinterpret_cast<uintptr_t>(meta) & 15u) != 0) return GEMM_ERR_UNSUPPORTED;
+        ep.meta = meta;
     }
     DeviceGuard g(h->device);
     if (!g.ok) return GEMM_ERR_CUDA;

@@ -74,19 +74,23 @@ constexpr int kEpiBarrier = 1;                      // named barrier of the 4 ep
 
 // Operand element types: 0 fp16, 1 bf16 (tcgen05 kind::f16), 2 E4M3, 3 E5M2 (kind::f8f6f4),
 // 4 E4M3 and 5 E5M2 with one E8M0 scale per 32 K elements of each row of A and column of B
-// (kind::mxf8f6f4, block-scaled).  A ring stage always holds 128-byte rows of K (one 128-byte
-// swizzle row), so the number of K elements per stage and per MMA (32 bytes) depends on the
-// element size; the shared-memory layout, the descriptors' byte offsets and the stage sizes
-// do not.
+// (kind::mxf8f6f4, block-scaled), 6 fp16 and 7 bf16 with A 2:4-sparse (kind::f16 .sp).
+// A ring stage holds one 128-byte swizzle row of K per row of B, so the number of K elements
+// per stage and per MMA (32 bytes of B) depends on the element size; the shared-memory layout,
+// the descriptors' byte offsets and the stage sizes do not.  A sparse A keeps half of K: its
+// stage rows are 64 bytes (64-byte swizzle), and one sparse MMA covers 32 K (64 bytes of B).
 template <int IN>
 struct Operand {
-    static constexpr int kBytes = IN >= 2 ? 1 : 2;
-    static constexpr int kStageK = 128 / kBytes;    // K elements per ring stage
-    static constexpr int kMmaK = 32 / kBytes;       // K elements per tcgen05.mma
-    static constexpr int kNBlock = 128 / kBytes;    // N elements per 128-byte row of an N-major B box
-    static constexpr bool kF8 = IN >= 2;
-    static constexpr bool kMX = IN >= 4;            // block-scaled
-    static constexpr uint32_t kFormat = IN >= 2 ? (IN - 2) & 1 : IN;  // instruction-descriptor A/B format
+    static constexpr bool kSparse = IN >= 6;
+    static constexpr bool kF8 = IN >= 2 && IN < 6;
+    static constexpr bool kMX = IN == 4 || IN == 5;  // block-scaled
+    static constexpr int kBytes = kF8 ? 1 : 2;
+    static constexpr int kStageK = 128 / kBytes;     // K elements per ring stage
+    static constexpr int kMmaK = (kSparse ? 64 : 32) / kBytes;  // K elements per tcgen05.mma
+    static constexpr int kNBlock = 128 / kBytes;     // N elements per 128-byte row of an N-major B box
+    static constexpr int kAStageK = kSparse ? kStageK / 2 : kStageK;  // stored A elements per stage row
+    static constexpr int kARowBytes = kAStageK * kBytes;
+    static constexpr uint32_t kFormat = kSparse ? IN - 6 : (kF8 ? (IN - 2) & 1 : IN);  // A/B format
 };
 
 // Block scales travel in 512-byte chunks: the E8M0 exponents of 128 rows (of A, or columns
@@ -97,7 +101,21 @@ struct Operand {
 // a matrix with G = ceil(K / 128) K groups starts at byte (rb * G + g) * 512.
 constexpr int kSfChunkBytes = 512;
 constexpr int kSfChunkRows = 128;
-constexpr int kSfTmemCol = 256;  // first TMEM column of the block scales (after one 256-column accumulator)
+constexpr int kSfTmemCol = 256;  // first TMEM column of the per-stage side data (after one 256-column accumulator)
+
+// 2:4 sparsity metadata travels in 4096-byte chunks: 128 rows of A by one ring stage (64 K).
+// The chunk holds one 2048-byte half per MMA of the stage (K [0, 32) and [32, 64) of the
+// stage); in a half, TMEM lane l's 16 bytes (at l * 16) are its 32-bit metadata word followed
+// by three padding words.  A group of four K elements takes 4 bits: the positions of its two
+// kept elements (low two bits, then high two).  The MMA reads rows in pairs: for rows
+// r = 16 b + i and r + 8 (i < 8), lane r holds groups 0-3 of the MMA's 32 K of row r (bits
+// 0-15) and of row r + 8 (bits 16-31); lane r + 8 holds groups 4-7 of the two rows the same
+// way (found by probing the instruction with single kept elements).  Chunk (row block rb,
+// stage s) of a matrix with S = ceil(K / 64) stages starts at byte (rb * S + s) * 4096.  Each
+// half goes to its own 8-column-aligned block of TMEM columns.
+constexpr int kMetaChunkBytes = 4096;
+constexpr int kMetaHalfBytes = 2048;
+constexpr int kMetaTmemStride = 8;  // TMEM columns between the metadata of consecutive MMAs
 
 // Error-word roles.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3;
@@ -125,6 +143,8 @@ struct KernelParams {
     int32_t sfb_blocks;          // ceil(N / 128)
     const uint8_t* sfa;          // ceil(M / 128) x num_kb chunks
     const uint8_t* sfb;          // sfb_blocks x num_kb chunks
+    // 2:4 sparsity metadata (sparse kernels only): ceil(M / 128) x num_kb chunks of kMetaChunkBytes
+    const uint8_t* meta;
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -190,11 +210,11 @@ struct WorkIter {
     }
 };
 
-// SF_BYTES: block-scale bytes per ring stage (0 without block scales); STG_BUFS: staging
-// buffers per epilogue warp.
-template <int B_ROWS, int STAGES, int SF_BYTES = 0, int STG_BUFS = 2>
+// SF_BYTES: side-data bytes per ring stage (block scales or sparsity metadata; 0 without);
+// STG_BUFS: staging buffers per epilogue warp; A_ROW_BYTES: bytes of an A row per stage.
+template <int B_ROWS, int STAGES, int SF_BYTES = 0, int STG_BUFS = 2, int A_ROW_BYTES = kRowBytes>
 struct Smem {
-    static constexpr int kABytes = kBM * kRowBytes;
+    static constexpr int kABytes = kBM * A_ROW_BYTES;
     static constexpr int kBBytes = B_ROWS * kRowBytes;
     static constexpr int kStageBytes = kABytes + kBBytes;
     static constexpr int kRing = STAGES * kStageBytes;
@@ -208,19 +228,23 @@ struct Smem {
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kTotal = kMiscOff + 16;     // tmem slot, abort flag, stream-K "last" flag
     static constexpr int kAlloc = kTotal + 1024;     // slack for aligning the base to 1 KB
-    static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0, "swizzle atoms need 1 KB alignment");
+    static_assert(kABytes % 1024 == 0 && kBBytes % 1024 == 0 && kStageBytes % 1024 == 0,
+                  "swizzle atoms need 1 KB alignment");
     static_assert(kStgOff % 1024 == 0, "the swizzled staging buffers need 1 KB alignment");
 };
 
 // Shared-memory layout of a kernel instantiation (host and device agree through this).
 // Block-scaled kernels add the scale chunks of each stage (one for A, one per 128 B rows)
-// and, to stay within 227 KB, keep one staging buffer per epilogue warp.
+// and, to stay within 227 KB, keep one staging buffer per epilogue warp; sparse kernels add
+// the stage's metadata chunk and store A rows of 64 bytes.
 template <int BN, int STAGES, int IN, bool PAIR>
 struct KernelLayout {
     static constexpr int kBRows = BN / (PAIR ? 2 : 1);
     static constexpr bool kMX = Operand<IN>::kMX;
-    static constexpr int kSfBytes = kMX ? kSfChunkBytes * (1 + kBRows / kSfChunkRows) : 0;
-    using S = Smem<kBRows, STAGES, kSfBytes, kMX ? 1 : 2>;
+    static constexpr bool kSparse = Operand<IN>::kSparse;
+    static constexpr int kSfBytes =
+        kMX ? kSfChunkBytes * (1 + kBRows / kSfChunkRows) : (kSparse ? kMetaChunkBytes : 0);
+    using S = Smem<kBRows, STAGES, kSfBytes, kMX ? 1 : 2, Operand<IN>::kARowBytes>;
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
@@ -245,6 +269,18 @@ __device__ __forceinline__ uint64_t smem_desc_plain(uint32_t addr, uint32_t lbo,
     d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
     d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
     d |= 1ull << 46;  // layout bits 61-63 = 0: no swizzle
+    return d;
+}
+
+// tcgen05 shared-memory matrix descriptor for a 64-byte-swizzled K-major operand tile (rows of
+// 64 bytes, 8-row atoms of 512 bytes `sbo` apart).
+__device__ __forceinline__ uint64_t smem_desc_sw64(uint32_t addr, uint32_t lbo, uint32_t sbo)
+{
+    uint64_t d = static_cast<uint64_t>((addr & 0x3FFFFu) >> 4);
+    d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+    d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+    d |= 1ull << 46;
+    d |= 4ull << 61;  // layout: 64-byte swizzle
     return d;
 }
 
@@ -529,16 +565,19 @@ __global__ void __launch_bounds__(kThreads, 1)
     constexpr int kRanks = PAIR ? 2 : 1;
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
-    // Block-scaled kernels keep one accumulator and put the scales of every ring stage in
-    // the TMEM columns after it; the others double-buffer the accumulator.
-    constexpr int kAccBufs = T::kMX ? 1 : 2;
-    constexpr uint32_t kTmemCols = T::kMX ? 512 : 2 * BN;
+    // Block-scaled and sparse kernels keep one accumulator and put the side data of every
+    // ring stage (scales, metadata) in the TMEM columns after it; the others double-buffer
+    // the accumulator.
+    constexpr bool kSide = T::kMX || T::kSparse;
+    constexpr int kAccBufs = kSide ? 1 : 2;
+    constexpr uint32_t kTmemCols = kSide ? 512 : 2 * BN;
     static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
     using L = typename KernelLayout<BN, STAGES, IN, PAIR>::S;
-    constexpr int kSfChunks = L::kSfBytes / kSfChunkBytes;  // per stage: A, then B
-    static_assert(!T::kMX || (!PAIR && BN <= kSfTmemCol &&
-                              kSfTmemCol + STAGES * kSfChunks * 4 <= static_cast<int>(kTmemCols)),
-                  "block-scaled kernels: one CTA, the accumulator and the scales fit in TMEM");
+    constexpr int kSfChunks = T::kMX ? L::kSfBytes / kSfChunkBytes : 0;  // per stage: A, then B
+    constexpr int kSideCols = T::kMX ? kSfChunks * 4 : (T::kSparse ? 2 * kMetaTmemStride : 0);  // TMEM cols / stage
+    static_assert(!kSide || (!PAIR && BN <= kSfTmemCol &&
+                             kSfTmemCol + STAGES * kSideCols <= static_cast<int>(kTmemCols)),
+                  "block-scaled / sparse kernels: one CTA, the accumulator and the side data fit in TMEM");
 
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1 KB (128-byte swizzle atoms repeat every 8 rows).
@@ -634,7 +673,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if (sf_b_chunks > kSfChunks - 1) sf_b_chunks = kSfChunks - 1;
                         }
                         if (leader) {
-                            const int sf_bytes = T::kMX ? (1 + sf_b_chunks) * kSfChunkBytes : 0;
+                            const int sf_bytes =
+                                T::kMX ? (1 + sf_b_chunks) * kSfChunkBytes : (T::kSparse ? kMetaChunkBytes : 0);
                             ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes + sf_bytes);
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -645,7 +685,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             else
                                 ptx::tma_load_2d(dst, tm_, x, y, fb);
                         };
-                        load(sa, &tmA, k0, y_a);
+                        load(sa, &tmA, kb * T::kAStageK, y_a);
                         if constexpr (NN) {
                             // B stored K x N: boxes of one 128-byte row of N (kNBlock elements)
                             // by kStageK rows of K, kStageK * 128 bytes each.
@@ -656,6 +696,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
                         }
+                        if constexpr (T::kSparse)
+                            ptx::bulk_load_1d(base + L::kSfOff + stage * L::kSfBytes,
+                                              p.meta + (tm * p.num_kb + kb) * kMetaChunkBytes, kMetaChunkBytes, fb);
                         if constexpr (T::kMX) {
                             const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
                             const int64_t g = kb;
@@ -693,8 +736,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else if (warp == kMmaWarp) {
         if (lane == 0 && leader) {
             // ---------------------------------------------------------------- MMA issuer
-            constexpr uint32_t idesc =
-                T::kMX ? idesc_mx<T::kFormat, NN, kTileM, BN>() : idesc_mma<T::kFormat, NN, kTileM, BN>();
+            // Sparse MMAs: the dense descriptor with the sparsity flag (bit 2).
+            constexpr uint32_t idesc = T::kMX ? idesc_mx<T::kFormat, NN, kTileM, BN>()
+                                              : (idesc_mma<T::kFormat, NN, kTileM, BN>() | (T::kSparse ? 4u : 0u));
             int stage = 0;
             uint32_t phase = 0;
             int acc = 0;
@@ -723,17 +767,36 @@ __global__ void __launch_bounds__(kThreads, 1)
                     // below, which read them; the stage's commit covers both.
                     uint32_t sf_tmem = 0;
                     if constexpr (T::kMX) {
-                        sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSfChunks * 4);
+                        sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
                         const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
 #pragma unroll
                         for (int c = 0; c < kSfChunks; ++c)
                             ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, smem_desc_plain(sf + c * kSfChunkBytes, 0, 128));
                     }
+                    // Sparsity metadata of this stage: per MMA k, 128 rows x 16 bytes -> TMEM lanes
+                    // 0-127, columns sf_tmem + 8k .. + 3 (8-column aligned).  The addresses are
+                    // checked against that alignment; a violation is reported, not issued.
+                    if constexpr (T::kSparse) {
+                        const uint32_t col = static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
+                        const uint32_t meta_smem = base + L::kSfOff + stage * L::kSfBytes;
+                        if ((col % kMetaTmemStride) != 0 || (meta_smem & 127u) != 0) {
+                            wd.fail(kRoleMma, tile, kb);
+                            aborted = true;
+                            break;
+                        }
+                        sf_tmem = tmem_base + col;
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+                            ptx::tmem_cp_128x128b(sf_tmem + h * kMetaTmemStride,
+                                                  smem_desc_plain(meta_smem + h * kMetaHalfBytes, 0, 128));
+                    }
 #pragma unroll
                     for (int k = 0; k < T::kStageK / T::kMmaK; ++k) {
-                        // A (K-major, 128B swizzle): the k-th K slice starts 32 B further along
-                        // each 128-byte row; 8-row groups are 1 KB apart (SBO).
-                        const uint64_t adesc = smem_desc_sw128(sa + k * 32, 16, 1024);
+                        // A (K-major): the k-th K slice starts 32 B further along each row;
+                        // 128-byte-swizzled rows, 8-row groups 1 KB apart (SBO) -- or, for a
+                        // sparse A, 64-byte-swizzled rows with 512-byte groups.
+                        const uint64_t adesc =
+                            T::kSparse ? smem_desc_sw64(sa + k * 32, 16, 512) : smem_desc_sw128(sa + k * 32, 16, 1024);
                         uint64_t bdesc;
                         if constexpr (NN) {
                             // B (N-major): rows are K; the k-th slice starts kMmaK rows of 128 B
@@ -741,7 +804,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // groups 1 KB apart (SBO).
                             bdesc = smem_desc_sw128(sb + k * (T::kMmaK * 128), T::kStageK * 128, 1024);
                         } else {
-                            bdesc = smem_desc_sw128(sb + k * 32, 16, 1024);
+                            // B (K-major): the k-th slice starts kMmaK elements along each row.
+                            bdesc = smem_desc_sw128(sb + k * (T::kMmaK * T::kBytes), 16, 1024);
                         }
                         const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
                         if constexpr (PAIR) {
@@ -753,6 +817,9 @@ __global__ void __launch_bounds__(kThreads, 1)
                             if constexpr (T::kMX)
                                 ptx::mma_mxf8_cta1(d_tmem, adesc, bdesc, idesc | mx_scale_ids(k), sf_tmem, sf_tmem + 4,
                                                    accumulate);
+                            else if constexpr (T::kSparse)
+                                ptx::mma_sp_f16_cta1(d_tmem, adesc, bdesc, sf_tmem + k * kMetaTmemStride, idesc,
+                                                     accumulate);
                             else if constexpr (T::kF8)
                                 ptx::mma_f8_cta1(d_tmem, adesc, bdesc, idesc, accumulate);
                             else

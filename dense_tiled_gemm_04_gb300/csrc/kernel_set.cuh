@@ -1,7 +1,8 @@
 // The set of kernel instantiations the host can launch, and how it names them.
 //
 // Each operand type's instantiations live in a translation unit of their own
-// (kernels_f16.cu, kernels_bf16.cu, kernels_e4m3.cu, kernels_e5m2.cu, kernels_mx.cu) so that nvcc
+// (kernels_f16.cu, kernels_bf16.cu, kernels_e4m3.cu, kernels_e5m2.cu, kernels_mx.cu,
+// kernels_sparse.cu) so that nvcc
 // compiles them in parallel; the host reaches them through the choice_* functions below,
 // which return the kernel's address and launch shape.
 #pragma once
@@ -17,8 +18,9 @@ struct KernelChoice {
     int config;
     int bm, bn;     // output tile of one CTA (1-CTA) or of the pair
     int b_box;      // rows (TN) / columns (NN) of B one CTA loads per stage
-    int stage_k;    // K elements per ring stage (one 128-byte row of each operand)
+    int stage_k;    // K elements per ring stage (one 128-byte row of B)
     int n_block;    // NN: N elements per B box (128 bytes)
+    int a_stage_k;  // stored A elements per stage row (stage_k, or half of it for a 2:4-sparse A)
     int stages;
     int cluster;    // CTAs per cluster
     const void* fn;
@@ -28,7 +30,7 @@ struct KernelChoice {
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN>
 KernelChoice one_cta_choice(int config)
 {
-    return {config, kBM, BN, BN, Operand<IN>::kStageK, Operand<IN>::kNBlock, STAGES, 1,
+    return {config, kBM, BN, BN, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK, STAGES, 1,
             reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, STAGES, IN, OUT_BF16, NN, false>),
             KernelLayout<BN, STAGES, IN, false>::S::kAlloc};
 }
@@ -37,7 +39,8 @@ template <int IN, bool OUT_BF16, bool NN>
 KernelChoice choice_for(int config)
 {
     if (config == 3)  // GEMM_CONFIG_256x256
-        return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, kPairStages, 2,
+        return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
+                kPairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kPairStages, IN, OUT_BF16, NN, true>),
                 KernelLayout<256, kPairStages, IN, true>::S::kAlloc};
     if (config == 2)  // GEMM_CONFIG_128x128
@@ -58,5 +61,7 @@ KernelChoice choice_e4m3(int config, bool out_bf16, bool nn);
 KernelChoice choice_e5m2(int config, bool out_bf16, bool nn);
 // Block-scaled 8-bit operands: one configuration (128 x 256, one CTA).
 KernelChoice choice_mx(bool e5m2, bool out_bf16, bool nn);
+// 2:4-sparse A, fp16 or bf16 (C of the same type): one configuration (128 x 256, one CTA).
+KernelChoice choice_sparse(bool bf16, bool nn);
 
 }  // namespace dtg

@@ -222,6 +222,27 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4(uint32_t taddr, uint64_t 
     asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
+// D (+)= A x B with A 2:4-sparse (kind::f16, K = 32 per instruction): A holds the two kept
+// values of every group of four along K, the metadata at sp_meta_tmem (TMEM) names their
+// positions.
+__device__ __forceinline__ void mma_sp_f16_cta1(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t meta_tmem,
+                                                uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::1.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Copy a 128-row x 128-bit matrix from shared memory (matrix descriptor sdesc) into TMEM
+// lanes 0-127, columns taddr .. taddr + 3.  Ordered before later tcgen05.mma of the thread.
+__device__ __forceinline__ void tmem_cp_128x128b(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::1.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive once on `bar` when every tcgen05 operation this thread issued so far completes.
 __device__ __forceinline__ void mma_commit_cta1(uint32_t bar)
 {

@@ -73,6 +73,9 @@ def load() -> ctypes.CDLL:
         "gemm_run_ex": ([p, ctypes.POINTER(gemm_args_t), p], i32),
         "gemm_run_mx": ([p, ctypes.POINTER(gemm_args_t), p, p, p], i32),
         "gemm_mx_scale_bytes": ([i64, i64], i64),
+        "gemm_run_sp": ([p, ctypes.POINTER(gemm_args_t), p, p], i32),
+        "gemm_sp_meta_bytes": ([i64, i64], i64),
+        "gemm_sp_compress": ([p, p, i64, i64, i64, i32, p, i64, p, p, p], i32),
         "gemm_mx_pack_scales": ([p, p, i64, i64, i64, p, p], i32),
         "gemm_sync_status": ([p, p], i32),
         "gemm_error_info": ([p, ctypes.POINTER(i32)], i32),
@@ -105,6 +108,11 @@ def check_args(A: int, B: int, C: int, M, N, K, lda, ldb, ldc, layout: int, dtyp
 def mx_scale_bytes(rows: int, K: int) -> int:
     """Bytes of the chunked block-scale layout for `rows` rows and K elements of K."""
     return int(load().gemm_mx_scale_bytes(rows, K))
+
+
+def sp_meta_bytes(M: int, K: int) -> int:
+    """Bytes of the chunked 2:4 sparsity metadata for M rows and K."""
+    return int(load().gemm_sp_meta_bytes(M, K))
 
 
 def tile_coord(tile: int, tiles_m: int, tiles_n: int, group_m: int):
@@ -314,6 +322,57 @@ class Gemm:
                              alpha, beta, int(c_col_major), scale_a, scale_b, _stream_ptr(stream))
         if st != OK:
             raise GemmError(st, "gemm_run_mx")
+        return C
+
+    def sp_compress(self, A: torch.Tensor, stream=None):
+        """2:4 compression of a dense fp16/bf16 device matrix (gemm_sp_compress, async):
+        returns (Ac: M x K/2 kept values, meta: chunked metadata bytes, bad: 1-element int32
+        device tensor counting groups with more than two non-zeros)."""
+        if A.dtype not in TORCH_TO_DTYPE or A.dim() != 2:
+            raise TypeError("A must be a 2-D float16 or bfloat16 tensor")
+        M, K = A.shape
+        if K % 4:
+            raise ValueError("K must be a multiple of 4")
+        Ac = empty_output(M, K // 2, A.dtype, A.device)
+        meta = torch.empty(max(sp_meta_bytes(M, K), 16), dtype=torch.uint8, device=A.device)
+        bad = torch.zeros(1, dtype=torch.int32, device=A.device)
+        st = self._lib.gemm_sp_compress(self._h, A.data_ptr() or None, M, K, _ld(A), TORCH_TO_DTYPE[A.dtype],
+                                        Ac.data_ptr() or None, _ld(Ac), meta.data_ptr(), bad.data_ptr(),
+                                        _stream_ptr(stream))
+        if st != OK:
+            raise GemmError(st, "gemm_sp_compress")
+        return Ac, meta, bad
+
+    def run_sp_raw(self, Ac: int, B: int, C: int, meta: int, M, N, K, lda, ldb, ldc, layout: int, dtype: int,
+                   alpha: float = 1.0, beta: float = 0.0, c_col_major: int = 0, stream: int = 0) -> int:
+        """gemm_run_sp on raw device addresses (Ac: the compressed A, lda its pitch; K logical)."""
+        a = gemm_args_t(Ac or None, B or None, C or None, M, N, K, lda, ldb, ldc, layout, dtype, alpha, beta,
+                        c_col_major, dtype, 1.0, 1.0)
+        return int(self._lib.gemm_run_sp(self._h, ctypes.byref(a), meta or None, stream or None))
+
+    def run_sp(self, Ac: torch.Tensor, B: torch.Tensor, meta: torch.Tensor, C: torch.Tensor | None = None,
+               layout: str = "NN", alpha: float = 1.0, beta: float = 0.0, c_col_major: bool = False,
+               stream=None) -> torch.Tensor:
+        """C = alpha * A·B + beta * C with A 2:4-sparse, given as (Ac, meta) from sp_compress.
+        K = 2 * Ac's columns.  Async on `stream`."""
+        M, K = Ac.shape[0], 2 * Ac.shape[1]
+        N = B.shape[1] if layout == "NN" else B.shape[0]
+        if (B.shape[0] if layout == "NN" else B.shape[1]) != K:
+            raise ValueError(f"shape mismatch: Ac {tuple(Ac.shape)}, B {tuple(B.shape)}, layout {layout}")
+        if Ac.dtype != B.dtype or Ac.dtype not in TORCH_TO_DTYPE:
+            raise TypeError("Ac and B must both be float16 or both bfloat16")
+        if meta.dtype != torch.uint8 or meta.numel() < sp_meta_bytes(M, K):
+            raise ValueError(f"meta must hold {sp_meta_bytes(M, K)} bytes")
+        shape = (N, M) if c_col_major else (M, N)
+        if C is None:
+            C = empty_output(*shape, Ac.dtype, Ac.device)
+        if tuple(C.shape) != shape or C.dtype != Ac.dtype:
+            raise ValueError("C has the wrong shape or dtype")
+        st = self.run_sp_raw(Ac.data_ptr(), B.data_ptr(), C.data_ptr(), meta.data_ptr(), M, N, K, _ld(Ac), _ld(B),
+                             _ld(C), LAYOUTS[layout], TORCH_TO_DTYPE[Ac.dtype], alpha, beta, int(c_col_major),
+                             _stream_ptr(stream))
+        if st != OK:
+            raise GemmError(st, "gemm_run_sp")
         return C
 
     def run_host(self, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor, layout: str = "NN", stream=None) -> int:

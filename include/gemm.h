@@ -176,6 +176,43 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
 gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* sfa, const void* sfb,
                           void* stream);
 
+/* 2:4 structured sparsity ("张量缩并：mma 语法", structured sparsity: with at most two
+ * non-zeros in every four consecutive elements along K of a row of A, the hardware skips the
+ * zero products; a metadata operand names the kept elements).  C = alpha * scale_a * scale_b *
+ * A·B + beta * C where A is given compressed:
+ *   - args->A: the kept values, M x K/2 (lda >= K/2, a multiple of 8; 16-byte aligned): for
+ *     every group g of four along K, the two kept elements in ascending position order.
+ *   - meta: their positions, in the chunked layout gemm_sp_compress writes
+ *     (gemm_sp_meta_bytes(M, K) bytes, 16-byte aligned): chunk (row block rb of 128 rows,
+ *     K stage s of 64) starts at byte (rb * ceil(K/64) + s) * 4096 and has two 2048-byte
+ *     halves, for K [64 s, 64 s + 32) and [64 s + 32, 64 s + 64); in a half, lane l of the
+ *     block takes 16 bytes at l * 16: a 32-bit word, then three words of padding.  A group
+ *     of four K elements takes 4 bits: the low two give the position (0..3) of the first kept
+ *     element, the high two the second, first < second.  Rows pair up: for rows r = 16 b + i
+ *     and r + 8 (i < 8), lane r's word holds groups 0-3 of the half's 32 K of row r (bits
+ *     0-15, group q at bits 4q) and of row r + 8 (bits 16-31); lane r + 8's word holds
+ *     groups 4-7 of the two rows the same way.  Positions must be distinct and ascending
+ *     (the pattern of padding rows and groups is (0, 1)); otherwise the result is undefined.
+ *   - dtype F16 or BF16 with out_dtype == dtype; K a multiple of 4 (else UNSUPPORTED); B, C,
+ *     alpha, beta, c_col_major and the status codes as in gemm_run_ex.  K == 0 gives C = beta
+ *     * C and ignores meta.  GEMM_OPT_CONFIG does not apply (one 128 x 256 configuration). */
+gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream);
+
+/* Bytes of the chunked sparsity metadata for M rows and K: ceil(M/128) * ceil(K/64) * 4096
+ * (0 when M or K is 0). */
+int64_t gemm_sp_meta_bytes(int64_t M, int64_t K);
+
+/* Enqueue on `stream` the compression of a dense 2:4 matrix A (M x K, lda >= K, device, 16-bit
+ * dtype F16 or BF16) into Ac (M x K/2, ldac >= K/2) and meta (gemm_sp_meta_bytes(M, K) bytes,
+ * 16-byte aligned).  Per group of four along K the first two non-zero elements are kept (a
+ * value is zero when it is +0 or -0); fewer are completed with the lowest free positions, in
+ * ascending order.  Groups with more than two non-zeros keep their first two and are counted
+ * into *bad_groups (a device int32, added to atomically; may be NULL).  M == 0 or K == 0 is a
+ * no-op; K % 4 != 0 or a misaligned meta is UNSUPPORTED; null pointers, lda < K or
+ * ldac < K/2 are INVALID_ARG. */
+gemm_status_t gemm_sp_compress(gemm_handle_t h, const void* A, int64_t M, int64_t K, int64_t lda, gemm_dtype_t dtype,
+                               void* Ac, int64_t ldac, void* meta, int32_t* bad_groups, void* stream);
+
 /* Bytes of the chunked block-scale layout for `rows` rows and K elements of K:
  * ceil(rows / 128) * ceil(K / 128) * 512 (0 when rows or K is 0).  Chunk (rb, g) covers rows
  * [128 rb, 128 rb + 128) and K blocks [4 g, 4 g + 4) and starts at byte (rb * ceil(K/128) + g)

@@ -144,3 +144,12 @@ def test_mx_scale_bytes_without_a_gpu(lib):
     so = lib.load()
     assert so.gemm_mx_pack_scales(None, None, 1, 1, 1, None, None) == lib.ERR_INVALID_ARG
     assert so.gemm_run_mx(None, None, None, None, None) == lib.ERR_INVALID_ARG
+
+
+def test_sparse_entry_points_without_a_gpu(lib):
+    assert lib.sp_meta_bytes(0, 64) == 0 and lib.sp_meta_bytes(5, 0) == 0
+    assert lib.sp_meta_bytes(1, 4) == 4096 and lib.sp_meta_bytes(128, 64) == 4096
+    assert lib.sp_meta_bytes(129, 65) == 2 * 2 * 4096
+    so = lib.load()
+    assert so.gemm_run_sp(None, None, None, None) == lib.ERR_INVALID_ARG
+    assert so.gemm_sp_compress(None, None, 1, 4, 4, 0, None, 2, None, None, None) == lib.ERR_INVALID_ARG
