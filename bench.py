@@ -3,8 +3,9 @@
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload W]
 
 ``--workload`` picks another row of the workload table: c1..c5 (16-bit operands),
-c4-e4m3 (8-bit operands, per-tensor scales, gemm_run_ex) or c4-mx (8-bit operands with
-E8M0 scales per 32 K elements, gemm_run_mx).
+c4-e4m3 (8-bit operands, per-tensor scales, gemm_run_ex), c4-mx (8-bit operands with
+E8M0 scales per 32 K elements, gemm_run_mx) or c4-sp (a 2:4-sparse A, gemm_run_sp; TFLOP/s
+counted dense-equivalent, 2MNK, against twice the dense peak).
 
 One step = one full GEMM (the whole hot path: TMA ring, tcgen05 MMA, epilogue) on
 inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank runs
@@ -165,9 +166,12 @@ def oracle_rows_fn(A, B, w):
     import oracle
     from dense_tiled_gemm_04_gb300.workloads import block_scales, tensor_scales
 
+    threads = oracle.max_threads()
+    if w.sparse:
+        Ac, E, _ = oracle.sparse24_compress(A)
+        return lambda rows: (oracle.gemm_sparse24(Ac, E, B, w.layout, w.dtype, rows=rows), threads)[1]
     if w.elem_bytes == 2:
         return lambda rows: oracle.gemm_rows(A, B, w.layout, w.dtype, rows)[2]
-    threads = oracle.max_threads()
     if w.scales == "block":
         sa, sb = block_scales(w)
         return lambda rows: (oracle.gemm_blockscaled(A, B, sa, sb, w.layout, w.dtype, w.out_dtype, rows=rows),
@@ -214,7 +218,7 @@ def run_reference(args, w):
     oracle.build()
     A, B = workload_inputs(w)
     threads = oracle.max_threads()
-    if w.elem_bytes == 1:
+    if w.elem_bytes == 1 or w.sparse:
         return run_reference_rows(args, w, A, B, threads)
     rng = np.random.default_rng(1)
     # Elements per step sized so warm-up + timed steps take about a minute in total.
@@ -288,19 +292,40 @@ def run_reference_rows(args, w, A, B, threads):
 
 def make_step(g, native, torch, w, A, B, C, stream):
     """The library call one step makes, for the workload's operand kind.  Returns
-    (step(), plan dict, extra device inputs, description of the kernel kind)."""
+    (step(), plan dict, the device tensors a step reads, description of the kernel kind)."""
     from dense_tiled_gemm_04_gb300.workloads import block_scales, tensor_scales
 
     sp = stream.cuda_stream
     lay, dt = native.LAYOUTS[w.layout], native.DTYPES[w.dtype]
     base = (A.data_ptr(), B.data_ptr(), C.data_ptr())
     dims = (w.M, w.N, w.K, A.stride(0), B.stride(0), C.stride(0))
+
+    def one_config_plan():
+        old = g.get_option(native.OPT_CONFIG)
+        g.set_option(native.OPT_CONFIG, native.CONFIG_128x256)  # the block-scaled / sparse configuration
+        plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
+        g.set_option(native.OPT_CONFIG, old)
+        return plan
+
+    if w.sparse:
+        # The compression is a one-time preparation of A (like packing weights): outside the step.
+        Ac, meta, bad = g.sp_compress(A, stream)
+        torch.cuda.synchronize(A.device)
+        if int(bad.item()) != 0:
+            raise RuntimeError("A is not 2:4 sparse")
+
+        def step():
+            st = g.run_sp_raw(Ac.data_ptr(), B.data_ptr(), C.data_ptr(), meta.data_ptr(), w.M, w.N, w.K, Ac.stride(0),
+                              B.stride(0), C.stride(0), lay, dt, 1.0, 0.0, 0, sp)
+            if st != native.OK:
+                raise native.GemmError(st, "gemm_run_sp")
+        return step, one_config_plan(), [Ac, meta, B], "kind::f16 .sp (2:4-sparse A)"
     if w.elem_bytes == 2:
         def step():
             st = g.run_raw(*base, *dims, lay, dt, sp)
             if st != native.OK:
                 raise native.GemmError(st, "gemm_run")
-        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [], "kind::f16"
+        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [A, B], "kind::f16"
     out = native.DTYPES[w.out_dtype]
     if w.scales == "tensor":
         s_a, s_b = tensor_scales(w)
@@ -309,7 +334,7 @@ def make_step(g, native, torch, w, A, B, C, stream):
             st = g.run_ex_raw(*base, *dims, lay, dt, 1.0, 0.0, 0, sp, out, s_a, s_b)
             if st != native.OK:
                 raise native.GemmError(st, "gemm_run_ex")
-        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [], "kind::f8f6f4, per-tensor scales"
+        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype), [A, B], "kind::f8f6f4, per-tensor scales"
     sa, sb = block_scales(w)
     psa = g.pack_scales(torch.from_numpy(sa).to(A.device), w.K, stream)
     psb = g.pack_scales(torch.from_numpy(sb).to(A.device), w.K, stream)
@@ -318,11 +343,7 @@ def make_step(g, native, torch, w, A, B, C, stream):
         st = g.run_mx_raw(*base, psa.data_ptr(), psb.data_ptr(), *dims, lay, dt, out, stream=sp)
         if st != native.OK:
             raise native.GemmError(st, "gemm_run_mx")
-    old = g.get_option(native.OPT_CONFIG)
-    g.set_option(native.OPT_CONFIG, native.CONFIG_128x256)  # the one block-scaled configuration
-    plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
-    g.set_option(native.OPT_CONFIG, old)
-    return step, plan, [psa, psb], "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
+    return step, one_config_plan(), [A, B, psa, psb], "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
 
 
 def run_ours(args, w):
@@ -352,7 +373,7 @@ def run_ours(args, w):
     A, B = A_cpu.to(dev), B_cpu.to(dev)
     C = native.empty_output(w.M, w.N, TORCH_DTYPES[w.out_dtype], dev)
     stream = torch.cuda.current_stream(dev)
-    step, plan, extra, kind = make_step(g, native, torch, w, A, B, C, stream)
+    step, plan, step_inputs, kind = make_step(g, native, torch, w, A, B, C, stream)
 
     for _ in range(max(args.warmup, 3)):
         step()
@@ -385,11 +406,12 @@ def run_ours(args, w):
     # End to end through the public C ABI on pinned host buffers: H2D of A and B, the
     # kernel, D2H of C, synchronised every step.
     e2e = None
-    if not args.no_e2e and w.elem_bytes == 1:
-        # 8-bit operands: the same library call, with the step's inputs (A, B and any block
-        # scales) copied in from pinned host memory and C copied back, every step.
-        hosts = [t.cpu().pin_memory() for t in (A, B, *extra)]
-        devs = [A, B, *extra]
+    if not args.no_e2e and (w.elem_bytes == 1 or w.sparse):
+        # 8-bit or sparse operands: the same library call, with the step's inputs (A or its
+        # compressed form, B, any block scales or metadata) copied in from pinned host memory
+        # and C copied back, every step.
+        hosts = [t.cpu().pin_memory() for t in step_inputs]
+        devs = step_inputs
         Ch = torch.empty(C.shape, dtype=C.dtype).pin_memory()
         e2e_steps = max(3, min(args.steps, 20))
         barrier(world)
@@ -424,14 +446,16 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
 
     peaks, peak_src = load_peaks()
-    # 8-bit operands: the bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25).
-    ratio = 2.0 if w.elem_bytes == 1 else 1.0
+    # 8-bit operands: the bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25); a
+    # 2:4-sparse A: twice the dense peak (sparse tensor rate), flops counted dense-equivalent.
+    ratio = 2.0 if (w.elem_bytes == 1 or w.sparse) else 1.0
     peak = ratio * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
     achieved = flops / (ms_step * 1e-3) / 1e12
     src = f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback bf16"
     roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
                 "traffic": load_traffic(args.workload),
-                "peak_source": src + (" x 2 (nominal fp8/bf16 dense ratio)" if ratio != 1.0 else ""),
+                "peak_source": src + (" x 2 (2:4 sparse tensor rate, dense-equivalent flops)" if w.sparse else
+                                      " x 2 (nominal fp8/bf16 dense ratio)" if ratio != 1.0 else ""),
                 "nominal_dense_peak_tflops": 2250.0 * ratio, "frac_of_nominal": achieved / (2250.0 * ratio),
                 "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
     if "bf16_tflops_sustained" in peaks:
@@ -449,7 +473,8 @@ def run_ours(args, w):
             "vs_baseline": None, "dtype": w.dtype,
             "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
                     f"(torch CPU generator, seed {w.seed})"
-                    + (", E8M0 block scales uniform in 124..130 (numpy generator)" if w.scales == "block" else ""),
+                    + (", E8M0 block scales uniform in 124..130 (numpy generator)" if w.scales == "block" else "")
+                    + (", A pruned to a seeded 2:4 pattern along K" if w.sparse else ""),
             "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
                        "accumulate": "fp32", "out": w.out_dtype,
                        "kernel": f"tcgen05 {kind}, {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
@@ -483,7 +508,7 @@ def main(argv=None):
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
-                    help="c1..c5, c4-e4m3, c4-mx (default c4, the headline workload)")
+                    help="c1..c5, c4-e4m3, c4-mx, c4-sp (default c4, the headline workload)")
     ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
                     help="kernel configuration (default: the library's own choice)")
     args = ap.parse_args(argv)

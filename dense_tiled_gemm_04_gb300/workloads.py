@@ -9,7 +9,9 @@ first, then B in its *stored* shape (K x N for NN, N x K for TN), in fp32; the
 values are scaled and rounded to the operand type (fp16, bf16, E4M3 or E5M2) by torch's
 round-to-nearest-even cast.  Block scales (E8M0 exponents, one per 32 K elements of each
 row of A and column of B) are drawn by a numpy generator seeded with seed + 1000,
-uniform in {124..130} (scales 1/8 .. 8).
+uniform in {124..130} (scales 1/8 .. 8).  A sparse workload's A is pruned to a 2:4 pattern
+along K (prune_24: two of the four positions of every group drawn uniformly from the six
+pairs by a numpy generator seeded with seed + 2000).
 Distributions: ``uniform`` = U[-1, 1) (``rand*2-1``), ``normal`` = N(0, 1)
 (``randn``), ``int`` = integers uniform in {-2..2} (``randint(-2, 3)``).
 A leading dimension larger than the row length pads each row with NaN, so a
@@ -38,6 +40,7 @@ class Workload:
     seed: int
     out: str = ""    # type of C ("" = dtype; 8-bit operands: "f16" | "bf16")
     scales: str = "none"  # 8-bit operands: "tensor" (scale_a = scale_b = K^-1/4) | "block" (E8M0 per 32 K)
+    sparse: bool = False  # A pruned to a 2:4 pattern along K (prune_24, seed + 2000)
 
     @property
     def out_dtype(self) -> str:
@@ -53,9 +56,12 @@ class Workload:
 
     @property
     def algorithmic_bytes(self) -> int:
-        """Read A and B (and their block scales) once, write the 16-bit C once."""
+        """Read A and B (and their block scales) once, write the 16-bit C once.  A 2:4 A
+        counts its kept half and 4 bits of positions per group of four."""
         sf = (self.M + self.N) * -(-self.K // 32) if self.scales == "block" else 0
-        return self.elem_bytes * (self.M * self.K + self.K * self.N) + 2 * self.M * self.N + sf
+        a = self.elem_bytes * self.M * self.K // 2 + self.M * self.K // 8 if self.sparse else \
+            self.elem_bytes * self.M * self.K
+        return a + self.elem_bytes * self.K * self.N + 2 * self.M * self.N + sf
 
     def with_dist(self, dist: str, scale: float = 1.0) -> "Workload":
         return replace(self, dist=dist, scale=scale)
@@ -73,6 +79,9 @@ WORKLOADS = {
                         "normal", 1.0, 5, out="bf16", scales="tensor"),
     "c4-mx": Workload("square E4M3 TN 8192^3, bf16 C, E8M0 scales per 32 K", 8192, 8192, 8192, "TN", "e4m3",
                       "normal", 1.0, 6, out="bf16", scales="block"),
+    # A with a 2:4 pattern along K: the structured-sparsity form of the same page.
+    "c4-sp": Workload("square bf16 TN 8192^3, A 2:4-sparse", 8192, 8192, 8192, "TN", "bf16", "normal",
+                      1.0 / math.sqrt(4096), 7, sparse=True),
 }
 
 
@@ -153,7 +162,10 @@ def make_inputs(M: int, N: int, K: int, layout: str, dtype: str, dist: str, seed
 
 
 def workload_inputs(w: Workload, lda: int | None = None, ldb: int | None = None):
-    return make_inputs(w.M, w.N, w.K, w.layout, w.dtype, w.dist, w.seed, w.scale, lda, ldb)
+    A, B = make_inputs(w.M, w.N, w.K, w.layout, w.dtype, w.dist, w.seed, w.scale, lda, ldb)
+    if w.sparse:
+        A = prune_24(A, w.seed + 2000)
+    return A, B
 
 
 def round_up(x: int, m: int) -> int:
