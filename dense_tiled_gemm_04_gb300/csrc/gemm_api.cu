@@ -24,6 +24,7 @@ using dtg::KernelParams;
 constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
+constexpr int32_t kTmapBytes = -1;  // get_tmap element type: raw bytes (side data)
 constexpr int kNumSlots = 72;  // 3 configurations x 12 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
@@ -163,6 +164,7 @@ bool get_tmap(std::vector<TmapEntry>* cache, const void* ptr, uint64_t inner, ui
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     // 8-bit floats travel as bytes: TMA only moves them, the MMA interprets them.
+    // kTmapBytes: raw bytes (side data).
     const CUtensorMapDataType dt = dtype == GEMM_DTYPE_BF16   ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
                                    : dtype == GEMM_DTYPE_F16 ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16
                                                              : CU_TENSOR_MAP_DATA_TYPE_UINT8;
@@ -190,7 +192,7 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
 {
     const bool nn = layout == GEMM_LAYOUT_NN, out_bf16 = out == GEMM_DTYPE_BF16;
     if (family == kBlockScaled) return dtg::choice_mx(in == GEMM_DTYPE_E5M2, out_bf16, nn);
-    if (family == kSparse24) return dtg::choice_sparse(in == GEMM_DTYPE_BF16, nn);
+    if (family == kSparse24) return dtg::choice_sparse(config, in == GEMM_DTYPE_BF16, nn);
     switch (in) {
     case GEMM_DTYPE_BF16: return dtg::choice_bf16(config, nn);
     case GEMM_DTYPE_E4M3: return dtg::choice_e4m3(config, out_bf16, nn);
@@ -371,7 +373,15 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     }
 
     const int family = ep.sfa ? kBlockScaled : (ep.meta ? kSparse24 : kDense);
-    const int config = family != kDense ? GEMM_CONFIG_128x256 : pick_config(o, dev, M, N);
+    // Block-scaled kernels: one configuration.  Sparse kernels: the CTA pair where the dense
+    // choice would take it (or when asked), else the one-CTA tile; the pair addresses the
+    // metadata by 16-byte rows with 32-bit TMA coordinates.
+    int config = pick_config(o, dev, M, N);
+    if (family == kBlockScaled) config = GEMM_CONFIG_128x256;
+    if (family == kSparse24) {
+        const bool rows_fit = cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / 16) < (int64_t(1) << 31);
+        config = (config == GEMM_CONFIG_256x256 && rows_fit) ? GEMM_CONFIG_256x256 : GEMM_CONFIG_128x256;
+    }
     const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
     const int slot = slot_of(config, dtype, out, layout, family);
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
@@ -431,7 +441,16 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.sfb_blocks = static_cast<int32_t>(cdiv(N, dtg::kSfChunkRows));
     kp.meta = static_cast<const uint8_t*>(ep.meta);
 
-    void* args[] = {&tA, &tB, &tC, &kp};
+    // Side data of a CTA-pair sparse kernel: the metadata chunks as rows of 16 bytes, a box of
+    // one chunk (256 rows) per stage and CTA.
+    CUtensorMap tS = tA;
+    if (family == kSparse24 && kc.cluster == 2) {
+        const uint64_t rows = static_cast<uint64_t>(cdiv(M, dtg::kBM) * cdiv(K, 64)) * (dtg::kMetaChunkBytes / 16);
+        if (!get_tmap(cache, ep.meta, 16, rows, 16, 16, dtg::kMetaChunkBytes / 16, kTmapBytes, &tS,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_ERR_CUDA;
+    }
+    void* args[] = {&tA, &tB, &tC, &tS, &kp};
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);

@@ -555,11 +555,13 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
     return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
 }
 
-// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).
+// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  tmS: the side data of a
+// CTA-pair sparse kernel (metadata chunks seen as rows of 16 bytes); unused otherwise.
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
-                        const __grid_constant__ CUtensorMap tmC, const KernelParams p)
+                        const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
+                        const KernelParams p)
 {
     using T = Operand<IN>;
     constexpr int kRanks = PAIR ? 2 : 1;
@@ -575,9 +577,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = typename KernelLayout<BN, STAGES, IN, PAIR>::S;
     constexpr int kSfChunks = T::kMX ? L::kSfBytes / kSfChunkBytes : 0;  // per stage: A, then B
     constexpr int kSideCols = T::kMX ? kSfChunks * 4 : (T::kSparse ? 2 * kMetaTmemStride : 0);  // TMEM cols / stage
-    static_assert(!kSide || (!PAIR && BN <= kSfTmemCol &&
+    static_assert(!kSide || ((!PAIR || T::kSparse) && BN <= kSfTmemCol &&
                              kSfTmemCol + STAGES * kSideCols <= static_cast<int>(kTmemCols)),
-                  "block-scaled / sparse kernels: one CTA, the accumulator and the side data fit in TMEM");
+                  "block-scaled kernels: one CTA; the accumulator and the side data fit in TMEM");
 
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1 KB (128-byte swizzle atoms repeat every 8 rows).
@@ -618,6 +620,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmC);
+        if constexpr (kSide && PAIR) ptx::prefetch_tmap(&tmS);
     }
     if (warp == kMmaWarp) {
         if constexpr (PAIR) {
@@ -675,7 +678,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if (leader) {
                             const int sf_bytes =
                                 T::kMX ? (1 + sf_b_chunks) * kSfChunkBytes : (T::kSparse ? kMetaChunkBytes : 0);
-                            ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * L::kStageBytes + sf_bytes);
+                            ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * (L::kStageBytes + sf_bytes));
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
                         }
@@ -696,9 +699,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                             // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
                         }
-                        if constexpr (T::kSparse)
-                            ptx::bulk_load_1d(base + L::kSfOff + stage * L::kSfBytes,
-                                              p.meta + (tm * p.num_kb + kb) * kMetaChunkBytes, kMetaChunkBytes, fb);
+                        if constexpr (T::kSparse) {
+                            // This CTA's 128 rows: metadata chunk (row block, stage) -- one 1-D bulk
+                            // copy, or, in a pair, a TMA box of 256 rows of 16 bytes that completes
+                            // on the leader's barrier like the A and B boxes.
+                            const int64_t chunk = (tm * kRanks + rank) * p.num_kb + kb;
+                            if constexpr (PAIR)
+                                load(base + L::kSfOff + stage * L::kSfBytes, &tmS, 0,
+                                     static_cast<int32_t>(chunk * (kMetaChunkBytes / 16)));
+                            else
+                                ptx::bulk_load_1d(base + L::kSfOff + stage * L::kSfBytes,
+                                                  p.meta + chunk * kMetaChunkBytes, kMetaChunkBytes, fb);
+                        }
                         if constexpr (T::kMX) {
                             const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
                             const int64_t g = kb;
@@ -786,9 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         sf_tmem = tmem_base + col;
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            ptx::tmem_cp_128x128b(sf_tmem + h * kMetaTmemStride,
-                                                  smem_desc_plain(meta_smem + h * kMetaHalfBytes, 0, 128));
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t d = smem_desc_plain(meta_smem + h * kMetaHalfBytes, 0, 128);
+                            if constexpr (PAIR)
+                                ptx::tmem_cp_128x128b_pair(sf_tmem + h * kMetaTmemStride, d);
+                            else
+                                ptx::tmem_cp_128x128b(sf_tmem + h * kMetaTmemStride, d);
+                        }
                     }
 #pragma unroll
                     for (int k = 0; k < T::kStageK / T::kMmaK; ++k) {
@@ -809,7 +825,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
                         if constexpr (PAIR) {
-                            if constexpr (T::kF8)
+                            if constexpr (T::kSparse)
+                                ptx::mma_sp_f16_pair(d_tmem, adesc, bdesc, sf_tmem + k * kMetaTmemStride, idesc,
+                                                     accumulate);
+                            else if constexpr (T::kF8)
                                 ptx::mma_f8_pair(d_tmem, adesc, bdesc, idesc, accumulate);
                             else
                                 ptx::mma_f16_pair(d_tmem, adesc, bdesc, idesc, accumulate);

@@ -1,14 +1,26 @@
-// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output.
+// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output: the one-CTA 128 x 256 tile
+// and the 256 x 256 CTA pair.
 #include "kernel_set.cuh"
 
 namespace dtg {
 namespace {
-template <int IN, bool BF16>
-KernelChoice sparse_choice(bool nn)
+constexpr int kSparsePairStages = 6;
+
+template <int IN, bool BF16, bool NN>
+KernelChoice sparse_choice(int config)
 {
-    return nn ? one_cta_choice<256, 4, IN, BF16, true>(1) : one_cta_choice<256, 4, IN, BF16, false>(1);
+    if (config == 3)  // GEMM_CONFIG_256x256
+        return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
+                kSparsePairStages, 2,
+                reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, true>),
+                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc};
+    return one_cta_choice<256, 4, IN, BF16, NN>(1);
 }
 }  // namespace
 
-KernelChoice choice_sparse(bool bf16, bool nn) { return bf16 ? sparse_choice<7, true>(nn) : sparse_choice<6, false>(nn); }
+KernelChoice choice_sparse(int config, bool bf16, bool nn)
+{
+    if (bf16) return nn ? sparse_choice<7, true, true>(config) : sparse_choice<7, true, false>(config);
+    return nn ? sparse_choice<6, false, true>(config) : sparse_choice<6, false, false>(config);
+}
 }  // namespace dtg

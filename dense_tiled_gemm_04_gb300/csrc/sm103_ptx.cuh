@@ -372,6 +372,26 @@ __device__ __forceinline__ void mma_f8_pair(uint32_t d_tmem, uint64_t adesc, uin
         : "memory");
 }
 
+// Pair form of mma_sp_f16_cta1 (M = 256 over the two CTAs; each CTA's metadata for its own
+// 128 rows sits at meta_tmem of its own TMEM).
+__device__ __forceinline__ void mma_sp_f16_pair(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t meta_tmem,
+                                                uint32_t idesc, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %5, 0;\n\t"
+        "tcgen05.mma.sp.cta_group::2.kind::f16 [%0], %1, %2, [%3], %4, p;\n\t}\n" ::"r"(d_tmem),
+        "l"(adesc), "l"(bdesc), "r"(meta_tmem), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Pair form of tmem_cp_128x128b, issued by the leader for both CTAs of the pair: each CTA's
+// shared memory at the descriptor's address goes to its own TMEM at taddr.
+__device__ __forceinline__ void tmem_cp_128x128b_pair(uint32_t taddr, uint64_t sdesc)
+{
+    asm volatile("tcgen05.cp.cta_group::2.128x128b [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
+}
+
 // Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of `cta_mask` when
 // all tcgen05 operations this thread issued so far complete.
 __device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)

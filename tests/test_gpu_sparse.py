@@ -39,6 +39,17 @@ def g():
     h.close()
 
 
+# AUTO picks the CTA pair for large problems; 128x256 / 256x256 force the one-CTA tile / the pair.
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256]
+
+
+@pytest.fixture
+def config(g, request):
+    g.set_option(native.OPT_CONFIG, request.param)
+    yield request.param
+    g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+
+
 def unpack_meta(meta: np.ndarray, M: int, K: int) -> np.ndarray:
     """The chunked metadata written back as plain words (M x ceil(K/32)), from the layout's
     definition: chunk (rb, s) at (rb * S + s) * 4096, word 2s + h in half h (2048 bytes), lane
@@ -120,9 +131,10 @@ def test_compress_matches_the_oracle(g, dtype, shape):
     assert meta.numel() >= native.sp_meta_bytes(M, K)
 
 
+@pytest.mark.parametrize("config", CONFIGS, indirect=True)
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-def test_int_operands_bit_exact(g, layout, dtype):
+def test_int_operands_bit_exact(g, config, layout, dtype):
     M, N, K = 300, 257, 520  # ragged M, N; K = 8 stages of 64 + 8
     A, B = make_inputs(M, N, K, layout, dtype, "int", seed=103)
     A = prune_24(A, seed=104)
@@ -145,13 +157,16 @@ def test_normal_operands_within_tolerance(g, layout, dtype):
     assert_close(got, oracle.gemm(A, B, layout, dtype), dtype, f"{dtype} {layout}")
 
 
-def test_one_kept_value_selects_its_b_row(g):
+@pytest.mark.parametrize("config", CONFIGS, indirect=True)
+def test_one_kept_value_selects_its_b_row(g, config):
     # A single 1.0 at K position k of row m: row m of C is row k of B (NN), for positions in
-    # every nibble of both metadata words of a stage and in a later stage.
-    M, N, K = 128, 64, 192
+    # every nibble of both metadata words of a stage and in a later stage, in both CTAs' rows
+    # of a pair tile (256 rows).
+    M, N, K = 256, 64, 192
     _, B = make_inputs(M, N, K, "NN", "f16", "int", seed=107)
     A = torch.zeros((M, K), dtype=torch.float16)
-    picks = [(0, 0), (1, 1), (2, 6), (3, 7), (5, 13), (31, 31), (32, 33), (40, 62), (77, 63), (100, 64), (127, 191)]
+    picks = [(0, 0), (1, 1), (2, 6), (3, 7), (5, 13), (31, 31), (32, 33), (40, 62), (77, 63), (100, 64), (127, 191),
+             (128, 2), (137, 11), (150, 40), (200, 127), (255, 190)]
     for m, k in picks:
         A[m, k] = 1.0
     Ac, meta, bad = compress(g, A)
@@ -162,9 +177,10 @@ def test_one_kept_value_selects_its_b_row(g):
         assert np.array_equal(got[m], bc[k]), (m, k)
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("col_major", [False, True])
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_accumulate_and_column_major_bit_exact(g, col_major, layout):
+def test_accumulate_and_column_major_bit_exact(g, config, col_major, layout):
     M, N, K = 333, 200, 264
     A, B = make_inputs(M, N, K, layout, "bf16", "int", seed=108)
     A = prune_24(A, seed=109)
@@ -179,8 +195,9 @@ def test_accumulate_and_column_major_bit_exact(g, col_major, layout):
 
 @pytest.mark.parametrize("shape", [(1, 1, 4), (7, 9, 16), (128, 256, 64), (129, 257, 132), (64, 48, 40),
                                    (3, 600, 36), (200, 136, 4096)])
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_edge_shapes(g, shape, layout):
+def test_edge_shapes(g, config, shape, layout):
     M, N, K = shape
     A, B = make_inputs(M, N, K, layout, "f16", "int", seed=111)
     A = prune_24(A, seed=112)
@@ -190,8 +207,9 @@ def test_edge_shapes(g, shape, layout):
     assert_exact(got, oracle.gemm(A, B, layout, "f16"), f"{shape} {layout}")
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("stream_k", [0, 1])
-def test_multi_tile_stream_k_bit_exact(g, stream_k):
+def test_multi_tile_stream_k_bit_exact(g, config, stream_k):
     M, N, K = 16384, 1024, 2048
     A, B = make_inputs(M, N, K, "TN", "bf16", "int", seed=113)
     A = prune_24(A, seed=114)
@@ -221,7 +239,8 @@ def test_full_size_8192_sampled(g, layout):
     assert_close(codes(C)[rows], oracle.gemm_rows(A, B, layout, "bf16", rows)[0], "bf16", f"8192^3 {layout}")
 
 
-def test_watchdog_reports_a_timeout(g):
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
+def test_watchdog_reports_a_timeout(g, config):
     M, N, K = 512, 512, 1024
     A, B = make_inputs(M, N, K, "TN", "f16", "int", seed=119)
     A = prune_24(A, seed=120)
