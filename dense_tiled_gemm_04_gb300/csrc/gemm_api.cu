@@ -191,7 +191,7 @@ enum Family { kDense = 0, kBlockScaled = 1, kSparse24 = 2 };
 KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
     const bool nn = layout == GEMM_LAYOUT_NN, out_bf16 = out == GEMM_DTYPE_BF16;
-    if (family == kBlockScaled) return dtg::choice_mx(in == GEMM_DTYPE_E5M2, out_bf16, nn);
+    if (family == kBlockScaled) return dtg::choice_mx(config, in == GEMM_DTYPE_E5M2, out_bf16, nn);
     if (family == kSparse24) return dtg::choice_sparse(config, in == GEMM_DTYPE_BF16, nn);
     switch (in) {
     case GEMM_DTYPE_BF16: return dtg::choice_bf16(config, nn);
@@ -373,13 +373,18 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     }
 
     const int family = ep.sfa ? kBlockScaled : (ep.meta ? kSparse24 : kDense);
-    // Block-scaled kernels: one configuration.  Sparse kernels: the CTA pair where the dense
-    // choice would take it (or when asked), else the one-CTA tile; the pair addresses the
-    // metadata by 16-byte rows with 32-bit TMA coordinates.
+    // Sparse kernels: the CTA pair where the dense choice would take it (or when asked), else
+    // the one-CTA 128 x 256 tile.  Block-scaled kernels: the one-CTA tile unless the pair is
+    // asked for (measured: the pair gains ~2 % at 8192^3 and loses ~7 % at 4096^3).  The pair
+    // addresses the side data by rows of 16 bytes with 32-bit TMA coordinates, which must fit.
     int config = pick_config(o, dev, M, N);
-    if (family == kBlockScaled) config = GEMM_CONFIG_128x256;
-    if (family == kSparse24) {
-        const bool rows_fit = cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / 16) < (int64_t(1) << 31);
+    if (family == kBlockScaled && o.config != GEMM_CONFIG_256x256) config = GEMM_CONFIG_128x256;
+    if (family != kDense) {
+        const int64_t lim = int64_t(1) << 31;
+        const bool rows_fit =
+            family == kSparse24
+                ? cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / 16) < lim
+                : (M > N ? cdiv(M, dtg::kBM) : cdiv(N, dtg::kBM)) * cdiv(K, 128) * (dtg::kSfChunkBytes / 16) < lim;
         config = (config == GEMM_CONFIG_256x256 && rows_fit) ? GEMM_CONFIG_256x256 : GEMM_CONFIG_128x256;
     }
     const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
@@ -441,16 +446,24 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.sfb_blocks = static_cast<int32_t>(cdiv(N, dtg::kSfChunkRows));
     kp.meta = static_cast<const uint8_t*>(ep.meta);
 
-    // Side data of a CTA-pair sparse kernel: the metadata chunks as rows of 16 bytes, a box of
-    // one chunk (256 rows) per stage and CTA.
-    CUtensorMap tS = tA;
+    // Side data of a CTA-pair kernel as rows of 16 bytes: the metadata chunks (a box of one
+    // chunk, 256 rows, per stage and CTA), or the A and B scale chunks (boxes of 32 rows).
+    CUtensorMap tS = tA, tS2 = tA;
     if (family == kSparse24 && kc.cluster == 2) {
         const uint64_t rows = static_cast<uint64_t>(cdiv(M, dtg::kBM) * cdiv(K, 64)) * (dtg::kMetaChunkBytes / 16);
         if (!get_tmap(cache, ep.meta, 16, rows, 16, 16, dtg::kMetaChunkBytes / 16, kTmapBytes, &tS,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
-    void* args[] = {&tA, &tB, &tC, &tS, &kp};
+    if (family == kBlockScaled && kc.cluster == 2) {
+        constexpr uint32_t kRows = dtg::kSfChunkBytes / 16;
+        const uint64_t rows_a = static_cast<uint64_t>(cdiv(M, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
+        const uint64_t rows_b = static_cast<uint64_t>(cdiv(N, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
+        if (!get_tmap(cache, ep.sfa, 16, rows_a, 16, 16, kRows, kTmapBytes, &tS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !get_tmap(cache, ep.sfb, 16, rows_b, 16, 16, kRows, kTmapBytes, &tS2, CU_TENSOR_MAP_SWIZZLE_NONE))
+            return GEMM_ERR_CUDA;
+    }
+    void* args[] = {&tA, &tB, &tC, &tS, &tS2, &kp};
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);

@@ -220,7 +220,7 @@ struct Smem {
     static constexpr int kRing = STAGES * kStageBytes;
     static constexpr int kSfOff = kRing;
     static constexpr int kSfBytes = SF_BYTES;
-    static constexpr int kStgOff = kSfOff + STAGES * SF_BYTES;
+    static constexpr int kStgOff = (kSfOff + STAGES * SF_BYTES + 1023) / 1024 * 1024;
     static constexpr int kStgBufs = STG_BUFS;
     static constexpr int kStg = kEpiWarps * STG_BUFS * kStgBytes;
     static constexpr int kBarOff = kStgOff + kStg;
@@ -242,8 +242,10 @@ struct KernelLayout {
     static constexpr int kBRows = BN / (PAIR ? 2 : 1);
     static constexpr bool kMX = Operand<IN>::kMX;
     static constexpr bool kSparse = Operand<IN>::kSparse;
+    // Block scales per CTA and stage: its A rows' chunk and the B chunks of the whole tile (each
+    // CTA of a pair produces all BN columns of its rows, so it holds every column's scales).
     static constexpr int kSfBytes =
-        kMX ? kSfChunkBytes * (1 + kBRows / kSfChunkRows) : (kSparse ? kMetaChunkBytes : 0);
+        kMX ? kSfChunkBytes * (1 + BN / kSfChunkRows) : (kSparse ? kMetaChunkBytes : 0);
     using S = Smem<kBRows, STAGES, kSfBytes, kMX ? 1 : 2, Operand<IN>::kARowBytes>;
 };
 
@@ -555,13 +557,14 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
     return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
 }
 
-// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  tmS: the side data of a
-// CTA-pair sparse kernel (metadata chunks seen as rows of 16 bytes); unused otherwise.
+// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  tmS, tmS2: the side data
+// of a CTA-pair kernel seen as rows of 16 bytes -- the metadata chunks (sparse), or the A and
+// the B scale chunks (block-scaled); unused otherwise.
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, bool PAIR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
-                        const KernelParams p)
+                        const __grid_constant__ CUtensorMap tmS2, const KernelParams p)
 {
     using T = Operand<IN>;
     constexpr int kRanks = PAIR ? 2 : 1;
@@ -577,9 +580,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     using L = typename KernelLayout<BN, STAGES, IN, PAIR>::S;
     constexpr int kSfChunks = T::kMX ? L::kSfBytes / kSfChunkBytes : 0;  // per stage: A, then B
     constexpr int kSideCols = T::kMX ? kSfChunks * 4 : (T::kSparse ? 2 * kMetaTmemStride : 0);  // TMEM cols / stage
-    static_assert(!kSide || ((!PAIR || T::kSparse) && BN <= kSfTmemCol &&
+    static_assert(!kSide || (BN <= kSfTmemCol &&
                              kSfTmemCol + STAGES * kSideCols <= static_cast<int>(kTmemCols)),
-                  "block-scaled kernels: one CTA; the accumulator and the side data fit in TMEM");
+                  "the accumulator and the side data fit in TMEM");
 
     extern __shared__ uint8_t smem_raw[];
     // Align the working area to 1 KB (128-byte swizzle atoms repeat every 8 rows).
@@ -621,6 +624,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmC);
         if constexpr (kSide && PAIR) ptx::prefetch_tmap(&tmS);
+        if constexpr (T::kMX && PAIR) ptx::prefetch_tmap(&tmS2);
     }
     if (warp == kMmaWarp) {
         if constexpr (PAIR) {
@@ -712,14 +716,26 @@ __global__ void __launch_bounds__(kThreads, 1)
                                                   p.meta + chunk * kMetaChunkBytes, kMetaChunkBytes, fb);
                         }
                         if constexpr (T::kMX) {
+                            // This CTA's A rows' chunk and the tile's B chunks: 1-D bulk copies,
+                            // or, in a pair, TMA boxes of 32 rows of 16 bytes completing on the
+                            // leader's barrier.
                             const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
                             const int64_t g = kb;
-                            ptx::bulk_load_1d(sf, p.sfa + (tm * p.num_kb + g) * kSfChunkBytes, kSfChunkBytes, fb);
+                            const int64_t ca = (tm * kRanks + rank) * p.num_kb + g;
                             const int64_t nb0 = tn * (BN / kSfChunkRows);
-                            for (int j = 0; j < sf_b_chunks; ++j)
-                                ptx::bulk_load_1d(sf + (1 + j) * kSfChunkBytes,
-                                                  p.sfb + ((nb0 + j) * p.num_kb + g) * kSfChunkBytes, kSfChunkBytes,
-                                                  fb);
+                            constexpr int kRows = kSfChunkBytes / 16;
+                            if constexpr (PAIR) {
+                                load(sf, &tmS, 0, static_cast<int32_t>(ca * kRows));
+                                for (int j = 0; j < sf_b_chunks; ++j)
+                                    load(sf + (1 + j) * kSfChunkBytes, &tmS2, 0,
+                                         static_cast<int32_t>(((nb0 + j) * p.num_kb + g) * kRows));
+                            } else {
+                                ptx::bulk_load_1d(sf, p.sfa + ca * kSfChunkBytes, kSfChunkBytes, fb);
+                                for (int j = 0; j < sf_b_chunks; ++j)
+                                    ptx::bulk_load_1d(sf + (1 + j) * kSfChunkBytes,
+                                                      p.sfb + ((nb0 + j) * p.num_kb + g) * kSfChunkBytes,
+                                                      kSfChunkBytes, fb);
+                            }
                         }
                     }
                     if (++stage == STAGES) {
@@ -782,8 +798,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                         sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
                         const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
 #pragma unroll
-                        for (int c = 0; c < kSfChunks; ++c)
-                            ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, smem_desc_plain(sf + c * kSfChunkBytes, 0, 128));
+                        for (int c = 0; c < kSfChunks; ++c) {
+                            const uint64_t d = smem_desc_plain(sf + c * kSfChunkBytes, 0, 128);
+                            if constexpr (PAIR)
+                                ptx::tmem_cp_32x128b_warpx4_pair(sf_tmem + 4 * c, d);
+                            else
+                                ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, d);
+                        }
                     }
                     // Sparsity metadata of this stage: per MMA k, 128 rows x 16 bytes -> TMEM lanes
                     // 0-127, columns sf_tmem + 8k .. + 3 (8-column aligned).  The addresses are
@@ -825,7 +846,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
                         if constexpr (PAIR) {
-                            if constexpr (T::kSparse)
+                            if constexpr (T::kMX)
+                                ptx::mma_mxf8_pair(d_tmem, adesc, bdesc, idesc | mx_scale_ids(k), sf_tmem, sf_tmem + 4,
+                                                   accumulate);
+                            else if constexpr (T::kSparse)
                                 ptx::mma_sp_f16_pair(d_tmem, adesc, bdesc, sf_tmem + k * kMetaTmemStride, idesc,
                                                      accumulate);
                             else if constexpr (T::kF8)

@@ -59,8 +59,9 @@ KernelChoice choice_f16(int config, bool nn);
 KernelChoice choice_bf16(int config, bool nn);
 KernelChoice choice_e4m3(int config, bool out_bf16, bool nn);
 KernelChoice choice_e5m2(int config, bool out_bf16, bool nn);
-// Block-scaled 8-bit operands: one configuration (128 x 256, one CTA).
-KernelChoice choice_mx(bool e5m2, bool out_bf16, bool nn);
+// Block-scaled 8-bit operands: config GEMM_CONFIG_256x256 (the CTA pair) or anything else (the
+// one-CTA 128 x 256 tile).
+KernelChoice choice_mx(int config, bool e5m2, bool out_bf16, bool nn);
 // 2:4-sparse A, fp16 or bf16 (C of the same type): config GEMM_CONFIG_256x256 (the CTA pair)
 // or anything else (the one-CTA 128 x 256 tile).
 KernelChoice choice_sparse(int config, bool bf16, bool nn);

@@ -167,7 +167,8 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
  * K elements, and scales in E8M0 (8-bit exponents; 255 is NaN): tcgen05's block-scaled MMA
  * applies them inside the contraction, so no separate dequantisation pass runs.
  *   - args: as for gemm_run_ex, with dtype E4M3 or E5M2 (anything else: INVALID_ARG).
- *     GEMM_OPT_CONFIG does not apply: these kernels use one 128 x 256 configuration.
+ *     Configurations: the one-CTA 128 x 256 tile, or the 256 x 256 CTA pair when
+ *     GEMM_OPT_CONFIG asks for GEMM_CONFIG_256x256.
  *   - sfa: the exponents ea of A (M x ceil(K/32)), sfb: those of B (one row per column n of
  *     Beff, N x ceil(K/32)), both device pointers, 16-byte aligned, in the chunked layout that
  *     gemm_mx_pack_scales writes (gemm_mx_scale_bytes(M, K) and (N, K) bytes).  Unused when
@@ -195,7 +196,8 @@ gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* 
  *     (the pattern of padding rows and groups is (0, 1)); otherwise the result is undefined.
  *   - dtype F16 or BF16 with out_dtype == dtype; K a multiple of 4 (else UNSUPPORTED); B, C,
  *     alpha, beta, c_col_major and the status codes as in gemm_run_ex.  K == 0 gives C = beta
- *     * C and ignores meta.  GEMM_OPT_CONFIG does not apply (one 128 x 256 configuration). */
+ *     * C and ignores meta.  Configurations: the 256 x 256 CTA pair where gemm_run would take
+ *     it (or when GEMM_OPT_CONFIG asks for it), else the one-CTA 128 x 256 tile. */
 gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream);
 
 /* Bytes of the chunked sparsity metadata for M rows and K: ceil(M/128) * ceil(K/64) * 4096

@@ -38,6 +38,17 @@ def g():
     h.close()
 
 
+# AUTO picks the CTA pair for large problems; 128x256 / 256x256 force the one-CTA tile / the pair.
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256]
+
+
+@pytest.fixture
+def config(g, request):
+    g.set_option(native.OPT_CONFIG, request.param)
+    yield request.param
+    g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+
+
 def scales(rows, K, spread, seed):
     rng = np.random.default_rng(seed)
     return rng.integers(127 - spread, 128 + spread, (rows, -(-K // 32))).astype(np.uint8)
@@ -107,10 +118,11 @@ def test_scale_bytes():
     assert native.mx_scale_bytes(300, 8192) == 3 * 64 * 512
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("in_dtype", ["e4m3", "e5m2"])
 @pytest.mark.parametrize("out", ["f16", "bf16"])
-def test_int_operands_bit_exact(g, layout, in_dtype, out):
+def test_int_operands_bit_exact(g, config, layout, in_dtype, out):
     M, N, K = 300, 600, 520  # ragged M, N (the last tile has one B scale chunk) and K (17 blocks)
     A, B = make_inputs(M, N, K, layout, in_dtype, "int", seed=61)
     sa, sb = scales(M, K, 2, seed=62), scales(N, K, 2, seed=63)
@@ -120,9 +132,10 @@ def test_int_operands_bit_exact(g, layout, in_dtype, out):
     assert_exact(got, ref, f"{in_dtype}->{out} {layout}")
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("in_dtype", ["e4m3", "e5m2"])
-def test_normal_operands_within_tolerance(g, layout, in_dtype):
+def test_normal_operands_within_tolerance(g, config, layout, in_dtype):
     M, N, K = 515, 389, 1000
     A, B = make_inputs(M, N, K, layout, in_dtype, "normal", seed=64)
     sa, sb = scales(M, K, 3, seed=65), scales(N, K, 3, seed=66)
@@ -144,9 +157,10 @@ def test_unit_scales_equal_the_unscaled_kernel(g):
     assert_close(got, oracle.gemm_typed(A, B, "TN", "e4m3", "bf16"), "bf16", "unit scales vs oracle")
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("col_major", [False, True])
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_accumulate_and_column_major_bit_exact(g, col_major, layout):
+def test_accumulate_and_column_major_bit_exact(g, config, col_major, layout):
     M, N, K = 333, 200, 264
     A, B = make_inputs(M, N, K, layout, "e4m3", "int", seed=68)
     sa, sb = scales(M, K, 2, seed=69), scales(N, K, 2, seed=70)
@@ -160,8 +174,9 @@ def test_accumulate_and_column_major_bit_exact(g, col_major, layout):
 
 @pytest.mark.parametrize("shape", [(1, 1, 1), (7, 9, 16), (128, 256, 128), (129, 257, 129), (64, 48, 40),
                                    (256, 256, 4096), (3, 600, 31)])
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_edge_shapes(g, shape, layout):
+def test_edge_shapes(g, config, shape, layout):
     M, N, K = shape
     A, B = make_inputs(M, N, K, layout, "e5m2", "int", seed=72)
     sa, sb = scales(M, K, 2, seed=73), scales(N, K, 2, seed=74)
@@ -170,26 +185,31 @@ def test_edge_shapes(g, shape, layout):
     assert_exact(got, oracle.gemm_blockscaled(A, B, sa, sb, layout, "e5m2", "f16"), f"{shape} {layout}")
 
 
-def test_one_block_scale_reaches_only_its_rows(g):
-    # A NaN exponent in one K block of one row of A poisons exactly that row of C.
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
+def test_one_block_scale_reaches_only_its_rows(g, config):
+    # A NaN exponent in one K block of one row of A poisons exactly that row of C, in either
+    # CTA's half of a pair tile; one of a column of B, exactly that column (in both halves).
     M, N, K = 256, 256, 256
     A, B = make_inputs(M, N, K, "TN", "e4m3", "int", seed=75)
     sa, sb = np.full((M, 8), 127, np.uint8), np.full((N, 8), 127, np.uint8)
     sa[77, 5] = 255
+    sa[180, 1] = 255
     got, _ = run_mx(g, A, B, sa, sb, "TN", "bf16")
     vals = oracle.decode(got, "bf16")
-    assert np.all(np.isnan(vals[77]))
-    assert not np.isnan(np.delete(vals, 77, axis=0)).any()
-    sa[77, 5] = 127
+    assert np.all(np.isnan(vals[[77, 180]]))
+    assert not np.isnan(np.delete(vals, [77, 180], axis=0)).any()
+    sa[77, 5] = sa[180, 1] = 127
     sb[200, 2] = 255
+    sb[40, 7] = 255
     got, _ = run_mx(g, A, B, sa, sb, "TN", "bf16")
     vals = oracle.decode(got, "bf16")
-    assert np.all(np.isnan(vals[:, 200]))
-    assert not np.isnan(np.delete(vals, 200, axis=1)).any()
+    assert np.all(np.isnan(vals[:, [40, 200]]))
+    assert not np.isnan(np.delete(vals, [40, 200], axis=1)).any()
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
 @pytest.mark.parametrize("stream_k", [0, 1])
-def test_multi_tile_stream_k_bit_exact(g, stream_k):
+def test_multi_tile_stream_k_bit_exact(g, config, stream_k):
     M, N, K = 16384, 1024, 2048
     A, B = make_inputs(M, N, K, "TN", "e4m3", "int", seed=76)
     sa, sb = scales(M, K, 2, seed=77), scales(N, K, 2, seed=78)
@@ -223,7 +243,8 @@ def test_full_size_8192_sampled(g, layout):
     assert_close(got[rows], ref, "bf16", f"8192^3 {layout}")
 
 
-def test_watchdog_reports_a_timeout(g):
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
+def test_watchdog_reports_a_timeout(g, config):
     M, N, K = 512, 512, 1024
     A, B = make_inputs(M, N, K, "TN", "e4m3", "int", seed=84)
     sa, sb = scales(M, K, 2, seed=85), scales(N, K, 2, seed=86)
