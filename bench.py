@@ -365,7 +365,8 @@ def run_ours(args, w):
     lib_build.build()
     g = native.Gemm(local)
     g.set_option(native.OPT_CONFIG, {"auto": native.CONFIG_AUTO, "128x256": native.CONFIG_128x256,
-                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256}[args.config])
+                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256,
+                                     "512x256": native.CONFIG_512x256}[args.config])
 
     from dense_tiled_gemm_04_gb300.workloads import TORCH_DTYPES
 
@@ -509,7 +510,7 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="c1..c5, c4-e4m3, c4-mx, c4-sp (default c4, the headline workload)")
-    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
+    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256", "512x256"], default="auto",
                     help="kernel configuration (default: the library's own choice)")
     args = ap.parse_args(argv)
     if args.warmup < 3:

@@ -25,7 +25,7 @@ constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int32_t kTmapBytes = -1;  // get_tmap element type: raw bytes (side data)
-constexpr int kNumSlots = 72;  // 3 configurations x 12 operand/output types x 2 layouts
+constexpr int kNumSlots = 96;  // 4 configurations x 12 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -203,7 +203,8 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
 
 int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
-    const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
+    const int c = config == GEMM_CONFIG_512x256 ? 3
+                  : config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
     const int f8 = 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0);  // 0..3
     const int types = family == kSparse24 ? 10 + in : (is_f8(in) ? (family == kBlockScaled ? 6 : 2) + f8 : in);
     return (c * 12 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
@@ -241,7 +242,8 @@ gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int 
 
 int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N)
 {
-    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256)
+    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256 ||
+        o.config == GEMM_CONFIG_512x256)
         return static_cast<int>(o.config);
     // AUTO: the 256 x 256 CTA-pair tile when there is at least one pair tile per pair of
     // SMs (it halves each SM's shared-memory traffic for B); otherwise the 128 x 256 tile
@@ -377,15 +379,25 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     // the one-CTA 128 x 256 tile.  Block-scaled kernels: the one-CTA tile unless the pair is
     // asked for (measured: the pair gains ~2 % at 8192^3 and loses ~7 % at 4096^3).  The pair
     // addresses the side data by rows of 16 bytes with 32-bit TMA coordinates, which must fit.
+    // The multicast configuration (two pairs sharing B) exists for 16-bit dense operands; the
+    // others run the pair in its place.
     int config = pick_config(o, dev, M, N);
-    if (family == kBlockScaled && o.config != GEMM_CONFIG_256x256) config = GEMM_CONFIG_128x256;
+    if (config == GEMM_CONFIG_512x256 && (family == kBlockScaled || is_f8(dtype))) config = GEMM_CONFIG_256x256;
+    if (family == kBlockScaled && o.config != GEMM_CONFIG_256x256 && o.config != GEMM_CONFIG_512x256)
+        config = GEMM_CONFIG_128x256;
     if (family != kDense) {
         const int64_t lim = int64_t(1) << 31;
         const bool rows_fit =
             family == kSparse24
                 ? cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / 16) < lim
                 : (M > N ? cdiv(M, dtg::kBM) : cdiv(N, dtg::kBM)) * cdiv(K, 128) * (dtg::kSfChunkBytes / 16) < lim;
-        config = (config == GEMM_CONFIG_256x256 && rows_fit) ? GEMM_CONFIG_256x256 : GEMM_CONFIG_128x256;
+        config = ((config == GEMM_CONFIG_256x256 || config == GEMM_CONFIG_512x256) && rows_fit) ? config
+                                                                                               : GEMM_CONFIG_128x256;
+        // AUTO, sparse A, many pair tiles: two pairs sharing B (measured +4-7 % at 8192^3, even
+        // at 4096^3, where each cluster gets fewer than 8 items).
+        if (family == kSparse24 && o.config == GEMM_CONFIG_AUTO && config == GEMM_CONFIG_256x256 &&
+            cdiv(M, 512) * cdiv(N, 256) >= 8 * (dev.num_sms / 4))
+            config = GEMM_CONFIG_512x256;
     }
     const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
     const int slot = slot_of(config, dtype, out, layout, family);
@@ -449,13 +461,13 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     // Side data of a CTA-pair kernel as rows of 16 bytes: the metadata chunks (a box of one
     // chunk, 256 rows, per stage and CTA), or the A and B scale chunks (boxes of 32 rows).
     CUtensorMap tS = tA, tS2 = tA;
-    if (family == kSparse24 && kc.cluster == 2) {
+    if (family == kSparse24 && kc.cluster >= 2) {
         const uint64_t rows = static_cast<uint64_t>(cdiv(M, dtg::kBM) * cdiv(K, 64)) * (dtg::kMetaChunkBytes / 16);
         if (!get_tmap(cache, ep.meta, 16, rows, 16, 16, dtg::kMetaChunkBytes / 16, kTmapBytes, &tS,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
-    if (family == kBlockScaled && kc.cluster == 2) {
+    if (family == kBlockScaled && kc.cluster >= 2) {
         constexpr uint32_t kRows = dtg::kSfChunkBytes / 16;
         const uint64_t rows_a = static_cast<uint64_t>(cdiv(M, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
         const uint64_t rows_b = static_cast<uint64_t>(cdiv(N, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
@@ -942,7 +954,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     switch (opt) {
     case GEMM_OPT_CONFIG:
         if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128 &&
-            value != GEMM_CONFIG_256x256)
+            value != GEMM_CONFIG_256x256 && value != GEMM_CONFIG_512x256)
             return GEMM_ERR_INVALID_ARG;
         o.config = value;
         return GEMM_OK;

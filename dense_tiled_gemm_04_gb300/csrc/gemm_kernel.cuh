@@ -236,7 +236,8 @@ struct Smem {
 // Shared-memory layout of a kernel instantiation (host and device agree through this).
 // Block-scaled kernels add the scale chunks of each stage (one for A, one per 128 B rows)
 // and, to stay within 227 KB, keep one staging buffer per epilogue warp; sparse kernels add
-// the stage's metadata chunk and store A rows of 64 bytes.
+// the stage's metadata chunk and store A rows of 64 bytes (the CTA-pair sparse kernel also
+// keeps one staging buffer, for a deeper ring).
 template <int BN, int STAGES, int IN, bool PAIR>
 struct KernelLayout {
     static constexpr int kBRows = BN / (PAIR ? 2 : 1);
@@ -246,7 +247,7 @@ struct KernelLayout {
     // CTA of a pair produces all BN columns of its rows, so it holds every column's scales).
     static constexpr int kSfBytes =
         kMX ? kSfChunkBytes * (1 + BN / kSfChunkRows) : (kSparse ? kMetaChunkBytes : 0);
-    using S = Smem<kBRows, STAGES, kSfBytes, kMX ? 1 : 2, Operand<IN>::kARowBytes>;
+    using S = Smem<kBRows, STAGES, kSfBytes, (kMX || (kSparse && PAIR)) ? 1 : 2, Operand<IN>::kARowBytes>;
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
@@ -316,12 +317,14 @@ __host__ __device__ constexpr uint32_t idesc_mma()
 struct Watchdog {
     volatile int32_t* abort_flag;  // shared memory
     const KernelParams* p;
-    uint32_t peer_abort = 0;       // shared::cluster address of the peer CTA's flag (CTA pairs), or 0
+    uint32_t peer_abort[3] = {0, 0, 0};  // shared::cluster addresses of the other CTAs' flags, 0 = none
 
     __device__ __forceinline__ void fail(int role, int64_t tile, int kb) const
     {
         *abort_flag = 1;
-        if (peer_abort) ptx::st_shared_cluster_u32(peer_abort, 1u);
+#pragma unroll
+        for (int i = 0; i < 3; ++i)
+            if (peer_abort[i]) ptx::st_shared_cluster_u32(peer_abort[i], 1u);
         if (atomicCAS(p->err, 0, 1) == 0) {
             p->err[1] = role;
             p->err[2] = static_cast<int32_t>(blockIdx.x);
@@ -557,17 +560,22 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
     return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
 }
 
-// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  tmS, tmS2: the side data
+// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  CLUSTER: 1 (one CTA), 2
+// (a CTA pair) or 4 (two CTA pairs computing vertically adjacent tiles -- tile rows 2 r and
+// 2 r + 1 of one tile column -- that share their B boxes by TMA multicast: each CTA loads half
+// of its pair-rank's B box for both pairs, which halves the L2 reads of B).  tmS, tmS2: the side data
 // of a CTA-pair kernel seen as rows of 16 bytes -- the metadata chunks (sparse), or the A and
 // the B scale chunks (block-scaled); unused otherwise.
-template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, bool PAIR>
+template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, int CLUSTER>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
                         const __grid_constant__ CUtensorMap tmS2, const KernelParams p)
 {
     using T = Operand<IN>;
-    constexpr int kRanks = PAIR ? 2 : 1;
+    constexpr bool PAIR = CLUSTER >= 2;
+    constexpr bool MC = CLUSTER == 4;          // two pairs sharing B (multicast)
+    constexpr int kRanks = PAIR ? 2 : 1;       // CTAs per MMA (pair)
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
     // Block-scaled and sparse kernels keep one accumulator and put the side data of every
@@ -602,15 +610,19 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t rank = PAIR ? ptx::cluster_ctarank() : 0u;  // 0: leader (issues the MMAs)
+    const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
+    const uint32_t rank = crank & 1u;         // rank in the pair; 0: the pair's leader (issues its MMAs)
+    const uint32_t pp = crank >> 1;           // pair within the cluster (MC)
+    const uint32_t lead_rank = crank & ~1u;   // cluster rank of this pair's leader
     const bool leader = rank == 0;
+    static_assert(!MC || (!T::kMX && !T::kF8 && BN == 256), "multicast: 16-bit (dense or sparse) 256-wide pair tiles");
     const int64_t unit = PAIR ? static_cast<int64_t>(ptx::cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
     const int64_t units = PAIR ? static_cast<int64_t>(ptx::num_clusters_x()) : static_cast<int64_t>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), 1);
+            ptx::mbar_init(empty_bar(s), MC ? 2 : 1);  // MC: both pairs release the stage
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
@@ -644,7 +656,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem_base = *tmem_slot;
 
     Watchdog wd{abort_flag, &p};
-    if constexpr (PAIR) wd.peer_abort = ptx::mapa_shared(ptx::smem_addr(const_cast<int32_t*>(abort_flag)), rank ^ 1u);
+    if constexpr (PAIR) {
+        const uint32_t own = ptx::smem_addr(const_cast<int32_t*>(abort_flag));
+        wd.peer_abort[0] = ptx::mapa_shared(own, crank ^ 1u);
+        if constexpr (MC) {
+            wd.peer_abort[1] = ptx::mapa_shared(own, crank ^ 2u);
+            wd.peer_abort[2] = ptx::mapa_shared(own, crank ^ 3u);
+        }
+    }
 
     if (warp == kProducerWarp) {
         if (lane == 0) {
@@ -659,18 +678,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             while (it.next(p, tile, kb0, kb1)) {
                 int64_t tm, tn;
                 tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+                if constexpr (MC) tm = 2 * tm + pp;  // a cluster's item is two tile rows
                 const int32_t y_a = static_cast<int32_t>(tm * kTileM + rank * kBM);
                 const int32_t n_b = static_cast<int32_t>(tn * BN + rank * kBRows);
                 for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
                     if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
-                    if (p.fault_inject && leader && unit == 0 && loaded == 1) {
+                    if (p.fault_inject && crank == 0 && unit == 0 && loaded == 1) {
                         // Test hook: leave this stage unarmed so the MMA thread's wait on it
                         // runs out and the watchdog path is exercised.
                     } else {
                         const uint32_t sa = base + stage * L::kStageBytes;
                         const uint32_t sb = sa + L::kABytes;
                         const int32_t k0 = kb * T::kStageK;
-                        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0) : full_bar(stage);
+                        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), lead_rank) : full_bar(stage);
                         // Block scales: the A chunk of this tile row and the B chunks of this
                         // tile's columns that exist (a ragged N may leave out the last).
                         int sf_b_chunks = 0;
@@ -696,9 +716,22 @@ __global__ void __launch_bounds__(kThreads, 1)
                         if constexpr (NN) {
                             // B stored K x N: boxes of one 128-byte row of N (kNBlock elements)
                             // by kStageK rows of K, kStageK * 128 bytes each.
+                            // MC: this CTA loads box pp of its pair-rank's two for both pairs.
+                            if constexpr (MC) {
+                                ptx::tma_load_2d_pair_mc(sb + pp * (T::kStageK * 128), &tmB,
+                                                         n_b + static_cast<int32_t>(pp) * T::kNBlock, k0, fb,
+                                                         static_cast<uint16_t>(0x5u << rank));
+                            } else {
 #pragma unroll
-                            for (int q = 0; q < kBRows / T::kNBlock; ++q)
-                                load(sb + q * (T::kStageK * 128), &tmB, n_b + q * T::kNBlock, k0);
+                                for (int q = 0; q < kBRows / T::kNBlock; ++q)
+                                    load(sb + q * (T::kStageK * 128), &tmB, n_b + q * T::kNBlock, k0);
+                            }
+                        } else if constexpr (MC) {
+                            // B stored N x K, MC: rows [64 pp, 64 pp + 64) of this pair-rank's
+                            // kBRows rows, multicast to the same-rank CTA of both pairs.
+                            ptx::tma_load_2d_pair_mc(sb + pp * (kBRows / 2) * kRowBytes, &tmB, k0,
+                                                     n_b + static_cast<int32_t>(pp) * (kBRows / 2), fb,
+                                                     static_cast<uint16_t>(0x5u << rank));
                         } else {
                             // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
@@ -871,7 +904,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     }
                     // The stage is free once these MMAs finish (in both CTAs of a pair).
                     if constexpr (PAIR)
-                        ptx::mma_commit_pair_mc(empty_bar(stage), 0x3);
+                        ptx::mma_commit_pair_mc(empty_bar(stage), MC ? 0xF : 0x3);
                     else
                         ptx::mma_commit_cta1(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -881,7 +914,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
                 if (aborted) break;
                 if constexpr (PAIR)
-                    ptx::mma_commit_pair_mc(accf_bar(acc), 0x3);  // accumulator complete
+                    ptx::mma_commit_pair_mc(accf_bar(acc), static_cast<uint16_t>(0x3u << lead_rank));  // accumulator complete
                 else
                     ptx::mma_commit_cta1(accf_bar(acc));
                 if (++acc == kAccBufs) {
@@ -892,7 +925,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (aborted) {
                 // Let every MMA issued so far finish before the TMEM is released.
                 if constexpr (PAIR)
-                    ptx::mma_commit_pair_mc(drain_bar, 0x1);
+                    ptx::mma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << crank));
                 else
                     ptx::mma_commit_cta1(drain_bar);
                 wd.drain(drain_bar, 0);
@@ -918,7 +951,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             __syncwarp();
             if (lane == 0) {
                 if constexpr (PAIR)
-                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0));
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), lead_rank));
                 else
                     ptx::mbar_arrive(acce_bar(acc));
             }
@@ -926,6 +959,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         while (it.next(p, tile, kb0, kb1)) {
             int64_t tm, tn;
             tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
+            if constexpr (MC) tm = 2 * tm + pp;
             const bool ok = wd.wait(accf_bar(acc), acc_phase, kRoleEpilogue, tile, -1);
             if (!epilogue_bar_and(ok)) break;  // all four epilogue warps leave together
             ptx::tc_fence_after_sync();
@@ -975,13 +1009,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int64_t tr = tile - p.dp_tiles;
                 constexpr size_t kSlotF4 = static_cast<size_t>(kBM) * BN / 4;
                 auto slot_f4 = [&](int64_t slot) {
-                    return reinterpret_cast<float4*>(p.ws) + (static_cast<size_t>(slot) * kRanks + rank) * kSlotF4 +
+                    return reinterpret_cast<float4*>(p.ws) + (static_cast<size_t>(slot) * CLUSTER + crank) * kSlotF4 +
                            row_in_cta;
                 };
                 int64_t first_unit, parts;
                 sk_parts(p, tr, first_unit, parts);
                 const int64_t my_part = unit - first_unit;
-                int32_t* counter = p.counters + tr * kRanks + rank;
+                int32_t* counter = p.counters + tr * CLUSTER + crank;
                 // Sum all parts in K order (so the result does not depend on who arrives
                 // last) and store.  With own_in_tmem this part's sums are read from TMEM at
                 // its place in the order instead of from the workspace.

@@ -1,18 +1,25 @@
-// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output: the one-CTA 128 x 256 tile
-// and the 256 x 256 CTA pair.
+// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output: the one-CTA 128 x 256 tile,
+// the 256 x 256 CTA pair and two pairs sharing B by multicast.
 #include "kernel_set.cuh"
 
 namespace dtg {
 namespace {
-constexpr int kSparsePairStages = 6;
+// A sparse stage is consumed in two MMAs (half the time of a dense one), so the ring needs
+// more stages for the same lead over the loads: 7 of 28 KB per CTA, with one staging buffer.
+constexpr int kSparsePairStages = 7;
 
 template <int IN, bool BF16, bool NN>
 KernelChoice sparse_choice(int config)
 {
+    if (config == 4)  // GEMM_CONFIG_512x256: two pairs sharing B by multicast
+        return {config, 4 * kBM, 256, 64, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
+                kSparsePairStages, 4,
+                reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, 4>),
+                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc};
     if (config == 3)  // GEMM_CONFIG_256x256
         return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kSparsePairStages, 2,
-                reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, true>),
+                reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, 2>),
                 KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc};
     return one_cta_choice<256, 4, IN, BF16, NN>(1);
 }

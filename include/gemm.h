@@ -87,7 +87,10 @@ enum {
     GEMM_CONFIG_AUTO = 0,
     GEMM_CONFIG_128x256 = 1,   /* 1-CTA tile 128 x 256 x 64, 4-stage ring                      */
     GEMM_CONFIG_128x128 = 2,   /* 1-CTA tile 128 x 128 x 64, 6-stage ring (more tiles)         */
-    GEMM_CONFIG_256x256 = 3    /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
+    GEMM_CONFIG_256x256 = 3,   /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
+    GEMM_CONFIG_512x256 = 4    /* 4-CTA cluster: two CTA pairs on tiles (2r, c) and (2r+1, c),
+                                  sharing B boxes by TMA multicast (16-bit dense operands;
+                                  other operand kinds run the CTA pair instead)               */
 };
 
 /* What gemm_run would launch for a problem (for benchmarks and tests). */
@@ -196,8 +199,9 @@ gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* 
  *     (the pattern of padding rows and groups is (0, 1)); otherwise the result is undefined.
  *   - dtype F16 or BF16 with out_dtype == dtype; K a multiple of 4 (else UNSUPPORTED); B, C,
  *     alpha, beta, c_col_major and the status codes as in gemm_run_ex.  K == 0 gives C = beta
- *     * C and ignores meta.  Configurations: the 256 x 256 CTA pair where gemm_run would take
- *     it (or when GEMM_OPT_CONFIG asks for it), else the one-CTA 128 x 256 tile. */
+ *     * C and ignores meta.  Configurations: where gemm_run would take the CTA pair, two pairs
+ *     sharing B (GEMM_CONFIG_512x256) when there are at least 8 such items per cluster, else the
+ *     pair; otherwise the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask for any of them. */
 gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream);
 
 /* Bytes of the chunked sparsity metadata for M rows and K: ceil(M/128) * ceil(K/64) * 4096

@@ -129,7 +129,8 @@ def test_small_workloads_full(g, name, dist):
 
 @pytest.mark.parametrize("name", ["c3", "c4", "c5"])
 @pytest.mark.parametrize("dist", ["workload", "int"])
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256,
+                                    native.CONFIG_512x256])
 def test_full_size_workloads_sampled(g, name, dist, config):
     w = WORKLOADS[name]
     if dist == "int":
@@ -160,7 +161,8 @@ SHAPES = [(1, 1, 1), (1, 8, 3), (3, 5, 7), (8, 8, 8), (17, 9, 33), (64, 64, 64),
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256,
+                                    native.CONFIG_512x256])
 def test_ragged_shapes(g, layout, dtype, config):
     g.set_option(native.OPT_CONFIG, config)
     try:
@@ -242,7 +244,7 @@ def native_dtype(dtype):
     return {"f16": torch.float16, "bf16": torch.bfloat16}[dtype]
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256, native.CONFIG_512x256])
 @pytest.mark.parametrize("layout", ["TN", "NN"])
 def test_several_tiles_per_cta_and_raster_groups(g, config, layout):
     M, N, K = 1000, 1000, 520
@@ -270,6 +272,20 @@ def test_plan_reports_pair_clusters(g):
     assert pl["cluster"] == 2 and pl["bm"] == 256 and pl["bn"] == 256
     assert pl["grid"] % 2 == 0 and 2 <= pl["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count
     assert pl["tiles_m"] == 32 and pl["tiles_n"] == 32 and pl["k_blocks"] == 128
+
+
+def test_plan_reports_multicast_clusters(g):
+    # Two CTA pairs per cluster of four, one 512 x 256 item (two tile rows) per cluster.
+    g.set_option(native.OPT_CONFIG, native.CONFIG_512x256)
+    try:
+        pl = g.plan(8192, 8192, 8192, "TN", "bf16")
+        fp8 = g.plan(8192, 8192, 8192, "TN", "e4m3")
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+    assert pl["cluster"] == 4 and pl["bm"] == 512 and pl["bn"] == 256 and pl["config"] == native.CONFIG_512x256
+    assert pl["grid"] % 4 == 0 and 4 <= pl["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count
+    assert pl["tiles_m"] == 16 and pl["tiles_n"] == 32
+    assert fp8["cluster"] == 2 and fp8["config"] == native.CONFIG_256x256  # 8-bit operands: the pair
 
 
 def test_large_extents(g):
@@ -342,7 +358,7 @@ def test_run_host_pipelined_chunks_and_padding(g, layout):
     assert_exact(got[:, :N], oracle.gemm(A, B, layout, "bf16"), "run_host chunks")
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_256x256, native.CONFIG_512x256])
 def test_watchdog_timeout_is_reported_and_context_survives(g, config):
     # One ring stage is left unarmed in CTA 0: the MMA thread's wait on it must run out,
     # the kernel must leave cleanly, and the host must read GEMM_ERR_TIMEOUT.
@@ -360,7 +376,8 @@ def test_watchdog_timeout_is_reported_and_context_survives(g, config):
         assert g.sync_status() == native.ERR_TIMEOUT
         info = g.error_info()
         # A timeout, first seen in the first CTA (or, for CTA pairs, either CTA of the first pair).
-        assert info[0] == 1 and info[2] in ((0, 1) if config == native.CONFIG_256x256 else (0,)), info
+        first = {native.CONFIG_256x256: (0, 1), native.CONFIG_512x256: (0, 1, 2, 3)}.get(config, (0,))
+        assert info[0] == 1 and info[2] in first, info
     finally:
         g.set_option(native.OPT_FAULT_INJECT, 0)
         g.set_option(native.OPT_TIMEOUT_NS, 2_000_000_000)

@@ -40,7 +40,7 @@ def g():
 
 
 # AUTO picks the CTA pair for large problems; 128x256 / 256x256 force the one-CTA tile / the pair.
-CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256]
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256, native.CONFIG_512x256]
 
 
 @pytest.fixture

@@ -50,6 +50,10 @@ CASES = [
     (1100, 1000, 1800, "TN", "f16", native.CONFIG_256x256, 12),
     (1100, 1000, 1800, "NN", "bf16", native.CONFIG_256x256, 6),
     (2000, 700, 3000, "TN", "bf16", native.CONFIG_256x256, 14),
+    # clusters of four: 20 CTAs = 5 units, 28 = 7 units, against 12 (512 x 256) items
+    (1100, 1000, 1800, "TN", "f16", native.CONFIG_512x256, 20),
+    (1100, 1000, 1800, "NN", "bf16", native.CONFIG_512x256, 28),
+    (2000, 700, 3000, "TN", "bf16", native.CONFIG_512x256, 20),
 ]
 
 
@@ -80,7 +84,7 @@ def test_stream_k_parity_and_plan(g, case):
         _reset(g)
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_128x128, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_128x128, native.CONFIG_256x256, native.CONFIG_512x256])
 def test_stream_k_on_equals_off_on_integers(g, config):
     M, N, K = 1000, 1000, 2048
     A, B = make_inputs(M, N, K, "TN", "bf16", "int", seed=99)
