@@ -183,8 +183,8 @@ int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
 bool is_f8(gemm_dtype_t t) { return t == GEMM_DTYPE_E4M3 || t == GEMM_DTYPE_E5M2; }
 int elem_bytes(gemm_dtype_t t) { return is_f8(t) ? 1 : 2; }
 
-// Kernel families beyond the dense one: block-scaled 8-bit operands, 2:4-sparse A.  Both run
-// one configuration (128 x 256, one CTA).
+// Kernel families beyond the dense one: block-scaled 8-bit operands, 2:4-sparse A (each with
+// the one-CTA 128 x 256 tile, the CTA pair and -- sparse only -- two pairs sharing B).
 enum Family { kDense = 0, kBlockScaled = 1, kSparse24 = 2 };
 
 // `out` is the type of C: equal to `in` for 16-bit operands, F16 or BF16 for 8-bit ones.

@@ -11,18 +11,28 @@
 //                 语法入门" §5: out-of-range reads contribute 0).
 //   warp 1        MMA issuer (one thread): per K block (128 bytes of K), four tcgen05.mma of
 //                 32 bytes of K each into the TMEM accumulator (kind::f16 for 16-bit operands,
-//                 kind::f8f6f4 for 8-bit ones), then tcgen05.commit releases the stage; after the item's
-//                 last K block a commit marks the accumulator full.  The first MMA of an
-//                 item overwrites (the zero-filled accumulator of §2), later ones add.
+//                 kind::f8f6f4 for 8-bit ones, kind::mxf8f6f4.block_scale for 8-bit ones with
+//                 E8M0 scales, kind::f16 .sp -- two MMAs of 32 K -- for a 2:4-sparse A), then
+//                 tcgen05.commit releases the stage; after the item's last K block a commit
+//                 marks the accumulator full.  The first MMA of an item overwrites (the
+//                 zero-filled accumulator of §2), later ones add.  Block scales and sparsity
+//                 metadata arrive with the stage and are copied into TMEM (tcgen05.cp) first.
 //   warps 2..5    epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
-//                 of its lane quadrant), fp32 -> fp16/bf16 round-to-nearest-even, staging
-//                 in 128-byte-swizzled shared memory and a TMA store that drops elements
-//                 outside M x N (§5: masked write-back).
+//                 of its lane quadrant), C = alpha * acc + beta * C, fp32 -> fp16/bf16
+//                 round-to-nearest-even, staging in 128-byte-swizzled shared memory and a TMA
+//                 store that drops elements outside M x N (§5: masked write-back); C may be
+//                 stored column-major (the page's transposed store).
 //
 // The accumulator is double-buffered in TMEM (2 x BN fp32 columns), so the epilogue of one
-// item overlaps the main loop of the next.
+// item overlaps the main loop of the next; the block-scaled and sparse kernels keep one
+// accumulator (their side data takes the other TMEM columns) and read it whole into registers
+// before storing, which hands it back to the MMA thread early.
 //
-// CTA pairs (PAIR = true): a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// Clusters: CLUSTER = 1 (one CTA), 2 (a CTA pair) or 4 (two CTA pairs on vertically adjacent
+// tiles that share their B boxes by TMA multicast; each stage's empty barrier then counts both
+// pairs).
+//
+// CTA pairs (CLUSTER >= 2): a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 (M = 256).  This is the two-warpgroup kernel of the same page
 // (two workers share one B tile, each takes its own rows of A) moved to the SM level:
 // CTA r loads rows [128 r, 128 r + 128) of the A tile and B rows/columns
