@@ -38,15 +38,25 @@ FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
 KERNEL_DIR = os.path.join("dense_tiled_gemm_04_gb300", "csrc")
 
 
+def _code_only(text: str) -> str:
+    """C++ source without comments and blank space, so that a comment edit does not count as
+    a kernel change (string literals in these sources hold no comment markers)."""
+    import re
+
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", "", text)
+    return re.sub(r"\s+", " ", text).strip()
+
+
 def kernel_fingerprint() -> str:
-    """Hash of the library sources; a stored ncu traffic figure is only reported for the
-    sources it was measured on."""
+    """Hash of the library sources (code only, see _code_only); a stored ncu traffic figure
+    is only reported for the code it was measured on."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, KERNEL_DIR)
     for name in sorted(os.listdir(d)):
         if name.endswith((".cu", ".cuh", ".h")):
-            with open(os.path.join(d, name), "rb") as f:
-                h.update(name.encode() + f.read())
+            with open(os.path.join(d, name), encoding="utf-8") as f:
+                h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
 
 
