@@ -482,15 +482,23 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     cfg.blockDim = dim3(dtg::kThreads, 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
     cfg.stream = stream;
-    cudaLaunchAttribute attr;
+    // Programmatic dependent launch: the grid may be scheduled while the stream's previous
+    // kernel finishes; the kernel runs its prologue, then waits (griddepcontrol.wait) for that
+    // kernel's completion before it touches global memory.
+    cudaLaunchAttribute attrs[2];
+    unsigned n_attrs = 0;
+    attrs[n_attrs].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attrs[n_attrs].val.programmaticStreamSerializationAllowed = 1;
+    ++n_attrs;
     if (kc.cluster > 1) {
-        attr.id = cudaLaunchAttributeClusterDimension;
-        attr.val.clusterDim.x = static_cast<unsigned>(kc.cluster);
-        attr.val.clusterDim.y = 1;
-        attr.val.clusterDim.z = 1;
-        cfg.attrs = &attr;
-        cfg.numAttrs = 1;
+        attrs[n_attrs].id = cudaLaunchAttributeClusterDimension;
+        attrs[n_attrs].val.clusterDim.x = static_cast<unsigned>(kc.cluster);
+        attrs[n_attrs].val.clusterDim.y = 1;
+        attrs[n_attrs].val.clusterDim.z = 1;
+        ++n_attrs;
     }
+    cfg.attrs = attrs;
+    cfg.numAttrs = n_attrs;
     if (cudaLaunchKernelExC(&cfg, kc.fn, args) != cudaSuccess) return GEMM_ERR_CUDA;
     return GEMM_OK;
 }

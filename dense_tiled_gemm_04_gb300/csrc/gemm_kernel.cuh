@@ -664,6 +664,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         __syncthreads();
     ptx::tc_fence_after_sync();
     const uint32_t tmem_base = *tmem_slot;
+    // Everything above touched only shared memory, TMEM and the kernel's parameters; global
+    // memory (A, B, C, side data, workspace) waits for the stream's previous kernel.
+    ptx::grid_dependency_wait();
+    ptx::launch_dependents();
 
     Watchdog wd{abort_flag, &p};
     if constexpr (PAIR) {

@@ -93,6 +93,11 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void* tmap, int3
         : "memory");
 }
 
+// Programmatic dependent launch: wait until the grids this one depends on have completed and
+// their memory operations are visible; let the grids that depend on this one be scheduled.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
 // 1-D bulk copy global -> shared of `bytes` bytes (both addresses 16-byte aligned, bytes a
 // multiple of 16), completing as transaction bytes on the mbarrier `bar`.
 __device__ __forceinline__ void bulk_load_1d(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar)
