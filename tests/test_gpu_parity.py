@@ -387,3 +387,34 @@ def test_watchdog_timeout_is_reported_and_context_survives(g, config):
     finally:
         g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
     assert_exact(got, oracle.gemm(A, B, w.layout, w.dtype), "after timeout")
+
+
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x128, native.CONFIG_256x256,
+                                    native.CONFIG_512x256])
+def test_dependent_gemms_on_one_stream(g, config):
+    # GEMM launches may be scheduled while the stream's previous kernel drains; they must still
+    # read that kernel's results.  Chain on one stream, no host sync in between: a torch kernel
+    # rewrites A in place, C1 = A·B, C2 = C1·B2 (reads C1 as its A), then torch negates C2.
+    M, N, K, N2 = 640, 512, 384, 256
+    A, B = make_inputs(M, N, K, "NN", "f16", "int", seed=201)
+    _, B2 = make_inputs(M, N2, N, "NN", "f16", "int", seed=202)
+    dA, dB, dB2 = A.cuda(), B.cuda(), B2.cuda()
+    g.set_option(native.OPT_CONFIG, config)
+    try:
+        for i in range(3):
+            dA.copy_(A.cuda())
+            dA.mul_(-1)                              # in-place torch kernel just before the GEMM
+            C1 = g.run(dA, dB, layout="NN")
+            C2 = g.run(C1, dB2, layout="NN")         # reads the previous GEMM's output
+            C2.neg_()                                # in-place torch kernel just after
+        torch.cuda.synchronize()
+        assert g.sync_status() == native.OK
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+    negA = (-A.float()).to(torch.float16)
+    ref1 = oracle.gemm(negA, B, "NN", "f16")
+    assert_exact(codes(C1), ref1, "C1 = (-A)·B")
+    c1_host = torch.from_numpy(ref1.view(np.int16)).view(torch.float16)
+    ref2 = oracle.gemm(c1_host, B2, "NN", "f16")
+    got2 = -oracle.decode(codes(C2), "f16")
+    assert np.array_equal(got2, oracle.decode(ref2, "f16")), "C2 = C1·B2 read a stale C1"
