@@ -1059,9 +1059,9 @@ int32_t gemm_api_version(void) { return GEMM_API_VERSION; }
 
 // ---------------------------------------------------------------- allocation-free entry point
 //
-// gemm_run_noalloc serves callers that cannot allocate device memory (stream capture in
-// progress, a host engine that owns all device memory, paths that cannot take the device
-// synchronisation an allocation may imply).  The GEMM kernel's only scratch -- the
+// gemm_run_noalloc serves callers that cannot allocate device memory (a host engine that
+// owns all device memory, paths that cannot take the device synchronisation an allocation
+// may imply, a process at its memory limit).  The GEMM kernel's only scratch -- the
 // 16-byte watchdog record that a handle normally cudaMallocs -- lives in the file-scope
 // array below instead.  Nothing here calls cudaMalloc, cudaFree or any allocating routine.
 namespace {

@@ -279,9 +279,8 @@ gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, in
 /* C = A·B without a handle and without allocating any device memory.
  *
  * The paper has no counterpart to this entry point; it exists for callers that cannot
- * call cudaMalloc: code enqueuing work while a stream is being captured into a graph,
- * plug-ins running inside an engine that owns every byte of device memory through its
- * own pool, latency-critical paths that cannot afford the implicit device-wide
+ * call cudaMalloc: plug-ins running inside an engine that owns every byte of device
+ * memory through its own pool, latency-critical paths that cannot afford the implicit device-wide
  * synchronisation an allocation may cause, or a process already at its memory limit.
  *
  * Arguments and layouts are those of gemm_run (A, B, C device pointers; same checks and

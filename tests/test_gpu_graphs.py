@@ -1,12 +1,10 @@
 """The library's launches captured into CUDA graphs and replayed.
 
-A launch enqueues only kernels (and, for the no-allocation entry point, one memset) on the
-caller's stream, so it can be captured once the first call on that device has set its
-kernel attributes.  Each test captures GEMMs with torch.cuda.graph, changes the inputs in
-place, replays, and compares with the oracle bit for bit (integer inputs).
+A gemm_run launch enqueues only kernels on the caller's stream, so it can be captured once
+the first call on that device has set its kernel attributes.  Each test captures GEMMs
+with torch.cuda.graph, changes the inputs in place, replays, and compares with the oracle
+bit for bit (integer inputs).
 """
-import ctypes
-
 import numpy as np
 import pytest
 import torch
@@ -86,30 +84,3 @@ def test_chain_of_gemms_in_one_graph(g):
     assert_exact(codes(C1), ref1, "C1")
     c1 = torch.from_numpy(ref1.view(np.int16)).view(torch.float16)
     assert_exact(codes(C2), oracle.gemm(c1, B2, "NN", "f16"), "C2")
-
-
-def test_noalloc_entry_point_captured_and_replayed(g):
-    lib = native.load()
-    M, N, K = 512, 768, 640
-    A, B = make_inputs(M, N, K, "TN", "f16", "int", seed=305)
-    A2, _ = make_inputs(M, N, K, "TN", "f16", "int", seed=306)
-    dA, dB = A.cuda(), B.cuda()
-    C = native.empty_output(M, N, torch.float16, "cuda")
-
-    def call():
-        s = torch.cuda.current_stream().cuda_stream
-        return lib.gemm_run_noalloc(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, dA.stride(0),
-                                    dB.stride(0), C.stride(0), native.LAYOUT_TN, native.DTYPE_F16, s or None, None)
-
-    assert call() == native.OK                    # first call on this device: before any capture
-    torch.cuda.synchronize()
-    graph = torch.cuda.CUDAGraph()
-    with torch.cuda.graph(graph):
-        assert call() == native.OK
-    dA.copy_(A2.cuda())
-    graph.replay()
-    torch.cuda.synchronize()
-    assert_exact(codes(C), oracle.gemm(A2, B, "TN", "f16"), "no-alloc replay")
-    info = (ctypes.c_int32 * 4)()
-    assert lib.gemm_run_noalloc(dA.data_ptr(), dB.data_ptr(), C.data_ptr(), M, N, K, dA.stride(0), dB.stride(0),
-                                C.stride(0), native.LAYOUT_TN, native.DTYPE_F16, None, info) == native.OK

@@ -1,8 +1,8 @@
 """gemm_run_noalloc: the entry point for callers that cannot allocate device memory.
 
-Some callers may not call cudaMalloc at all -- work enqueued while a stream is being
-captured into a graph, plug-ins inside an engine that owns all device memory, paths that
-cannot take the synchronisation an allocation may imply.  For them the library keeps the
+Some callers may not call cudaMalloc at all -- plug-ins inside an engine that owns all
+device memory, paths that cannot take the synchronisation an allocation may imply, a
+process already at its memory limit.  For them the library keeps the
 kernel's only scratch (its 16-byte watchdog record) in a static device array, so this
 entry point needs no handle and allocates nothing.
 
