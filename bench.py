@@ -35,6 +35,8 @@ if ROOT not in sys.path:
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor roofline"
 WORKLOAD = "c4"
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+L2_BYTES = 129 * 10**6        # GB300 L2
+FLUSH_BYTES = 512 * 2**20     # the buffer written between steps whose inputs fit in L2
 KERNEL_DIR = os.path.join("dense_tiled_gemm_04_gb300", "csrc")
 
 
@@ -48,13 +50,19 @@ def _code_only(text: str) -> str:
     return re.sub(r"\s+", " ", text).strip()
 
 
+# What a launch's DRAM traffic depends on besides the kernel's code: the launch shape.
+PLAN_KEYS = ("config", "bm", "bn", "bk", "stages", "cluster", "grid", "dp_tiles", "sk_base", "sk_extra")
+HOST_SOURCE = "gemm_api.cu"  # argument checks, tensor maps, plans and the host pipeline
+
+
 def kernel_fingerprint() -> str:
-    """Hash of the library sources (code only, see _code_only); a stored ncu traffic figure
-    is only reported for the code it was measured on."""
+    """Hash of the kernels' device sources (code only, see _code_only; the host side is left
+    out, its launch shape is compared through PLAN_KEYS); a stored ncu traffic figure is only
+    reported for the code and the launch shape it was measured on."""
     h = hashlib.sha256()
     d = os.path.join(ROOT, KERNEL_DIR)
     for name in sorted(os.listdir(d)):
-        if name.endswith((".cu", ".cuh", ".h")):
+        if name.endswith((".cu", ".cuh", ".h")) and name != HOST_SOURCE:
             with open(os.path.join(d, name), encoding="utf-8") as f:
                 h.update(name.encode() + _code_only(f.read()).encode())
     return h.hexdigest()[:16]
@@ -69,15 +77,19 @@ def load_peaks():
     return dict(FALLBACK_PEAKS), "fallback"
 
 
-def load_traffic(workload_key: str):
-    """DRAM bytes per launch from the committed ncu summary, if it matches this kernel."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def launch_shape(plan: dict) -> dict:
+    return {k: int(plan[k]) for k in PLAN_KEYS}
+
+
+def load_traffic(workload_key: str, plan: dict, path: str = os.path.join(ROOT, "profiles", "traffic.json")):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on this kernel
+    code with this launch shape."""
     if not os.path.exists(path):
         return None
     with open(path) as f:
         d = json.load(f)
     entry = d.get(workload_key)
-    if not entry or entry.get("kernel_sha") != kernel_fingerprint():
+    if not entry or entry.get("kernel_sha") != kernel_fingerprint() or entry.get("plan") != launch_shape(plan):
         return None
     return entry.get("dram_bytes_per_launch")
 
@@ -251,7 +263,8 @@ def run_reference(args, w):
         "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_s * 1e3, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic: seeded N(0,1)/sqrt(K) bf16 inputs (torch CPU generator, seed 3)",
+        "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
+                f"(torch CPU generator, seed {w.seed})",
         "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout, "in_dtype": w.dtype,
                    "sample_per_step": f"{elems} random elements of C"},
         "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
@@ -300,6 +313,41 @@ def run_reference_rows(args, w, A, B, threads):
 # ------------------------------------------------------------------ GPU arm
 
 
+def roofline_line(w, ms_step: float, peaks: dict, peak_src: str, traffic):
+    """The roofline object of the JSON line for workload w at ms_step per launch.
+
+    8-bit operands take the bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25); a
+    2:4-sparse A takes twice the dense peak (the sparse tensor rate), flops counted
+    dense-equivalent.  The bound is whichever roofline time is longer: 2MNK at the tensor
+    peak, or the algorithmic bytes at the measured copy bandwidth."""
+    flops = float(w.flops)
+    ratio = 2.0 if (w.elem_bytes == 1 or w.sparse) else 1.0
+    peak = ratio * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
+    hbm = float(peaks.get("hbm_gbs", FALLBACK_PEAKS["hbm_gbs"]))
+    achieved = flops / (ms_step * 1e-3) / 1e12
+    achieved_gbs = w.algorithmic_bytes / (ms_step * 1e-3) / 1e9
+    src = f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback bf16"
+    tensor = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
+              "traffic": traffic,
+              "peak_source": src + (" x 2 (2:4 sparse tensor rate, dense-equivalent flops)" if w.sparse else
+                                    " x 2 (nominal fp8/bf16 dense ratio)" if ratio != 1.0 else "")}
+    if w.algorithmic_bytes / (hbm * 1e9) > flops / (peak * 1e12):
+        line = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s", "frac": achieved_gbs / hbm,
+                "traffic": traffic,
+                "peak_source": f"{peak_src}: copy bandwidth (read + write)" if peak_src == "measured"
+                else "fallback copy bandwidth",
+                "tensor": {k: tensor[k] for k in ("achieved", "peak", "unit", "frac")}}
+    else:
+        line = dict(tensor, achieved_gbs=achieved_gbs)
+    line.update({"nominal_dense_peak_tflops": 2250.0 * ratio, "frac_of_nominal": achieved / (2250.0 * ratio),
+                 "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes})
+    if "bf16_tflops_sustained" in peaks:
+        line["frac_of_sustained"] = achieved / (ratio * float(peaks["bf16_tflops_sustained"]))
+    return line
+
+
+
+
 def make_step(g, native, torch, w, A, B, C, stream):
     """The library call one step makes, for the workload's operand kind.  Returns
     (step(), plan dict, the device tensors a step reads, description of the kernel kind)."""
@@ -309,13 +357,6 @@ def make_step(g, native, torch, w, A, B, C, stream):
     lay, dt = native.LAYOUTS[w.layout], native.DTYPES[w.dtype]
     base = (A.data_ptr(), B.data_ptr(), C.data_ptr())
     dims = (w.M, w.N, w.K, A.stride(0), B.stride(0), C.stride(0))
-
-    def one_config_plan():
-        old = g.get_option(native.OPT_CONFIG)
-        g.set_option(native.OPT_CONFIG, native.CONFIG_128x256)  # the block-scaled / sparse configuration
-        plan = g.plan(w.M, w.N, w.K, w.layout, w.dtype)
-        g.set_option(native.OPT_CONFIG, old)
-        return plan
 
     if w.sparse:
         # The compression is a one-time preparation of A (like packing weights): outside the step.
@@ -329,7 +370,8 @@ def make_step(g, native, torch, w, A, B, C, stream):
                               B.stride(0), C.stride(0), lay, dt, 1.0, 0.0, 0, sp)
             if st != native.OK:
                 raise native.GemmError(st, "gemm_run_sp")
-        return step, one_config_plan(), [Ac, meta, B], "kind::f16 .sp (2:4-sparse A)"
+        return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype, "sparse24"), [Ac, meta, B], \
+            "kind::f16 .sp (2:4-sparse A)"
     if w.elem_bytes == 2:
         def step():
             st = g.run_raw(*base, *dims, lay, dt, sp)
@@ -353,7 +395,8 @@ def make_step(g, native, torch, w, A, B, C, stream):
         st = g.run_mx_raw(*base, psa.data_ptr(), psb.data_ptr(), *dims, lay, dt, out, stream=sp)
         if st != native.OK:
             raise native.GemmError(st, "gemm_run_mx")
-    return step, one_config_plan(), [A, B, psa, psb], "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
+    return step, g.plan(w.M, w.N, w.K, w.layout, w.dtype, "block_scaled"), [A, B, psa, psb], \
+        "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
 
 
 def run_ours(args, w):
@@ -393,14 +436,28 @@ def run_ours(args, w):
     sampler = ClockSampler(local)
     sampler.start()
     time.sleep(0.3)  # let the sampler start before the timed region
-    ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    # Inputs that fit in L2 would be served from it by the previous step: for those, every
+    # timed step is preceded by a write of a buffer several times larger than L2 (outside
+    # the step's own events), and the step time is the sum of the per-step event times.
+    flush = w.algorithmic_bytes < L2_BYTES
+    flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
     barrier(world)
     torch.cuda.synchronize(dev)
     t_wall0 = time.perf_counter()
-    ev0.record(stream)
-    for _ in range(args.steps):
-        step()
-    ev1.record(stream)
+    if flush:
+        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+               for _ in range(args.steps)]
+        for i, (e0, e1) in enumerate(evs):
+            flush_buf.fill_(i)
+            e0.record(stream)
+            step()
+            e1.record(stream)
+    else:
+        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        ev0.record(stream)
+        for _ in range(args.steps):
+            step()
+        ev1.record(stream)
     torch.cuda.synchronize(dev)
     t_wall1 = time.perf_counter()
     barrier(world)
@@ -408,7 +465,8 @@ def run_ours(args, w):
     st = g.sync_status(stream)
     if st != native.OK:
         raise native.GemmError(st, "watchdog")
-    ms_total = ev0.elapsed_time(ev1)
+    ms_total = sum(e0.elapsed_time(e1) for e0, e1 in evs) if flush else ev0.elapsed_time(ev1)
+    del flush_buf
     ms_total = reduce_max([ms_total], world, dev)[0]
     ms_step = ms_total / args.steps
     flops = float(w.flops)
@@ -457,20 +515,7 @@ def run_ours(args, w):
                "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
 
     peaks, peak_src = load_peaks()
-    # 8-bit operands: the bf16 peak times the nominal fp8 / bf16 dense ratio (4.5 / 2.25); a
-    # 2:4-sparse A: twice the dense peak (sparse tensor rate), flops counted dense-equivalent.
-    ratio = 2.0 if (w.elem_bytes == 1 or w.sparse) else 1.0
-    peak = ratio * float(peaks.get("bf16_tflops", FALLBACK_PEAKS["bf16_tflops"]))
-    achieved = flops / (ms_step * 1e-3) / 1e12
-    src = f"{peak_src}: cuBLAS bf16 8192^3 burst" if peak_src == "measured" else "fallback bf16"
-    roofline = {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s", "frac": achieved / peak,
-                "traffic": load_traffic(args.workload),
-                "peak_source": src + (" x 2 (2:4 sparse tensor rate, dense-equivalent flops)" if w.sparse else
-                                      " x 2 (nominal fp8/bf16 dense ratio)" if ratio != 1.0 else ""),
-                "nominal_dense_peak_tflops": 2250.0 * ratio, "frac_of_nominal": achieved / (2250.0 * ratio),
-                "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes}
-    if "bf16_tflops_sustained" in peaks:
-        roofline["frac_of_sustained"] = achieved / (ratio * float(peaks["bf16_tflops_sustained"]))
+    roofline = roofline_line(w, ms_step, peaks, peak_src, load_traffic(args.workload, plan))
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -491,10 +536,15 @@ def run_ours(args, w):
                        "kernel": f"tcgen05 {kind}, {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
                                  f"ring, {plan['grid']} persistent CTAs"
                                  + (f" in {plan['grid'] // plan['cluster']} CTA pairs (cta_group::2)"
-                                    if plan["cluster"] == 2 else ""),
+                                    if plan["cluster"] == 2 else
+                                    f" in {plan['grid'] // 4} clusters of four (two CTA pairs sharing B by multicast)"
+                                    if plan["cluster"] == 4 else ""),
                        "l2": (f"inputs larger than L2 (A, B, C = {w.algorithmic_bytes / 2**20:.0f} MiB > 129 MB), "
-                              "no flush") if w.algorithmic_bytes > 129e6 else "inputs fit in L2: warm-L2 number",
-                       "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU"},
+                              "no flush") if w.algorithmic_bytes >= L2_BYTES else
+                             (f"inputs fit in L2 ({w.algorithmic_bytes / 2**20:.1f} MiB): a {FLUSH_BYTES >> 20} MiB "
+                              "buffer is written before every step, outside its events (cold L2)"),
+                       "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU",
+                       "plan": launch_shape(plan), "kernel_sha": kernel_fingerprint()},
             "roofline": roofline,
             "cpu_baseline": cpu,
             "e2e": e2e,

@@ -82,6 +82,8 @@ struct LaunchOptions {
     int64_t raster_group = kGroupDefault;
     int64_t fault_inject = 0;
     int64_t stream_k = 1;
+    int64_t host_row_chunks = 8;
+    int64_t host_col_chunks = 4;
 };
 
 // Per-device facts and lazily-set per-kernel state.  Guarded by `mu`.
@@ -94,12 +96,14 @@ struct DeviceState {
 
 // Streams and events of gemm_run_host's copy/compute pipeline (created on first use).
 struct HostPipe {
-    static constexpr int kMaxChunks = 8;
-    static constexpr int kChunksWanted = 4;
+    static constexpr int kMaxRowChunks = 16;  // row chunks of A (and C)
+    static constexpr int kMaxColChunks = 8;   // column chunks of C (B's rows for TN, columns for NN)
+    static constexpr int kMaxPieces = kMaxRowChunks + kMaxColChunks;
     bool ready = false;
-    cudaStream_t in[2] = {nullptr, nullptr}, out = nullptr;
-    cudaEvent_t start = nullptr, b[2] = {nullptr, nullptr}, done = nullptr;
-    cudaEvent_t a[kMaxChunks] = {}, c[kMaxChunks] = {};
+    cudaStream_t in = nullptr, out = nullptr;  // host -> device copies, in order; device -> host copies
+    cudaEvent_t start = nullptr, done = nullptr;
+    cudaEvent_t arrived[kMaxPieces] = {};      // per input piece, in transfer order
+    cudaEvent_t computed[kMaxPieces] = {};     // per GEMM launch
 };
 
 // Stream-K workspace: fp32 partial sums and arrival counters (see gemm_kernel.cuh).
@@ -353,28 +357,10 @@ gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void
     return validate_args(A, B, C, M, N, K, lda, ldb, ldc, layout, dtype);
 }
 
-// Enqueue C = A·B (arguments already validated, M, N > 0) on the current device.
-// `ws` == nullptr restricts the schedule to whole tiles (no stream-K workspace).
-gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Workspace* ws,
-                          std::vector<TmapEntry>* cache, int32_t* err,
-                          const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
-                          int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream,
-                          const Epilogue& ep = Epilogue())
+// The configuration launch_gemm runs for a problem with operands of kind `family`.
+int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N, int64_t K,
+                  gemm_dtype_t dtype, int family)
 {
-    const gemm_dtype_t out = ep.out < 0 ? dtype : ep.out;
-    if (K == 0) {
-        int blocks = static_cast<int>(cdiv(M * N, 256));
-        const int cap = dev.num_sms * 8;
-        if (blocks > cap) blocks = cap;
-        uint16_t* c16 = static_cast<uint16_t*>(C);
-        if (out == GEMM_DTYPE_BF16)
-            dtg::scale_c_kernel<true><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
-        else
-            dtg::scale_c_kernel<false><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
-        return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
-    }
-
-    const int family = ep.sfa ? kBlockScaled : (ep.meta ? kSparse24 : kDense);
     // Sparse kernels: the CTA pair where the dense choice would take it (or when asked), else
     // the one-CTA 128 x 256 tile.  Block-scaled kernels: the one-CTA tile unless the pair is
     // asked for (measured: the pair gains ~2 % at 8192^3 and loses ~7 % at 4096^3).  The pair
@@ -399,6 +385,32 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
             cdiv(M, 512) * cdiv(N, 256) >= 8 * (dev.num_sms / 4))
             config = GEMM_CONFIG_512x256;
     }
+    return config;
+}
+
+// Enqueue C = A·B (arguments already validated, M, N > 0) on the current device.
+// `ws` == nullptr restricts the schedule to whole tiles (no stream-K workspace).
+gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Workspace* ws,
+                          std::vector<TmapEntry>* cache, int32_t* err,
+                          const void* A, const void* B, void* C, int64_t M, int64_t N, int64_t K, int64_t lda,
+                          int64_t ldb, int64_t ldc, gemm_layout_t layout, gemm_dtype_t dtype, cudaStream_t stream,
+                          const Epilogue& ep = Epilogue())
+{
+    const gemm_dtype_t out = ep.out < 0 ? dtype : ep.out;
+    if (K == 0) {
+        int blocks = static_cast<int>(cdiv(M * N, 256));
+        const int cap = dev.num_sms * 8;
+        if (blocks > cap) blocks = cap;
+        uint16_t* c16 = static_cast<uint16_t*>(C);
+        if (out == GEMM_DTYPE_BF16)
+            dtg::scale_c_kernel<true><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
+        else
+            dtg::scale_c_kernel<false><<<blocks, 256, 0, stream>>>(c16, M, N, ldc, ep.col_major, ep.beta);
+        return cudaPeekAtLastError() == cudaSuccess ? GEMM_OK : GEMM_ERR_CUDA;
+    }
+
+    const int family = ep.sfa ? kBlockScaled : (ep.meta ? kSparse24 : kDense);
+    const int config = choose_config(o, dev, M, N, K, dtype, family);
     const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
     const int slot = slot_of(config, dtype, out, layout, family);
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
@@ -631,6 +643,17 @@ __global__ void sparse24_compress_kernel(const uint16_t* A, int64_t M, int64_t K
     }
 }
 
+// Boundaries of `wanted` (at most) equal chunks of an extent, each a multiple of 256 long
+// (whole pair tiles) and at least `min_size` long, except the last: bounds[0] = 0,
+// bounds[n] = extent; returns n.
+int host_chunks(int64_t extent, int64_t wanted, int64_t min_size, int64_t* bounds)
+{
+    const int64_t size = std::max<int64_t>(min_size, (cdiv(extent, wanted) + 255) / 256 * 256);
+    const int n = static_cast<int>(cdiv(extent, size));
+    for (int i = 0; i <= n; ++i) bounds[i] = std::min<int64_t>(static_cast<int64_t>(i) * size, extent);
+    return n;
+}
+
 }  // namespace
 
 extern "C" {
@@ -686,11 +709,11 @@ gemm_status_t gemm_destroy(gemm_handle_t h)
         if (h->ws.partials && cudaFree(h->ws.partials) != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->ws.counters && cudaFree(h->ws.counters) != cudaSuccess) st = GEMM_ERR_CUDA;
         if (h->pipe.ready) {
-            for (cudaStream_t q : {h->pipe.in[0], h->pipe.in[1], h->pipe.out}) cudaStreamDestroy(q);
-            for (cudaEvent_t e : {h->pipe.start, h->pipe.b[0], h->pipe.b[1], h->pipe.done}) cudaEventDestroy(e);
-            for (int i = 0; i < HostPipe::kMaxChunks; ++i) {
-                cudaEventDestroy(h->pipe.a[i]);
-                cudaEventDestroy(h->pipe.c[i]);
+            for (cudaStream_t q : {h->pipe.in, h->pipe.out}) cudaStreamDestroy(q);
+            for (cudaEvent_t e : {h->pipe.start, h->pipe.done}) cudaEventDestroy(e);
+            for (int i = 0; i < HostPipe::kMaxPieces; ++i) {
+                cudaEventDestroy(h->pipe.arrived[i]);
+                cudaEventDestroy(h->pipe.computed[i]);
             }
         }
     }
@@ -855,13 +878,13 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     HostPipe& hp = h->pipe;
     if (!hp.ready) {
-        for (cudaStream_t* q : {&hp.in[0], &hp.in[1], &hp.out})
+        for (cudaStream_t* q : {&hp.in, &hp.out})
             if (cudaStreamCreateWithFlags(q, cudaStreamNonBlocking) != cudaSuccess) return GEMM_ERR_CUDA;
-        for (cudaEvent_t* e : {&hp.start, &hp.b[0], &hp.b[1], &hp.done})
+        for (cudaEvent_t* e : {&hp.start, &hp.done})
             if (cudaEventCreateWithFlags(e, cudaEventDisableTiming) != cudaSuccess) return GEMM_ERR_CUDA;
-        for (int i = 0; i < HostPipe::kMaxChunks; ++i)
-            if (cudaEventCreateWithFlags(&hp.a[i], cudaEventDisableTiming) != cudaSuccess ||
-                cudaEventCreateWithFlags(&hp.c[i], cudaEventDisableTiming) != cudaSuccess)
+        for (int i = 0; i < HostPipe::kMaxPieces; ++i)
+            if (cudaEventCreateWithFlags(&hp.arrived[i], cudaEventDisableTiming) != cudaSuccess ||
+                cudaEventCreateWithFlags(&hp.computed[i], cudaEventDisableTiming) != cudaSuccess)
                 return GEMM_ERR_CUDA;
         hp.ready = true;
     }
@@ -894,44 +917,74 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
     const char* hB = static_cast<const char*>(B);
     char* hC = static_cast<char*>(C);
 
-    // Pipeline: B first (its two halves on two copy streams), then A in row chunks
-    // alternating between the copy streams; the GEMM of a chunk starts on `stream` once B
-    // and the chunk's rows are in, and the chunk's rows of C go back on a third stream
-    // while later chunks compute.  Chunks are whole multiples of 256 rows.
-    const int64_t chunk = std::max<int64_t>(2048, ((M + HostPipe::kChunksWanted - 1) / HostPipe::kChunksWanted + 255) /
-                                                      256 * 256);
-    const int nchunks = static_cast<int>(std::min<int64_t>((M + chunk - 1) / chunk, HostPipe::kMaxChunks));
-    const int64_t rows_per = (M + nchunks - 1) / nchunks;
-    if (cudaEventRecord(hp.start, s) != cudaSuccess) return GEMM_ERR_CUDA;
-    for (cudaStream_t q : {hp.in[0], hp.in[1], hp.out})
-        if (cudaStreamWaitEvent(q, hp.start, 0) != cudaSuccess) return GEMM_ERR_CUDA;
-    if (K > 0) {
-        const int64_t half = b_rows / 2;
-        if (half > 0 && cudaMemcpy2DAsync(dB, dldb * 2, hB, ldb * 2, b_cols * 2, half, cudaMemcpyHostToDevice,
-                                          hp.in[0]) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (cudaMemcpy2DAsync(dB + half * dldb * 2, dldb * 2, hB + half * ldb * 2, ldb * 2, b_cols * 2,
-                              b_rows - half, cudaMemcpyHostToDevice, hp.in[1]) != cudaSuccess)
-            return GEMM_ERR_CUDA;
+    // Pipeline.  The host link, not the GPU, bounds this call, so the aim is to keep the
+    // host-to-device copies running back to back and to copy C back while they run.  A is
+    // split into row chunks and C's columns into column chunks (B's rows for TN, B's
+    // columns for NN).  The inputs go over on one stream in the order B chunk 0, A chunk 0,
+    // B chunk 1, A chunk 1, ... (the rest of the longer list last).  When a piece has
+    // arrived, the GEMM of every block of C it completes is launched on `stream` (one
+    // launch: the new A chunk against the B columns already in, or the new B chunk against
+    // the A rows already in), and that block of C goes back on a third stream while later
+    // pieces are still arriving.  Chunks are at least 1024 rows and 2048 columns, so each
+    // launch still fills the GPU.  Measured on 8192^3 bf16 (a link of ~210 GB/s each way,
+    // ~336 GB/s both ways at once; 1.30 ms for the inputs alone): 8 x 4 chunks 1.72 ms per
+    // call, 4 x 2 1.76, 16 x 1 (512-row GEMMs that each stream all of B) 2.37.
+    int64_t rb[HostPipe::kMaxRowChunks + 1], cb[HostPipe::kMaxColChunks + 1];
+    const int nr = host_chunks(M, h->opts.host_row_chunks, 1024, rb);
+    const int nc = host_chunks(N, h->opts.host_col_chunks, 2048, cb);
+    struct Piece {
+        bool a;  // a row chunk of A (else a column chunk of C's B)
+        int idx;
+    };
+    Piece order[HostPipe::kMaxPieces];
+    int np = 0;
+    for (int k = 0; k < std::max(nr, nc); ++k) {
+        if (k < nc) order[np++] = {false, k};
+        if (k < nr) order[np++] = {true, k};
     }
-    if (cudaEventRecord(hp.b[0], hp.in[0]) != cudaSuccess || cudaEventRecord(hp.b[1], hp.in[1]) != cudaSuccess ||
-        cudaStreamWaitEvent(s, hp.b[0], 0) != cudaSuccess || cudaStreamWaitEvent(s, hp.b[1], 0) != cudaSuccess)
-        return GEMM_ERR_CUDA;
-    for (int i = 0; i < nchunks; ++i) {
-        const int64_t r0 = i * rows_per, rows = std::min(rows_per, M - r0);
-        if (rows <= 0) break;
-        cudaStream_t qin = hp.in[i & 1];
-        if (K > 0 && cudaMemcpy2DAsync(dA + r0 * dlda * 2, dlda * 2, hA + r0 * lda * 2, lda * 2, K * 2, rows,
-                                       cudaMemcpyHostToDevice, qin) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        if (cudaEventRecord(hp.a[i], qin) != cudaSuccess || cudaStreamWaitEvent(s, hp.a[i], 0) != cudaSuccess)
-            return GEMM_ERR_CUDA;
-        const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, dA + r0 * dlda * 2, dB,
-                                             dC + r0 * dldc * 2, rows, N, K, dlda, dldb, dldc, layout, dtype, s);
+
+    if (cudaEventRecord(hp.start, s) != cudaSuccess) return GEMM_ERR_CUDA;
+    for (cudaStream_t q : {hp.in, hp.out})
+        if (cudaStreamWaitEvent(q, hp.start, 0) != cudaSuccess) return GEMM_ERR_CUDA;
+    int a_in = 0, b_in = 0, launches = 0;  // A / B chunks arrived so far (in order)
+    for (int p = 0; p < np; ++p) {
+        const Piece pc = order[p];
+        if (K > 0) {
+            cudaError_t e;
+            if (pc.a) {
+                const int64_t r0 = rb[pc.idx], rows = rb[pc.idx + 1] - r0;
+                e = cudaMemcpy2DAsync(dA + r0 * dlda * 2, dlda * 2, hA + r0 * lda * 2, lda * 2, K * 2, rows,
+                                      cudaMemcpyHostToDevice, hp.in);
+            } else {
+                const int64_t c0 = cb[pc.idx], cols = cb[pc.idx + 1] - c0;
+                e = nn ? cudaMemcpy2DAsync(dB + c0 * 2, dldb * 2, hB + c0 * 2, ldb * 2, cols * 2, K,
+                                           cudaMemcpyHostToDevice, hp.in)
+                       : cudaMemcpy2DAsync(dB + c0 * dldb * 2, dldb * 2, hB + c0 * ldb * 2, ldb * 2, K * 2, cols,
+                                           cudaMemcpyHostToDevice, hp.in);
+            }
+            if (e != cudaSuccess) return GEMM_ERR_CUDA;
+        }
+        if (cudaEventRecord(hp.arrived[p], hp.in) != cudaSuccess) return GEMM_ERR_CUDA;
+        int64_t r0, r1, c0, c1;  // the block of C this piece completes
+        if (pc.a) {
+            ++a_in;
+            r0 = rb[pc.idx], r1 = rb[pc.idx + 1], c0 = 0, c1 = cb[b_in];
+        } else {
+            ++b_in;
+            r0 = 0, r1 = rb[a_in], c0 = cb[pc.idx], c1 = cb[pc.idx + 1];
+        }
+        if (r1 <= r0 || c1 <= c0) continue;
+        if (cudaStreamWaitEvent(s, hp.arrived[p], 0) != cudaSuccess) return GEMM_ERR_CUDA;
+        const char* bblk = nn ? dB + c0 * 2 : dB + c0 * dldb * 2;
+        char* cblk = dC + (r0 * dldc + c0) * 2;
+        const gemm_status_t st = launch_gemm(h->opts, h->dev, &h->ws, &h->tmaps, h->d_err, dA + r0 * dlda * 2, bblk,
+                                             cblk, r1 - r0, c1 - c0, K, dlda, dldb, dldc, layout, dtype, s);
         if (st != GEMM_OK) return st;
-        if (cudaEventRecord(hp.c[i], s) != cudaSuccess || cudaStreamWaitEvent(hp.out, hp.c[i], 0) != cudaSuccess)
+        if (cudaEventRecord(hp.computed[launches], s) != cudaSuccess ||
+            cudaStreamWaitEvent(hp.out, hp.computed[launches], 0) != cudaSuccess)
             return GEMM_ERR_CUDA;
-        if (cudaMemcpy2DAsync(hC + r0 * ldc * 2, ldc * 2, dC + r0 * dldc * 2, dldc * 2, N * 2, rows,
+        ++launches;
+        if (cudaMemcpy2DAsync(hC + (r0 * ldc + c0) * 2, ldc * 2, cblk, dldc * 2, (c1 - c0) * 2, r1 - r0,
                               cudaMemcpyDeviceToHost, hp.out) != cudaSuccess)
             return GEMM_ERR_CUDA;
     }
@@ -986,6 +1039,14 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
         if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
         o.stream_k = value;
         return GEMM_OK;
+    case GEMM_OPT_HOST_ROW_CHUNKS:
+        if (value < 1 || value > HostPipe::kMaxRowChunks) return GEMM_ERR_INVALID_ARG;
+        o.host_row_chunks = value;
+        return GEMM_OK;
+    case GEMM_OPT_HOST_COL_CHUNKS:
+        if (value < 1 || value > HostPipe::kMaxColChunks) return GEMM_ERR_INVALID_ARG;
+        o.host_col_chunks = value;
+        return GEMM_OK;
     default:
         return GEMM_ERR_INVALID_ARG;
     }
@@ -1002,27 +1063,40 @@ gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value
     case GEMM_OPT_RASTER_GROUP: *value = o.raster_group; return GEMM_OK;
     case GEMM_OPT_FAULT_INJECT: *value = o.fault_inject; return GEMM_OK;
     case GEMM_OPT_STREAM_K: *value = o.stream_k; return GEMM_OK;
+    case GEMM_OPT_HOST_ROW_CHUNKS: *value = o.host_row_chunks; return GEMM_OK;
+    case GEMM_OPT_HOST_COL_CHUNKS: *value = o.host_col_chunks; return GEMM_OK;
     default: return GEMM_ERR_INVALID_ARG;
     }
+}
+
+gemm_status_t gemm_query_plan_kind(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_layout_t layout,
+                                   gemm_dtype_t dtype, gemm_kind_t kind, gemm_plan_t* plan)
+{
+    if (!h || !plan || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
+    if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
+    const bool b16 = dtype == GEMM_DTYPE_F16 || dtype == GEMM_DTYPE_BF16;
+    if (kind == GEMM_KIND_DENSE ? !(b16 || is_f8(dtype))
+                                : kind == GEMM_KIND_BLOCK_SCALED ? !is_f8(dtype)
+                                                                 : kind == GEMM_KIND_SPARSE24 ? !b16 : true)
+        return GEMM_ERR_INVALID_ARG;
+    // 8-bit operands: the plan of the bf16-output kernel (the fp16-output one is the same).
+    const gemm_dtype_t out = is_f8(dtype) ? GEMM_DTYPE_BF16 : dtype;
+    const int family = static_cast<int>(kind);  // gemm_kind_t and Family number the kinds alike
+    DeviceGuard g(h->device);
+    if (!g.ok) return GEMM_ERR_CUDA;
+    const int config = choose_config(h->opts, h->dev, M, N, K, dtype, family);
+    const KernelChoice kc = kernel_choice(config, dtype, out, layout, family);
+    const int slot = slot_of(config, dtype, out, layout, family);
+    const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);
+    if (ready != GEMM_OK) return ready;
+    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], &h->ws, M, N, K, kc, plan);
+    return GEMM_OK;
 }
 
 gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K, gemm_layout_t layout,
                               gemm_dtype_t dtype, gemm_plan_t* plan)
 {
-    if (!h || !plan || M < 0 || N < 0 || K < 0) return GEMM_ERR_INVALID_ARG;
-    if (layout != GEMM_LAYOUT_NN && layout != GEMM_LAYOUT_TN) return GEMM_ERR_INVALID_ARG;
-    if (dtype != GEMM_DTYPE_F16 && dtype != GEMM_DTYPE_BF16 && !is_f8(dtype)) return GEMM_ERR_INVALID_ARG;
-    // 8-bit operands: the plan of the bf16-output kernel (the fp16-output one is the same).
-    const gemm_dtype_t out = is_f8(dtype) ? GEMM_DTYPE_BF16 : dtype;
-    const int config = pick_config(h->opts, h->dev, M, N);
-    const KernelChoice kc = kernel_choice(config, dtype, out, layout);
-    const int slot = slot_of(config, dtype, out, layout);
-    DeviceGuard g(h->device);
-    if (!g.ok) return GEMM_ERR_CUDA;
-    const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);
-    if (ready != GEMM_OK) return ready;
-    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], &h->ws, M, N, K, kc, plan);
-    return GEMM_OK;
+    return gemm_query_plan_kind(h, M, N, K, layout, dtype, GEMM_KIND_DENSE, plan);
 }
 
 gemm_status_t gemm_check_args(const void* A, const void* B, const void* C, int64_t M, int64_t N, int64_t K,

@@ -17,12 +17,14 @@ LAYOUT_NN, LAYOUT_TN = 0, 1
 DTYPE_F16, DTYPE_BF16, DTYPE_E4M3, DTYPE_E5M2 = 0, 1, 2, 3
 LAYOUTS = {"NN": LAYOUT_NN, "TN": LAYOUT_TN}
 DTYPES = {"f16": DTYPE_F16, "bf16": DTYPE_BF16, "e4m3": DTYPE_E4M3, "e5m2": DTYPE_E5M2}
+KINDS = {"dense": 0, "block_scaled": 1, "sparse24": 2}  # gemm_kind_t
 TORCH_TO_DTYPE = {torch.float16: DTYPE_F16, torch.bfloat16: DTYPE_BF16}
 # 8-bit operand types (gemm_run_ex only).
 TORCH_TO_DTYPE_EX = {**TORCH_TO_DTYPE, torch.float8_e4m3fn: DTYPE_E4M3, torch.float8_e5m2: DTYPE_E5M2}
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
-OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT, OPT_STREAM_K = range(6)
+OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT, OPT_STREAM_K, \
+    OPT_HOST_ROW_CHUNKS, OPT_HOST_COL_CHUNKS = range(8)
 CONFIG_AUTO, CONFIG_128x256, CONFIG_128x128, CONFIG_256x256, CONFIG_512x256 = range(5)
 
 
@@ -82,6 +84,7 @@ def load() -> ctypes.CDLL:
         "gemm_set_option": ([p, i32, i64], i32),
         "gemm_get_option": ([p, i32, ctypes.POINTER(i64)], i32),
         "gemm_query_plan": ([p, i64, i64, i64, i32, i32, ctypes.POINTER(gemm_plan_t)], i32),
+        "gemm_query_plan_kind": ([p, i64, i64, i64, i32, i32, i32, ctypes.POINTER(gemm_plan_t)], i32),
         "gemm_check_args": ([p, p, p, i64, i64, i64, i64, i64, i64, i32, i32], i32),
         "gemm_tile_coord": ([i64, i64, i64, i64, ctypes.POINTER(i64), ctypes.POINTER(i64)], i32),
         "gemm_run_noalloc": ([p, p, p, i64, i64, i64, i64, i64, i64, i32, i32, p, ctypes.POINTER(i32)], i32),
@@ -195,11 +198,13 @@ class Gemm:
             raise GemmError(st, "gemm_get_option")
         return v.value
 
-    def plan(self, M, N, K, layout="NN", dtype="f16") -> dict:
+    def plan(self, M, N, K, layout="NN", dtype="f16", kind: str = "dense") -> dict:
+        """The launch the entry point for `kind` ("dense", "block_scaled", "sparse24") would make."""
         pl = gemm_plan_t()
-        st = self._lib.gemm_query_plan(self._h, M, N, K, LAYOUTS[layout], DTYPES[dtype], ctypes.byref(pl))
+        st = self._lib.gemm_query_plan_kind(self._h, M, N, K, LAYOUTS[layout], DTYPES[dtype], KINDS[kind],
+                                            ctypes.byref(pl))
         if st != OK:
-            raise GemmError(st, "gemm_query_plan")
+            raise GemmError(st, "gemm_query_plan_kind")
         return {f: getattr(pl, f) for f, _ in gemm_plan_t._fields_}
 
     def error_info(self):

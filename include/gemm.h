@@ -76,10 +76,14 @@ enum {
     GEMM_OPT_FAULT_INJECT = 4, /* test hook: 1 = CTA 0's producer leaves one ring stage unarmed,
                                   so a consumer wait runs out and the watchdog path returns
                                   GEMM_ERR_TIMEOUT through gemm_sync_status (no GPU fault)   */
-    GEMM_OPT_STREAM_K = 5      /* 1 (default): when whole tiles would leave the last wave
+    GEMM_OPT_STREAM_K = 5,     /* 1 (default): when whole tiles would leave the last wave
                                   part-empty, share the K blocks of the last tiles evenly
                                   between CTAs (partial sums merged in K order, so results
                                   are deterministic); 0: whole tiles only                     */
+    GEMM_OPT_HOST_ROW_CHUNKS = 6, /* gemm_run_host: row chunks of A and C, 1..16 (default 8;
+                                  chunks are at least 1024 rows)                              */
+    GEMM_OPT_HOST_COL_CHUNKS = 7  /* gemm_run_host: column chunks of C (B's rows for TN, its
+                                  columns for NN), 1..8 (default 4; at least 2048 columns)   */
 };
 
 typedef int32_t gemm_config_t;
@@ -98,7 +102,7 @@ typedef struct {
     int32_t config;     /* GEMM_CONFIG_* actually chosen                                     */
     int32_t bm, bn, bk; /* output tile (per cluster) and K block                             */
     int32_t stages;     /* shared-memory ring depth                                          */
-    int32_t cluster;    /* CTAs per cluster (1 or 2)                                         */
+    int32_t cluster;    /* CTAs per cluster (1, 2 or 4)                                       */
     int64_t tiles_m, tiles_n, k_blocks;
     int64_t grid;       /* CTAs launched (persistent)                                        */
     int32_t threads;    /* threads per CTA                                                   */
@@ -235,10 +239,14 @@ gemm_status_t gemm_mx_pack_scales(gemm_handle_t h, const void* src, int64_t rows
                                   void* dst, void* stream);
 
 /* Same operation on HOST buffers (pinned memory lets the copies run as DMA): copies A and
- * B to handle-owned device buffers on `stream`, runs the kernel, copies C back (only the
- * M x N window, never the row padding) and synchronises the stream.  Returns the
- * watchdog status as gemm_sync_status does.  Grows its device buffers on demand
- * (cudaMalloc) -- call once outside any timed region to size them. */
+ * B to handle-owned device buffers, runs the kernel, copies C back (only the M x N window,
+ * never the row padding) and synchronises `stream`.  The copies and the GEMMs overlap: A
+ * and C are cut into row chunks and C's columns into column chunks (GEMM_OPT_HOST_ROW_CHUNKS,
+ * GEMM_OPT_HOST_COL_CHUNKS); the inputs go over in order on one internal stream, each block
+ * of C is computed on `stream` as soon as its rows of A and columns of B are in and goes
+ * back on another internal stream while later inputs arrive.  Returns the watchdog status
+ * as gemm_sync_status does.  Grows its device buffers on demand (cudaMalloc) -- call once
+ * outside any timed region to size them. */
 gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void* C,
                             int64_t M, int64_t N, int64_t K,
                             int64_t lda, int64_t ldb, int64_t ldc,
@@ -260,6 +268,19 @@ gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value
 /* Fill *plan with the launch gemm_run would make for this problem (no GPU work). */
 gemm_status_t gemm_query_plan(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
                               gemm_layout_t layout, gemm_dtype_t dtype, gemm_plan_t* plan);
+
+/* Operand kinds for gemm_query_plan_kind: the operands of gemm_run / gemm_run_ex (dense), of
+ * gemm_run_mx (8-bit with E8M0 block scales) and of gemm_run_sp (a 2:4-sparse A). */
+typedef int32_t gemm_kind_t;
+enum { GEMM_KIND_DENSE = 0, GEMM_KIND_BLOCK_SCALED = 1, GEMM_KIND_SPARSE24 = 2 };
+
+/* Fill *plan with the launch the entry point for operands of `kind` would make (no GPU
+ * work).  dtype is the operand type: F16/BF16/E4M3/E5M2 for DENSE (the same as
+ * gemm_query_plan), E4M3/E5M2 for BLOCK_SCALED, F16/BF16 for SPARSE24 (K is the logical,
+ * uncompressed K).  INVALID_ARG for another combination. */
+gemm_status_t gemm_query_plan_kind(gemm_handle_t h, int64_t M, int64_t N, int64_t K,
+                                   gemm_layout_t layout, gemm_dtype_t dtype, gemm_kind_t kind,
+                                   gemm_plan_t* plan);
 
 /* The argument checks gemm_run applies, without a handle or a GPU: INVALID_ARG,
  * UNSUPPORTED or OK exactly as gemm_run would return them before launching.  Pointers

@@ -263,6 +263,29 @@ def test_several_tiles_per_cta_and_raster_groups(g, config, layout):
         g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
 
 
+def test_plan_kind_reports_the_launch_of_each_operand_kind(g):
+    # What gemm_run_sp / gemm_run_mx launch for 8192^3 TN by default: two CTA pairs sharing B
+    # (7-stage ring) for a 2:4-sparse A, the one-CTA 128 x 256 tile (4 stages) for block scales.
+    sp = g.plan(8192, 8192, 8192, "TN", "bf16", "sparse24")
+    assert (sp["config"], sp["cluster"], sp["bm"], sp["bn"], sp["stages"]) == (native.CONFIG_512x256, 4, 512, 256, 7)
+    mx = g.plan(8192, 8192, 8192, "TN", "e4m3", "block_scaled")
+    assert (mx["config"], mx["cluster"], mx["bm"], mx["bn"], mx["stages"]) == (native.CONFIG_128x256, 1, 128, 256, 4)
+    assert g.plan(8192, 8192, 8192, "TN", "bf16") == g.plan(8192, 8192, 8192, "TN", "bf16", "dense")
+    for dtype, kind in (("bf16", "block_scaled"), ("e4m3", "sparse24")):
+        with pytest.raises(native.GemmError):
+            g.plan(64, 64, 64, "TN", dtype, kind)
+
+
+def test_host_chunk_options_defaults_and_limits(g):
+    assert g.get_option(native.OPT_HOST_ROW_CHUNKS) == 8
+    assert g.get_option(native.OPT_HOST_COL_CHUNKS) == 4
+    for opt, hi in ((native.OPT_HOST_ROW_CHUNKS, 16), (native.OPT_HOST_COL_CHUNKS, 8)):
+        for bad in (0, hi + 1):
+            with pytest.raises(native.GemmError):
+                g.set_option(opt, bad)
+    assert g.get_option(native.OPT_HOST_ROW_CHUNKS) == 8
+
+
 def test_plan_reports_pair_clusters(g):
     g.set_option(native.OPT_CONFIG, native.CONFIG_256x256)
     try:
@@ -339,19 +362,32 @@ def test_run_host_matches_oracle(g):
 
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_run_host_pipelined_chunks_and_padding(g, layout):
-    # 5000 rows go through the host path in several row chunks (copy / compute / copy back
-    # overlapped); host buffers have padded rows whose padding must be left alone.
-    M, N, K = 5000, 1000, 520
-    A, B = make_inputs(M, N, K, layout, "bf16", "int", seed=12, lda=K + 8, ldb=(N if layout == "NN" else K) + 16)
+@pytest.mark.parametrize("M,N,K,chunks", [(5000, 1000, 520, None), (4500, 4100, 264, None),
+                                          (4500, 4100, 264, (1, 1)), (3000, 5000, 136, (16, 8))])
+def test_run_host_pipelined_chunks_and_padding(g, layout, M, N, K, chunks):
+    # The host path cuts A into row chunks and C's columns into column chunks (by default at
+    # most 8 x 4, at least 1024 rows and 2048 columns: 5000 rows -> 4 x 1024 + 904; 4100
+    # columns -> 2048 + 2048 + 4), and computes each block of C in its own launch as its
+    # inputs arrive; host buffers have padded rows whose padding must be left alone (pitches
+    # are multiples of 8 elements, as gemm_run_host requires).
+    pad8 = lambda x: -(-x // 8) * 8  # noqa: E731
+    A, B = make_inputs(M, N, K, layout, "bf16", "int", seed=12, lda=pad8(K + 8),
+                       ldb=pad8((N if layout == "NN" else K) + 16))
     Ah = A.as_strided((M, A.stride(0)), (A.stride(0), 1)).pin_memory()[:, :K]
     rows_b = B.shape[0]
     Bh = B.as_strided((rows_b, B.stride(0)), (B.stride(0), 1)).pin_memory()[:, :B.shape[1]]
-    ldc = N + 24
+    ldc = pad8(N + 24)
     Cbuf = torch.full((M, ldc), 0, dtype=torch.int16).view(torch.bfloat16).pin_memory()
     Cbuf.view(torch.int16).fill_(SENTINEL)
     C = Cbuf[:, :N]
-    st = g.run_host(Ah, Bh, C, layout)
+    try:
+        if chunks is not None:
+            g.set_option(native.OPT_HOST_ROW_CHUNKS, chunks[0])
+            g.set_option(native.OPT_HOST_COL_CHUNKS, chunks[1])
+        st = g.run_host(Ah, Bh, C, layout)
+    finally:
+        g.set_option(native.OPT_HOST_ROW_CHUNKS, 8)
+        g.set_option(native.OPT_HOST_COL_CHUNKS, 4)
     assert st == native.OK, native.status_string(st)
     got = Cbuf.view(torch.int16).numpy().view(np.uint16)
     assert_guard(got, M, N)
