@@ -87,3 +87,57 @@ def test_random_epilogues(g, chunk):
         assert guard_ok(out, r, cc), f"write outside the C window: case {c}"
         want = oracle.gemm_axpby(A, B, layout, dtype, alpha, beta, C0)
         assert_exact(got, want, f"case {c} alpha={alpha} beta={beta} col_major={col_major}")
+
+
+def draw_8bit_case(rng):
+    c = draw_case(rng)
+    c.update(in_dtype=str(rng.choice(["e4m3", "e5m2"])), out=str(rng.choice(["f16", "bf16"])),
+             alpha=float(rng.choice([1.0, 0.5, 2.0])), beta=float(rng.choice([0.0, 1.0])),
+             col_major=int(rng.integers(0, 2)))
+    return c
+
+
+def test_random_8bit_operands_with_tensor_and_block_scales(g):
+    from test_gpu_fp8 import factor, int_c, run8
+    from test_gpu_mx import run_mx, scales
+
+    rng = np.random.default_rng(6000)
+    for i in range(16):
+        c = draw_8bit_case(rng)
+        M, N, K, layout = c["M"], c["N"], c["K"], c["layout"]
+        A, B = make_inputs(M, N, K, layout, c["in_dtype"], "int", seed=6100 + i)
+        C0 = int_c(M, N, c["out"], 6200 + i)
+        kw = dict(alpha=c["alpha"], beta=c["beta"], col_major=bool(c["col_major"]), c_init=C0)
+        if i % 2 == 0:  # per-tensor scales, gemm_run_ex
+            got, guard = with_options(g, c, lambda: run8(g, A, B, layout, c["out"], scale_a=0.5, scale_b=2.0, **kw))
+            want = oracle.gemm_typed(A, B, layout, c["in_dtype"], c["out"], alpha=factor(c["alpha"], 0.5, 2.0),
+                                     beta=c["beta"], Cin=C0)
+        else:  # E8M0 block scales, gemm_run_mx
+            sa, sb = scales(M, K, 2, seed=6300 + i), scales(N, K, 2, seed=6400 + i)
+            got, guard = with_options(g, c, lambda: run_mx(g, A, B, sa, sb, layout, c["out"], **kw))
+            want = oracle.gemm_blockscaled(A, B, sa, sb, layout, c["in_dtype"], c["out"], alpha=c["alpha"],
+                                           beta=c["beta"], Cin=C0)
+        assert guard, f"write outside the C window: case {c}"
+        assert_exact(got, want, f"case {i} {c}")
+
+
+def test_random_sparse_operands(g):
+    from dense_tiled_gemm_04_gb300.workloads import prune_24
+    from test_gpu_sparse import compress, run_sp
+
+    rng = np.random.default_rng(7000)
+    for i in range(12):
+        c = draw_case(rng)
+        M, N, layout, dtype = c["M"], c["N"], c["layout"], c["dtype"]
+        K = 4 * max(1, c["K"] // 4)  # a 2:4 A needs K in groups of four
+        alpha, beta = float(rng.choice([1.0, 2.0])), float(rng.choice([0.0, -1.0]))
+        col_major = int(rng.integers(0, 2))
+        A, B = make_inputs(M, N, K, layout, dtype, "int", seed=7100 + i)
+        A = prune_24(A, seed=7200 + i)
+        C0 = int_codes(M, N, dtype, 7300 + i)
+        Ac, meta, bad = compress(g, A)
+        assert bad == 0
+        got, guard = with_options(g, c, lambda: run_sp(g, Ac, meta, B, layout, dtype, alpha=alpha, beta=beta,
+                                                       col_major=bool(col_major), c_init=C0))
+        assert guard, f"write outside the C window: case {c}"
+        assert_exact(got, oracle.gemm_axpby(A, B, layout, dtype, alpha, beta, C0), f"case {i} {c}")
