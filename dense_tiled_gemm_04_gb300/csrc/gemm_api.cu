@@ -226,7 +226,7 @@ gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int 
             cudaLaunchConfig_t cfg;
             std::memset(&cfg, 0, sizeof(cfg));
             cfg.gridDim = dim3(static_cast<unsigned>(kc.cluster * (dev.num_sms / kc.cluster)), 1, 1);
-            cfg.blockDim = dim3(dtg::kThreads, 1, 1);
+            cfg.blockDim = dim3(static_cast<unsigned>(kc.threads), 1, 1);
             cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
             cudaLaunchAttribute attr;
             attr.id = cudaLaunchAttributeClusterDimension;
@@ -307,7 +307,7 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     }
     if (plan->dp_tiles == tiles && tiles < units) units = tiles;  // whole tiles only: no idle units
     plan->grid = units * kc.cluster;
-    plan->threads = dtg::kThreads;
+    plan->threads = kc.threads;
     plan->smem_bytes = kc.smem;
 }
 
@@ -361,16 +361,15 @@ gemm_status_t validate(gemm_handle_t h, const void* A, const void* B, const void
 int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N, int64_t K,
                   gemm_dtype_t dtype, int family)
 {
-    // Sparse kernels: the CTA pair where the dense choice would take it (or when asked), else
-    // the one-CTA 128 x 256 tile.  Block-scaled kernels: the one-CTA tile unless the pair is
-    // asked for (measured: the pair gains ~2 % at 8192^3 and loses ~7 % at 4096^3).  The pair
+    // Sparse and block-scaled kernels: the CTA pair where the dense choice would take it (or
+    // when asked), else the one-CTA 128 x 256 tile (block-scaled, measured with the scale
+    // warp: the pair gains 6-9 % at 8192^3 and 5-12 % at 6144^3, ties at 4096^3).  The pair
     // addresses the side data by rows of 16 bytes with 32-bit TMA coordinates, which must fit.
-    // The multicast configuration (two pairs sharing B) exists for 16-bit dense operands; the
-    // others run the pair in its place.
+    // The multicast configuration (two pairs sharing B) exists for 16-bit dense operands and
+    // 2:4-sparse A; the others run the pair in its place.
     int config = pick_config(o, dev, M, N);
     if (config == GEMM_CONFIG_512x256 && (family == kBlockScaled || is_f8(dtype))) config = GEMM_CONFIG_256x256;
-    if (family == kBlockScaled && o.config != GEMM_CONFIG_256x256 && o.config != GEMM_CONFIG_512x256)
-        config = GEMM_CONFIG_128x256;
+    if (family == kBlockScaled && config == GEMM_CONFIG_128x128) config = GEMM_CONFIG_128x256;
     if (family != kDense) {
         const int64_t lim = int64_t(1) << 31;
         const bool rows_fit =
@@ -491,7 +490,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     cudaLaunchConfig_t cfg;
     std::memset(&cfg, 0, sizeof(cfg));
     cfg.gridDim = dim3(static_cast<unsigned>(plan.grid), 1, 1);
-    cfg.blockDim = dim3(dtg::kThreads, 1, 1);
+    cfg.blockDim = dim3(static_cast<unsigned>(kc.threads), 1, 1);
     cfg.dynamicSmemBytes = static_cast<size_t>(kc.smem);
     cfg.stream = stream;
     // Programmatic dependent launch: the grid may be scheduled while the stream's previous

@@ -25,6 +25,7 @@ struct KernelChoice {
     int cluster;    // CTAs per cluster
     const void* fn;
     int smem;
+    int threads = kThreads;  // per CTA (kThreadsMX for the block-scaled kernels)
 };
 
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN>
@@ -32,7 +33,7 @@ KernelChoice one_cta_choice(int config)
 {
     return {config, kBM, BN, BN, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK, STAGES, 1,
             reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, STAGES, IN, OUT_BF16, NN, 1>),
-            KernelLayout<BN, STAGES, IN, false>::S::kAlloc};
+            KernelLayout<BN, STAGES, IN, false>::S::kAlloc, Operand<IN>::kMX ? kThreadsMX : kThreads};
 }
 
 template <int IN, bool OUT_BF16, bool NN>

@@ -174,8 +174,9 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
  * K elements, and scales in E8M0 (8-bit exponents; 255 is NaN): tcgen05's block-scaled MMA
  * applies them inside the contraction, so no separate dequantisation pass runs.
  *   - args: as for gemm_run_ex, with dtype E4M3 or E5M2 (anything else: INVALID_ARG).
- *     Configurations: the one-CTA 128 x 256 tile, or the 256 x 256 CTA pair when
- *     GEMM_OPT_CONFIG asks for GEMM_CONFIG_256x256.
+ *     Configurations: the 256 x 256 CTA pair where gemm_run would take a pair tile (at least
+ *     one pair tile per pair of SMs), else the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask
+ *     for either (GEMM_CONFIG_256x256 / _512x256: the pair; _128x256 / _128x128: one CTA).
  *   - sfa: the exponents ea of A (M x ceil(K/32)), sfb: those of B (one row per column n of
  *     Beff, N x ceil(K/32)), both device pointers, 16-byte aligned, in the chunked layout that
  *     gemm_mx_pack_scales writes (gemm_mx_scale_bytes(M, K) and (N, K) bytes).  Unused when
@@ -258,7 +259,7 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
 gemm_status_t gemm_sync_status(gemm_handle_t h, void* stream);
 
 /* Details of the last watchdog expiry seen by gemm_sync_status / gemm_run_host:
- * info[0] = 1 (timeout), info[1] = role (0 producer, 1 mma, 2 epilogue, 3 drain),
+ * info[0] = 1 (timeout), info[1] = role (0 producer, 1 mma, 2 epilogue, 3 drain, 4 scale copies),
  * info[2] = CTA index, info[3] = tile index * 65536 + K block.  Zeros if none. */
 gemm_status_t gemm_error_info(gemm_handle_t h, int32_t info[4]);
 
