@@ -73,12 +73,13 @@ namespace dtg {
 constexpr int kBM = 128;          // accumulator rows per CTA (one TMEM lane per row)
 constexpr int kRowBytes = 128;    // K bytes per operand row of a ring stage (one 128-byte swizzle row)
 constexpr int kThreads = 192;     // 6 warps
-constexpr int kThreadsMX = 224;   // block-scaled kernels: a 7th warp copies each stage's scales into TMEM
+constexpr int kThreadsSide = 224; // block-scaled and 2:4-sparse kernels: a 7th warp copies each
+                                  // stage's side data (scales, metadata) into TMEM
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
 constexpr int kEpiWarp0 = 2;
 constexpr int kEpiWarps = 4;
-constexpr int kScaleWarp = 6;     // block-scaled kernels only
+constexpr int kSideWarp = 6;      // block-scaled and 2:4-sparse kernels only
 constexpr int kEpiCols = 64;                        // columns per staged TMA store box
 constexpr int kStgBytes = 32 * kEpiCols * 2;        // one warp's 32 x 64 box, 4 KB
 constexpr uint32_t kWaitSleepNs = 20000;           // longest single suspension of a waiting thread
@@ -130,7 +131,7 @@ constexpr int kMetaHalfBytes = 2048;
 constexpr int kMetaTmemStride = 8;  // TMEM columns between the metadata of consecutive MMAs
 
 // Error-word roles.
-constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3, kRoleScale = 4;
+constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleDrain = 3, kRoleSide = 4;
 
 struct KernelParams {
     int32_t M, N, K;
@@ -580,7 +581,7 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
 // of a CTA-pair kernel seen as rows of 16 bytes -- the metadata chunks (sparse), or the A and
 // the B scale chunks (block-scaled); unused otherwise.
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, int CLUSTER>
-__global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
+__global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? kThreadsSide : kThreads, 1)
     gemm_tcgen05_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                         const __grid_constant__ CUtensorMap tmC, const __grid_constant__ CUtensorMap tmS,
                         const __grid_constant__ CUtensorMap tmS2, const KernelParams p)
@@ -617,7 +618,7 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
     auto accf_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + b); };
     auto acce_bar = [&](int b) { return bar0 + 8u * (2 * STAGES + 2 + b); };
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
-    auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };  // block-scaled: scales in TMEM
+    auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };  // side data of stage s in TMEM
     const uint32_t sdrain_bar = bar0 + 8u * (3 * STAGES + 5);
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int32_t* const abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMiscOff + 4);
@@ -644,7 +645,7 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
             ptx::mbar_init(acce_bar(b), kEpiWarps * kRanks);
         }
         ptx::mbar_init(drain_bar, 1);
-        if constexpr (T::kMX) {
+        if constexpr (kSide) {
             for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sfr_bar(s), 1);
             ptx::mbar_init(sdrain_bar, 1);
         }
@@ -839,10 +840,10 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    // Block-scaled kernels wait for the stage's scales to be in TMEM (the
-                    // scale warp copies them once the stage's data is in); the others for the
-                    // stage's data.
-                    if (!wd.wait(T::kMX ? sfr_bar(stage) : full_bar(stage), phase, kRoleMma, tile, kb)) {
+                    // Block-scaled and sparse kernels wait for the stage's side data to be in
+                    // TMEM (the side warp copies it once the stage's data is in); the others
+                    // for the stage's data.
+                    if (!wd.wait(kSide ? sfr_bar(stage) : full_bar(stage), phase, kRoleMma, tile, kb)) {
                         aborted = true;
                         break;
                     }
@@ -852,27 +853,8 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
                     // Block scales of this stage in TMEM: A at sf_tmem, B from sf_tmem + 4.
                     uint32_t sf_tmem = 0;
                     if constexpr (T::kMX) sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
-                    // Sparsity metadata of this stage: per MMA k, 128 rows x 16 bytes -> TMEM lanes
-                    // 0-127, columns sf_tmem + 8k .. + 3 (8-column aligned).  The addresses are
-                    // checked against that alignment; a violation is reported, not issued.
-                    if constexpr (T::kSparse) {
-                        const uint32_t col = static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
-                        const uint32_t meta_smem = base + L::kSfOff + stage * L::kSfBytes;
-                        if ((col % kMetaTmemStride) != 0 || (meta_smem & 127u) != 0) {
-                            wd.fail(kRoleMma, tile, kb);
-                            aborted = true;
-                            break;
-                        }
-                        sf_tmem = tmem_base + col;
-#pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const uint64_t d = smem_desc_plain(meta_smem + h * kMetaHalfBytes, 0, 128);
-                            if constexpr (PAIR)
-                                ptx::tmem_cp_128x128b_pair(sf_tmem + h * kMetaTmemStride, d);
-                            else
-                                ptx::tmem_cp_128x128b(sf_tmem + h * kMetaTmemStride, d);
-                        }
-                    }
+                    // Sparsity metadata of this stage in TMEM: MMA k's at sf_tmem + 8 k.
+                    if constexpr (T::kSparse) sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
 #pragma unroll
                     for (int k = 0; k < T::kStageK / T::kMmaK; ++k) {
                         // A (K-major): the k-th K slice starts 32 B further along each row;
@@ -945,15 +927,17 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
             }
         }
         __syncwarp();
-    } else if (T::kMX && warp == kScaleWarp) {
+    } else if (kSide && warp == kSideWarp) {
         if (lane == 0 && leader) {
-            // ---------------------------------------------------------------- scale copies
-            // Block-scaled kernels: once a stage's data is in, its scale chunks go from shared
-            // memory into the stage's TMEM columns (4 per chunk: A's, then B's) and a commit
-            // tells the MMA thread they are there.  Issued by the MMA thread itself, the three
-            // copies per stage held its MMAs back (measured: ~15 % of the tensor pipe's time);
-            // from this warp they overlap them.  The stage is released (empty barrier) only
-            // after the MMAs that follow these copies, so no copy outlives its source.
+            // ---------------------------------------------------------------- side data
+            // Block-scaled and sparse kernels: once a stage's data is in, its side data goes
+            // from shared memory into the stage's TMEM columns -- the scale chunks (4 columns
+            // each: A's, then B's) or the two metadata halves (one 8-column block per MMA) --
+            // and a commit tells the MMA thread it is there.  Issued by the MMA thread itself,
+            // these copies held its MMAs back (measured: three copies per stage cost ~15 % of
+            // the tensor pipe's time); from this warp they overlap the MMAs.  The stage is
+            // released (empty barrier) only after the MMAs that follow the copies, so no copy
+            // outlives its source.
             int stage = 0;
             uint32_t phase = 0;
             bool aborted = false;
@@ -962,20 +946,40 @@ __global__ void __launch_bounds__(Operand<IN>::kMX ? kThreadsMX : kThreads, 1)
             int kb0, kb1;
             while (!aborted && it.next(p, tile, kb0, kb1)) {
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!wd.wait(full_bar(stage), phase, kRoleScale, tile, kb)) {
+                    if (!wd.wait(full_bar(stage), phase, kRoleSide, tile, kb)) {
                         aborted = true;
                         break;
                     }
                     ptx::tc_fence_after_sync();
-                    const uint32_t sf_tmem = tmem_base + static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
+                    const uint32_t col = static_cast<uint32_t>(kSfTmemCol + stage * kSideCols);
+                    const uint32_t sf_tmem = tmem_base + col;
                     const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
+                    if constexpr (T::kMX) {
 #pragma unroll
-                    for (int c = 0; c < kSfChunks; ++c) {
-                        const uint64_t d = smem_desc_plain(sf + c * kSfChunkBytes, 0, 128);
-                        if constexpr (PAIR)
-                            ptx::tmem_cp_32x128b_warpx4_pair(sf_tmem + 4 * c, d);
-                        else
-                            ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, d);
+                        for (int c = 0; c < kSfChunks; ++c) {
+                            const uint64_t d = smem_desc_plain(sf + c * kSfChunkBytes, 0, 128);
+                            if constexpr (PAIR)
+                                ptx::tmem_cp_32x128b_warpx4_pair(sf_tmem + 4 * c, d);
+                            else
+                                ptx::tmem_cp_32x128b_warpx4(sf_tmem + 4 * c, d);
+                        }
+                    } else {
+                        // Per MMA k, 128 rows x 16 bytes -> TMEM lanes 0-127, columns
+                        // sf_tmem + 8k .. + 3 (8-column aligned).  The addresses are checked
+                        // against that alignment; a violation is reported, not issued.
+                        if ((col % kMetaTmemStride) != 0 || (sf & 127u) != 0) {
+                            wd.fail(kRoleSide, tile, kb);
+                            aborted = true;
+                            break;
+                        }
+#pragma unroll
+                        for (int h = 0; h < 2; ++h) {
+                            const uint64_t d = smem_desc_plain(sf + h * kMetaHalfBytes, 0, 128);
+                            if constexpr (PAIR)
+                                ptx::tmem_cp_128x128b_pair(sf_tmem + h * kMetaTmemStride, d);
+                            else
+                                ptx::tmem_cp_128x128b(sf_tmem + h * kMetaTmemStride, d);
+                        }
                     }
                     if constexpr (PAIR)
                         ptx::mma_commit_pair_mc(sfr_bar(stage), static_cast<uint16_t>(1u << crank));

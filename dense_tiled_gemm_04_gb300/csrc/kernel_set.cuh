@@ -25,7 +25,7 @@ struct KernelChoice {
     int cluster;    // CTAs per cluster
     const void* fn;
     int smem;
-    int threads = kThreads;  // per CTA (kThreadsMX for the block-scaled kernels)
+    int threads = kThreads;  // per CTA (kThreadsSide for the block-scaled and sparse kernels)
 };
 
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN>
@@ -33,7 +33,8 @@ KernelChoice one_cta_choice(int config)
 {
     return {config, kBM, BN, BN, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK, STAGES, 1,
             reinterpret_cast<const void*>(&gemm_tcgen05_kernel<BN, STAGES, IN, OUT_BF16, NN, 1>),
-            KernelLayout<BN, STAGES, IN, false>::S::kAlloc, Operand<IN>::kMX ? kThreadsMX : kThreads};
+            KernelLayout<BN, STAGES, IN, false>::S::kAlloc,
+            (Operand<IN>::kMX || Operand<IN>::kSparse) ? kThreadsSide : kThreads};
 }
 
 template <int IN, bool OUT_BF16, bool NN>

@@ -13,7 +13,7 @@ KernelChoice mx_choice(int config)
         return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kMxPairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kMxPairStages, IN, OUT_BF16, NN, 2>),
-                KernelLayout<256, kMxPairStages, IN, true>::S::kAlloc, kThreadsMX};
+                KernelLayout<256, kMxPairStages, IN, true>::S::kAlloc, kThreadsSide};
     return one_cta_choice<256, 4, IN, OUT_BF16, NN>(1);
 }
 

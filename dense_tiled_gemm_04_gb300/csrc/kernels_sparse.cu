@@ -15,12 +15,12 @@ KernelChoice sparse_choice(int config)
         return {config, 4 * kBM, 256, 64, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kSparsePairStages, 4,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, 4>),
-                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc};
+                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc, kThreadsSide};
     if (config == 3)  // GEMM_CONFIG_256x256
         return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kSparsePairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, 2>),
-                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc};
+                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc, kThreadsSide};
     return one_cta_choice<256, 4, IN, BF16, NN>(1);
 }
 }  // namespace

@@ -259,7 +259,7 @@ gemm_status_t gemm_run_host(gemm_handle_t h, const void* A, const void* B, void*
 gemm_status_t gemm_sync_status(gemm_handle_t h, void* stream);
 
 /* Details of the last watchdog expiry seen by gemm_sync_status / gemm_run_host:
- * info[0] = 1 (timeout), info[1] = role (0 producer, 1 mma, 2 epilogue, 3 drain, 4 scale copies),
+ * info[0] = 1 (timeout), info[1] = role (0 producer, 1 mma, 2 epilogue, 3 drain, 4 side-data copies),
  * info[2] = CTA index, info[3] = tile index * 65536 + K block.  Zeros if none. */
 gemm_status_t gemm_error_info(gemm_handle_t h, int32_t info[4]);
 
