@@ -362,11 +362,12 @@ int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int
                   gemm_dtype_t dtype, int family)
 {
     // Sparse and block-scaled kernels: the CTA pair where the dense choice would take it (or
-    // when asked), else the one-CTA 128 x 256 tile (block-scaled, measured with the scale
-    // warp: the pair gains 6-9 % at 8192^3 and 5-12 % at 6144^3, ties at 4096^3).  The pair
-    // addresses the side data by rows of 16 bytes with 32-bit TMA coordinates, which must fit.
-    // The multicast configuration (two pairs sharing B) exists for 16-bit dense operands and
-    // 2:4-sparse A; the others run the pair in its place.
+    // when asked), else the one-CTA 128 x 256 tile (measured with the side-data warp and
+    // 128-byte side-data rows: block-scaled, the pair gains 6-9 % at 8192^3, 5-12 % at 6144^3,
+    // ties at 4096^3; sparse at 8192^3, the pair 2236 TF/s, two pairs sharing B 2140).  The pair
+    // addresses the side data by rows of kSideRowBytes with 32-bit TMA coordinates, which must fit.
+    // The multicast configuration (two pairs sharing B, on request) exists for 16-bit dense
+    // operands and 2:4-sparse A; the others run the pair in its place.
     int config = pick_config(o, dev, M, N);
     if (config == GEMM_CONFIG_512x256 && (family == kBlockScaled || is_f8(dtype))) config = GEMM_CONFIG_256x256;
     if (family == kBlockScaled && config == GEMM_CONFIG_128x128) config = GEMM_CONFIG_128x256;
@@ -374,15 +375,11 @@ int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int
         const int64_t lim = int64_t(1) << 31;
         const bool rows_fit =
             family == kSparse24
-                ? cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / 16) < lim
-                : (M > N ? cdiv(M, dtg::kBM) : cdiv(N, dtg::kBM)) * cdiv(K, 128) * (dtg::kSfChunkBytes / 16) < lim;
+                ? cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / dtg::kSideRowBytes) < lim
+                : (M > N ? cdiv(M, dtg::kBM) : cdiv(N, dtg::kBM)) * cdiv(K, 128) * (dtg::kSfChunkBytes / dtg::kSideRowBytes) <
+                      lim;
         config = ((config == GEMM_CONFIG_256x256 || config == GEMM_CONFIG_512x256) && rows_fit) ? config
                                                                                                : GEMM_CONFIG_128x256;
-        // AUTO, sparse A, many pair tiles: two pairs sharing B (measured +4-7 % at 8192^3, even
-        // at 4096^3, where each cluster gets fewer than 8 items).
-        if (family == kSparse24 && o.config == GEMM_CONFIG_AUTO && config == GEMM_CONFIG_256x256 &&
-            cdiv(M, 512) * cdiv(N, 256) >= 8 * (dev.num_sms / 4))
-            config = GEMM_CONFIG_512x256;
     }
     return config;
 }
@@ -469,21 +466,24 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.sfb_blocks = static_cast<int32_t>(cdiv(N, dtg::kSfChunkRows));
     kp.meta = static_cast<const uint8_t*>(ep.meta);
 
-    // Side data of a CTA-pair kernel as rows of 16 bytes: the metadata chunks (a box of one
-    // chunk, 256 rows, per stage and CTA), or the A and B scale chunks (boxes of 32 rows).
+    // Side data of a CTA-pair kernel as rows of kSideRowBytes (128): the metadata chunks (a
+    // box of one chunk, 32 rows, per stage and CTA), or the A and B scale chunks (boxes of 4
+    // rows).  Wide rows keep each box a few long transfers instead of many 16-byte ones.
     CUtensorMap tS = tA, tS2 = tA;
     if (family == kSparse24 && kc.cluster >= 2) {
-        const uint64_t rows = static_cast<uint64_t>(cdiv(M, dtg::kBM) * cdiv(K, 64)) * (dtg::kMetaChunkBytes / 16);
-        if (!get_tmap(cache, ep.meta, 16, rows, 16, 16, dtg::kMetaChunkBytes / 16, kTmapBytes, &tS,
+        constexpr uint32_t kRb = dtg::kSideRowBytes;
+        const uint64_t rows = static_cast<uint64_t>(cdiv(M, dtg::kBM) * cdiv(K, 64)) * (dtg::kMetaChunkBytes / kRb);
+        if (!get_tmap(cache, ep.meta, kRb, rows, kRb, kRb, dtg::kMetaChunkBytes / kRb, kTmapBytes, &tS,
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
     if (family == kBlockScaled && kc.cluster >= 2) {
-        constexpr uint32_t kRows = dtg::kSfChunkBytes / 16;
+        constexpr uint32_t kRb = dtg::kSideRowBytes;
+        constexpr uint32_t kRows = dtg::kSfChunkBytes / kRb;
         const uint64_t rows_a = static_cast<uint64_t>(cdiv(M, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
         const uint64_t rows_b = static_cast<uint64_t>(cdiv(N, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
-        if (!get_tmap(cache, ep.sfa, 16, rows_a, 16, 16, kRows, kTmapBytes, &tS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !get_tmap(cache, ep.sfb, 16, rows_b, 16, 16, kRows, kTmapBytes, &tS2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (!get_tmap(cache, ep.sfa, kRb, rows_a, kRb, kRb, kRows, kTmapBytes, &tS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !get_tmap(cache, ep.sfb, kRb, rows_b, kRb, kRb, kRows, kTmapBytes, &tS2, CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
     void* args[] = {&tA, &tB, &tC, &tS, &tS2, &kp};

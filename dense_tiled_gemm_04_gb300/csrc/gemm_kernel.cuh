@@ -115,6 +115,9 @@ struct Operand {
 constexpr int kSfChunkBytes = 512;
 constexpr int kSfChunkRows = 128;
 constexpr int kSfTmemCol = 256;  // first TMEM column of the per-stage side data (after one 256-column accumulator)
+// CTA-pair kernels load side data (scale chunks, metadata chunks) through tensor maps that view
+// the chunked buffer as rows of this many bytes, so a chunk is a box of whole rows.
+constexpr int kSideRowBytes = 128;
 
 // 2:4 sparsity metadata travels in 4096-byte chunks: 128 rows of A by one ring stage (64 K).
 // The chunk holds one 2048-byte half per MMA of the stage (K [0, 32) and [32, 64) of the
@@ -578,7 +581,7 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
 // (a CTA pair) or 4 (two CTA pairs computing vertically adjacent tiles -- tile rows 2 r and
 // 2 r + 1 of one tile column -- that share their B boxes by TMA multicast: each CTA loads half
 // of its pair-rank's B box for both pairs, which halves the L2 reads of B).  tmS, tmS2: the side data
-// of a CTA-pair kernel seen as rows of 16 bytes -- the metadata chunks (sparse), or the A and
+// of a CTA-pair kernel seen as rows of kSideRowBytes -- the metadata chunks (sparse), or the A and
 // the B scale chunks (block-scaled); unused otherwise.
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, int CLUSTER>
 __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? kThreadsSide : kThreads, 1)
@@ -762,25 +765,25 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         }
                         if constexpr (T::kSparse) {
                             // This CTA's 128 rows: metadata chunk (row block, stage) -- one 1-D bulk
-                            // copy, or, in a pair, a TMA box of 256 rows of 16 bytes that completes
+                            // copy, or, in a pair, a TMA box of whole kSideRowBytes rows that completes
                             // on the leader's barrier like the A and B boxes.
                             const int64_t chunk = (tm * kRanks + rank) * p.num_kb + kb;
                             if constexpr (PAIR)
                                 load(base + L::kSfOff + stage * L::kSfBytes, &tmS, 0,
-                                     static_cast<int32_t>(chunk * (kMetaChunkBytes / 16)));
+                                     static_cast<int32_t>(chunk * (kMetaChunkBytes / kSideRowBytes)));
                             else
                                 ptx::bulk_load_1d(base + L::kSfOff + stage * L::kSfBytes,
                                                   p.meta + chunk * kMetaChunkBytes, kMetaChunkBytes, fb);
                         }
                         if constexpr (T::kMX) {
                             // This CTA's A rows' chunk and the tile's B chunks: 1-D bulk copies,
-                            // or, in a pair, TMA boxes of 32 rows of 16 bytes completing on the
+                            // or, in a pair, TMA boxes of whole kSideRowBytes rows completing on the
                             // leader's barrier.
                             const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
                             const int64_t g = kb;
                             const int64_t ca = (tm * kRanks + rank) * p.num_kb + g;
                             const int64_t nb0 = tn * (BN / kSfChunkRows);
-                            constexpr int kRows = kSfChunkBytes / 16;
+                            constexpr int kRows = kSfChunkBytes / kSideRowBytes;
                             if constexpr (PAIR) {
                                 load(sf, &tmS, 0, static_cast<int32_t>(ca * kRows));
                                 for (int j = 0; j < sf_b_chunks; ++j)

@@ -204,9 +204,9 @@ gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* 
  *     (the pattern of padding rows and groups is (0, 1)); otherwise the result is undefined.
  *   - dtype F16 or BF16 with out_dtype == dtype; K a multiple of 4 (else UNSUPPORTED); B, C,
  *     alpha, beta, c_col_major and the status codes as in gemm_run_ex.  K == 0 gives C = beta
- *     * C and ignores meta.  Configurations: where gemm_run would take the CTA pair, two pairs
- *     sharing B (GEMM_CONFIG_512x256) when there are at least 8 such items per cluster, else the
- *     pair; otherwise the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask for any of them. */
+ *     * C and ignores meta.  Configurations: the CTA pair where gemm_run would take it, else
+ *     the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask for either, or for two pairs sharing
+ *     B (GEMM_CONFIG_512x256). */
 gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream);
 
 /* Bytes of the chunked sparsity metadata for M rows and K: ceil(M/128) * ceil(K/64) * 4096

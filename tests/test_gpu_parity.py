@@ -264,12 +264,12 @@ def test_several_tiles_per_cta_and_raster_groups(g, config, layout):
 
 
 def test_plan_kind_reports_the_launch_of_each_operand_kind(g):
-    # What gemm_run_sp / gemm_run_mx launch for 8192^3 TN by default: two CTA pairs sharing B
-    # (7-stage ring, 7 warps) for a 2:4-sparse A, the CTA pair (6 stages, 7 warps) for block
-    # scales; a small block-scaled problem takes the one-CTA 128 x 256 tile (4 stages).
+    # What gemm_run_sp / gemm_run_mx launch for 8192^3 TN by default: the CTA pair (7-stage
+    # ring, 7 warps) for a 2:4-sparse A, the CTA pair (6 stages, 7 warps) for block scales; a
+    # small block-scaled problem takes the one-CTA 128 x 256 tile (4 stages).
     sp = g.plan(8192, 8192, 8192, "TN", "bf16", "sparse24")
     assert (sp["config"], sp["cluster"], sp["bm"], sp["bn"], sp["stages"], sp["threads"]) == \
-        (native.CONFIG_512x256, 4, 512, 256, 7, 224)
+        (native.CONFIG_256x256, 2, 256, 256, 7, 224)
     mx = g.plan(8192, 8192, 8192, "TN", "e4m3", "block_scaled")
     assert (mx["config"], mx["cluster"], mx["bm"], mx["bn"], mx["stages"], mx["threads"]) == \
         (native.CONFIG_256x256, 2, 256, 256, 6, 224)
