@@ -16,7 +16,11 @@
 //                 tcgen05.commit releases the stage; after the item's last K block a commit
 //                 marks the accumulator full.  The first MMA of an item overwrites (the
 //                 zero-filled accumulator of §2), later ones add.  Block scales and sparsity
-//                 metadata arrive with the stage and are copied into TMEM (tcgen05.cp) first.
+//                 metadata arrive with the stage; the MMA thread waits until warp 6 has
+//                 copied them into TMEM.
+//   warp 6        block-scaled and sparse kernels only (side data): per K block, once the
+//                 stage is in, tcgen05.cp of its scales or metadata into the stage's TMEM
+//                 columns, then a commit the MMA thread waits on.
 //   warps 2..5    epilogue: tcgen05.ld of the accumulator (each warp owns the 32 TMEM lanes
 //                 of its lane quadrant), C = alpha * acc + beta * C, fp32 -> fp16/bf16
 //                 round-to-nearest-even, staging in 128-byte-swizzled shared memory and a TMA
