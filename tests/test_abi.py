@@ -153,3 +153,35 @@ def test_sparse_entry_points_without_a_gpu(lib):
     so = lib.load()
     assert so.gemm_run_sp(None, None, None, None) == lib.ERR_INVALID_ARG
     assert so.gemm_sp_compress(None, None, 1, 4, 4, 0, None, 2, None, None, None) == lib.ERR_INVALID_ARG
+
+
+def header_enum_values():
+    """Every `NAME = value` inside the header's enum blocks (values are integer literals)."""
+    text = re.sub(r"/\*.*?\*/", "", open(HEADER).read(), flags=re.S)
+    values = {}
+    for body in re.findall(r"enum\s*\{(.*?)\}", text, flags=re.S):
+        for name, value in re.findall(r"(GEMM_\w+)\s*=\s*(\d+)", body):
+            values[name] = int(value)
+    return values
+
+
+def test_binding_constants_match_the_header(lib):
+    values = header_enum_values()
+    pairs = {
+        "GEMM_LAYOUT_NN": lib.LAYOUT_NN, "GEMM_LAYOUT_TN": lib.LAYOUT_TN,
+        "GEMM_DTYPE_F16": lib.DTYPE_F16, "GEMM_DTYPE_BF16": lib.DTYPE_BF16,
+        "GEMM_DTYPE_E4M3": lib.DTYPE_E4M3, "GEMM_DTYPE_E5M2": lib.DTYPE_E5M2,
+        "GEMM_OK": lib.OK, "GEMM_ERR_INVALID_ARG": lib.ERR_INVALID_ARG, "GEMM_ERR_UNSUPPORTED": lib.ERR_UNSUPPORTED,
+        "GEMM_ERR_ARCH": lib.ERR_ARCH, "GEMM_ERR_CUDA": lib.ERR_CUDA, "GEMM_ERR_TIMEOUT": lib.ERR_TIMEOUT,
+        "GEMM_OPT_CONFIG": lib.OPT_CONFIG, "GEMM_OPT_TIMEOUT_NS": lib.OPT_TIMEOUT_NS,
+        "GEMM_OPT_MAX_CTAS": lib.OPT_MAX_CTAS, "GEMM_OPT_RASTER_GROUP": lib.OPT_RASTER_GROUP,
+        "GEMM_OPT_FAULT_INJECT": lib.OPT_FAULT_INJECT, "GEMM_OPT_STREAM_K": lib.OPT_STREAM_K,
+        "GEMM_OPT_HOST_ROW_CHUNKS": lib.OPT_HOST_ROW_CHUNKS, "GEMM_OPT_HOST_COL_CHUNKS": lib.OPT_HOST_COL_CHUNKS,
+        "GEMM_CONFIG_AUTO": lib.CONFIG_AUTO, "GEMM_CONFIG_128x256": lib.CONFIG_128x256,
+        "GEMM_CONFIG_128x128": lib.CONFIG_128x128, "GEMM_CONFIG_256x256": lib.CONFIG_256x256,
+        "GEMM_CONFIG_512x256": lib.CONFIG_512x256,
+        "GEMM_KIND_DENSE": lib.KINDS["dense"], "GEMM_KIND_BLOCK_SCALED": lib.KINDS["block_scaled"],
+        "GEMM_KIND_SPARSE24": lib.KINDS["sparse24"],
+    }
+    assert set(pairs) <= set(values), sorted(set(pairs) - set(values))
+    assert {k: values[k] for k in pairs} == pairs
