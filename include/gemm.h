@@ -306,7 +306,10 @@ gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, in
  * synchronisation an allocation may cause, or a process already at its memory limit.
  *
  * Arguments and layouts are those of gemm_run (A, B, C device pointers; same checks and
- * status codes); the kernel, tile configuration and results are the same.  The only
+ * status codes), and so are the kernel and its tile configuration; the schedule takes whole
+ * tiles only (gemm_run may split the K blocks of a last, part-empty wave between CTAs), so
+ * the fp32 sums may run in another order: results agree within rounding, bit for bit on
+ * integer-valued inputs.  The only
  * scratch the kernel needs -- its 16-byte watchdog record -- lives in a 256-byte
  * file-scope __device__ array inside the library (every GPU that loads the library keeps
  * those 256 bytes until the process exits).  A call whose scratch need exceeded that
