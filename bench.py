@@ -8,9 +8,9 @@ E8M0 scales per 32 K elements, gemm_run_mx) or c4-sp (a 2:4-sparse A, gemm_run_s
 counted dense-equivalent, 2MNK, against twice the dense peak).
 
 One step = one full GEMM (the whole hot path: TMA ring, tcgen05 MMA, epilogue) on
-inputs resident in HBM.  Prints one JSON line (rank 0).  Under torchrun each rank runs
-its own independent GEMM of the same size (weak scaling; no collective on the data
-path); the timed region is bracketed by a barrier and the maximum over ranks is kept.
+inputs resident in HBM.  Prints one JSON line.  The library is a one-GPU library: with
+--gpus > 1, or under a launcher that starts more than one rank (WORLD_SIZE > 1), the
+benchmark refuses to run and exits with status 2.
 
 ``--impl reference`` times the CPU oracle (fp64 triple loop) on bounded samples of the
 same workload on the host cores: the slow reference arm, not a GPU implementation.
@@ -34,7 +34,12 @@ if ROOT not in sys.path:
 
 METRIC = "GEMM TFLOP/s at 1 GB300 and % of dense FP16/BF16 tensor roofline"
 WORKLOAD = "c4"
+# Roofline denominators when no measured peaks are present: one earlier measurement of a
+# cuBLAS bf16 GEMM and of a device copy on a GB300.
 FALLBACK_PEAKS = {"bf16_tflops": 1900.0, "hbm_gbs": 6800.0}
+# NVIDIA's published dense FP16/BF16 tensor rate of one GB300 (2.25 PFLOP/s; its larger figures
+# assume 2:4 sparsity).  Context only: the roofline uses the measured peaks.
+NOMINAL_DENSE_TFLOPS = 2250.0
 L2_BYTES = 129 * 10**6        # GB300 L2
 FLUSH_BYTES = 512 * 2**20     # the buffer written between steps whose inputs fit in L2
 KERNEL_DIR = os.path.join("dense_tiled_gemm_04_gb300", "csrc")
@@ -94,90 +99,148 @@ def load_traffic(workload_key: str, plan: dict, path: str = os.path.join(ROOT, "
     return entry.get("dram_bytes_per_launch")
 
 
+# NVML clock-event reason bits (nvmlClocksEventReason*): the ones a bench line reports.
+NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown", 0x40: "hw_thermal_slowdown",
+                0x80: "hw_power_brake_slowdown"}
+NVML_CLOCK_SM = 1
+CLOCK_POLL_S = 0.002  # NVML is polled every 2 ms, so a 10 ms timed region still gets samples
+
+
+class NvmlReader:
+    """Reads the SM clock, its maximum, the power draw and the clock-event reasons of one GPU
+    through the driver's NVML library (ctypes; nothing to install).  Read-only: it changes no
+    setting of the GPU."""
+
+    def __init__(self, uuid: str = "", index: int = 0, lib=None):
+        import ctypes
+
+        self.ct = ctypes
+        self.lib = lib if lib is not None else ctypes.CDLL("libnvidia-ml.so.1")
+        if self.lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        self.handle = ctypes.c_void_p()
+        self.matched = "uuid"
+        u = uuid if uuid.startswith("GPU-") else "GPU-" + uuid
+        if not uuid or self.lib.nvmlDeviceGetHandleByUUID(u.encode(), ctypes.byref(self.handle)) != 0:
+            self.matched = "index"
+            if self.lib.nvmlDeviceGetHandleByIndex_v2(ctypes.c_uint(index), ctypes.byref(self.handle)) != 0:
+                raise OSError("no NVML handle for the device")
+        mx = ctypes.c_uint(0)
+        self.lib.nvmlDeviceGetMaxClockInfo(self.handle, NVML_CLOCK_SM, ctypes.byref(mx))
+        self.sm_max = float(mx.value)
+
+    def read(self):
+        """(SM MHz, power W or None, reason bitmask or None)."""
+        ct = self.ct
+        clk, pw, rs = ct.c_uint(0), ct.c_uint(0), ct.c_ulonglong(0)
+        if self.lib.nvmlDeviceGetClockInfo(self.handle, NVML_CLOCK_SM, ct.byref(clk)) != 0:
+            return None
+        power = pw.value / 1000.0 if self.lib.nvmlDeviceGetPowerUsage(self.handle, ct.byref(pw)) == 0 else None
+        fn = getattr(self.lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            getattr(self.lib, "nvmlDeviceGetCurrentClocksThrottleReasons")
+        reasons = rs.value if fn(self.handle, ct.byref(rs)) == 0 else None
+        return float(clk.value), power, reasons
+
+
+def summarize_clocks(samples, sm_max, t0: float, t1: float, source: str):
+    """Clock record of the samples (t, SM MHz, power W, reason bits) taken inside [t0, t1]."""
+    inside = [s for s in samples if t0 <= s[0] <= t1]
+    if not inside:
+        return {"sm_mhz": None, "sm_max_mhz": sm_max, "reasons": [], "samples": 0, "source": source,
+                "note": f"no sample fell inside the {1e3 * (t1 - t0):.1f} ms region"}
+    sm = [s[1] for s in inside]
+    pw = [s[2] for s in inside if s[2] is not None]
+    reasons = set()
+    for s in inside:
+        if s[3] is not None:
+            reasons.update(name for bit, name in NVML_REASONS.items() if s[3] & bit)
+    out = {"sm_mhz": statistics.median(sm), "sm_min_mhz": min(sm), "sm_max_mhz": sm_max,
+           "reasons": sorted(reasons), "samples": len(sm), "source": source}
+    if pw:
+        out["power_w_max"] = max(pw)
+    return out
+
+
 class ClockSampler:
-    """nvidia-smi clock/throttle sampling while the timed region runs."""
+    """Samples the GPU's clocks in a background thread while timed regions run: NVML every
+    CLOCK_POLL_S, or, without NVML, nvidia-smi every 50 ms."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    SMI_FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active")
 
-    def __init__(self, device_index: int):
-        self.dev = device_index
+    def __init__(self, uuid: str = "", index: int = 0, reader=None):
+        self.samples = []
+        self.sm_max = None
+        self.stop_flag = threading.Event()
+        self.thread = None
         self.proc = None
-        self.lines = []
-        self.t = None
+        self.reader = reader
+        self.source = "nvml"
+        if self.reader is None:
+            try:
+                self.reader = NvmlReader(uuid, index)
+            except OSError:
+                self.reader = None
+                self.source = "nvidia-smi"
+        if self.reader is not None:
+            self.sm_max = self.reader.sm_max
+            self.source = f"nvml ({getattr(self.reader, 'matched', 'uuid')}), every {CLOCK_POLL_S * 1e3:.0f} ms"
+        self.index = index
 
     def start(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.dev), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "50"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-        except (FileNotFoundError, OSError):
-            self.proc = None
-            return
-        self.t = threading.Thread(target=self._read, daemon=True)
-        self.t.start()
-
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append((time.perf_counter(), line.strip()))
-
-    def stop(self, t0: float, t1: float):
-        if not self.proc:
-            return None
-        self.proc.terminate()
-        try:
-            self.proc.wait(timeout=5)
-        except subprocess.TimeoutExpired:
-            self.proc.kill()
-        self.t.join(timeout=2)
-        sm, mx, pw, reasons = [], [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for ts, line in self.lines:
-            if not (t0 <= ts <= t1):
-                continue
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 8:
-                continue
+        if self.reader is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
+        else:
             try:
-                sm.append(float(parts[0]))
-                mx.append(float(parts[1]))
-                pw.append(float(parts[2]))
-            except ValueError:
+                self.proc = subprocess.Popen(
+                    ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_FIELDS}",
+                     "--format=csv,noheader,nounits", "-lms", "50"], stdout=subprocess.PIPE,
+                    stderr=subprocess.DEVNULL, text=True)
+            except (FileNotFoundError, OSError):
+                return
+            self.thread = threading.Thread(target=self._read_smi, daemon=True)
+        self.thread.start()
+
+    def _poll(self):
+        while not self.stop_flag.is_set():
+            r = self.reader.read()
+            if r is not None:
+                self.samples.append((time.perf_counter(), *r))
+            time.sleep(CLOCK_POLL_S)
+
+    def _read_smi(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            try:
+                sm, mx, pw, act = float(parts[0]), float(parts[1]), float(parts[2]), int(parts[3], 16)
+            except (ValueError, IndexError):
                 continue
-            for name, val in zip(names, parts[4:8]):
-                if val.lower().startswith("active"):
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "power_w_max": max(pw),
-                "reasons": sorted(reasons), "samples": len(sm)}
+            self.sm_max = mx
+            self.samples.append((time.perf_counter(), sm, pw, act))
+
+    def stop(self):
+        self.stop_flag.set()
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+        if self.thread:
+            self.thread.join(timeout=2)
+
+    def region(self, t0: float, t1: float):
+        return summarize_clocks(list(self.samples), self.sm_max, t0, t1, self.source)
 
 
-def dist_env():
-    rank = int(os.environ.get("RANK", "0"))
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    return rank, world, local
-
-
-def reduce_max(values, world, device=None):
-    """Max of per-rank floats over all ranks (identity when world == 1)."""
-    if world == 1:
-        return list(values)
-    import torch
-    import torch.distributed as dist
-
-    t = torch.tensor(values, dtype=torch.float64, device=device)
-    dist.all_reduce(t, op=dist.ReduceOp.MAX)
-    return t.tolist()
-
-
-def barrier(world):
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.barrier()
+def one_gpu_refusal(gpus: int, env=None):
+    """None when the run asks for one GPU and one process; otherwise the reason it is refused.
+    The library computes on one GPU: it has no multi-GPU path to measure."""
+    env = os.environ if env is None else env
+    world = int(env.get("WORLD_SIZE", "1"))
+    if gpus != 1 or world != 1:
+        return (f"bench.py measures a one-GPU library: --gpus {gpus} with WORLD_SIZE {world} is refused "
+                "(run it with --gpus 1, without a multi-process launcher)")
+    return None
 
 
 # ------------------------------------------------------------------ CPU oracle timing
@@ -234,9 +297,6 @@ def run_reference(args, w):
     import oracle
     from dense_tiled_gemm_04_gb300.workloads import workload_inputs
 
-    rank, world, _ = dist_env()
-    if rank != 0:
-        return 0
     oracle.build()
     A, B = workload_inputs(w)
     threads = oracle.max_threads()
@@ -339,7 +399,8 @@ def roofline_line(w, ms_step: float, peaks: dict, peak_src: str, traffic):
                 "tensor": {k: tensor[k] for k in ("achieved", "peak", "unit", "frac")}}
     else:
         line = dict(tensor, achieved_gbs=achieved_gbs)
-    line.update({"nominal_dense_peak_tflops": 2250.0 * ratio, "frac_of_nominal": achieved / (2250.0 * ratio),
+    line.update({"nominal_dense_peak_tflops": NOMINAL_DENSE_TFLOPS * ratio,
+                 "frac_of_nominal": achieved / (NOMINAL_DENSE_TFLOPS * ratio),
                  "algorithmic_flops_per_launch": flops, "algorithmic_bytes_per_launch": w.algorithmic_bytes})
     if "bf16_tflops_sustained" in peaks:
         line["frac_of_sustained"] = achieved / (ratio * float(peaks["bf16_tflops_sustained"]))
@@ -399,29 +460,44 @@ def make_step(g, native, torch, w, A, B, C, stream):
         "kind::mxf8f6f4.block_scale, E8M0 scales per 32 K"
 
 
+# Tensor-pipe rate per SM and clock for 16-bit operands: one 128 x 256 x 16 MMA (524,288
+# multiply-adds) every 128 clocks, measured with a one-thread issue loop on this GPU; 8-bit
+# operands and a 2:4-sparse A (dense-equivalent) count twice as many.  The minimum cycles of a
+# work unit's share of the tiles follow from it.
+MACS_PER_CLK_SM_16BIT = 4096
+SUSTAINED_S = 2.0  # length of the back-to-back sustained leg
+
+
+def cycle_figures(w, plan: dict, ms_step: float, sm_mhz):
+    """Clock-normalised view of a launch: SM cycles per launch and per output tile of one work
+    unit (a CTA, or a CTA pair), and the tensor pipe's minimum for that tile."""
+    if not sm_mhz:
+        return None
+    units = plan["grid"] // plan["cluster"]
+    tiles = plan["tiles_m"] * plan["tiles_n"]
+    cycles = ms_step * 1e-3 * sm_mhz * 1e6
+    rate = MACS_PER_CLK_SM_16BIT * (2 if (w.elem_bytes == 1 or w.sparse) else 1)
+    min_tile = plan["bm"] * plan["bn"] * w.K / (plan["cluster"] * rate)  # per SM of the unit
+    per_tile = cycles * units / tiles
+    return {"sm_mhz": sm_mhz, "cycles_per_launch": cycles, "cycles_per_tile": per_tile,
+            "min_cycles_per_tile": min_tile, "tensor_busy_est": min_tile / per_tile}
+
+
 def run_ours(args, w):
     import torch
 
     from dense_tiled_gemm_04_gb300 import build as lib_build
     from dense_tiled_gemm_04_gb300 import native
-    from dense_tiled_gemm_04_gb300.workloads import workload_inputs
+    from dense_tiled_gemm_04_gb300.workloads import TORCH_DTYPES, workload_inputs
 
-    rank, world, local = dist_env()
     if not torch.cuda.is_available():
         raise RuntimeError("bench.py needs a CUDA device")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=dev)
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
     lib_build.build()
-    g = native.Gemm(local)
+    g = native.Gemm(0)
     g.set_option(native.OPT_CONFIG, {"auto": native.CONFIG_AUTO, "128x256": native.CONFIG_128x256,
-                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256,
-                                     "512x256": native.CONFIG_512x256}[args.config])
-
-    from dense_tiled_gemm_04_gb300.workloads import TORCH_DTYPES
+                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256}[args.config])
 
     A_cpu, B_cpu = workload_inputs(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
@@ -433,44 +509,60 @@ def run_ours(args, w):
         step()
     torch.cuda.synchronize(dev)
 
-    sampler = ClockSampler(local)
+    props = torch.cuda.get_device_properties(dev)
+    sampler = ClockSampler(str(getattr(props, "uuid", "")), 0)
     sampler.start()
-    time.sleep(0.3)  # let the sampler start before the timed region
+    time.sleep(0.1)  # let the sampler start before the timed region
     # Inputs that fit in L2 would be served from it by the previous step: for those, every
     # timed step is preceded by a write of a buffer several times larger than L2 (outside
     # the step's own events), and the step time is the sum of the per-step event times.
     flush = w.algorithmic_bytes < L2_BYTES
     flush_buf = torch.empty(FLUSH_BYTES // 4, dtype=torch.int32, device=dev) if flush else None
-    barrier(world)
-    torch.cuda.synchronize(dev)
-    t_wall0 = time.perf_counter()
-    if flush:
-        evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-               for _ in range(args.steps)]
-        for i, (e0, e1) in enumerate(evs):
-            flush_buf.fill_(i)
-            e0.record(stream)
-            step()
-            e1.record(stream)
-    else:
-        ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        ev0.record(stream)
-        for _ in range(args.steps):
-            step()
-        ev1.record(stream)
-    torch.cuda.synchronize(dev)
-    t_wall1 = time.perf_counter()
-    barrier(world)
-    clocks = sampler.stop(t_wall0, t_wall1)
+
+    def timed(n):
+        """Run n steps; (ms per step by CUDA events on the launching stream, wall t0, t1)."""
+        torch.cuda.synchronize(dev)
+        t0 = time.perf_counter()
+        if flush:
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+            for i, (e0, e1) in enumerate(evs):
+                flush_buf.fill_(i)
+                e0.record(stream)
+                step()
+                e1.record(stream)
+        else:
+            ev0, ev1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            ev0.record(stream)
+            for _ in range(n):
+                step()
+            ev1.record(stream)
+        torch.cuda.synchronize(dev)
+        t1 = time.perf_counter()
+        ms = sum(e0.elapsed_time(e1) for e0, e1 in evs) if flush else ev0.elapsed_time(ev1)
+        return ms / n, t0, t1
+
+    # The timed region: exactly --steps steps.
+    ms_step, t_wall0, t_wall1 = timed(args.steps)
+    clocks = sampler.region(t_wall0, t_wall1)
+    # The sustained leg: the same step back to back for about SUSTAINED_S seconds (the power
+    # limit of the part settles within them), with its own clock record.
+    sustained = None
+    if not args.no_sustained:
+        wall_per_step = (t_wall1 - t_wall0) / args.steps
+        n_sus = int(min(20000, max(args.steps, math.ceil(SUSTAINED_S / max(wall_per_step, 1e-6)))))
+        ms_sus, s0, s1 = timed(n_sus)
+        sus_clocks = sampler.region(s0, s1)
+        sustained = {"value": float(w.flops) / (ms_sus * 1e-3) / 1e12, "unit": "TFLOP/s", "ms_per_step": ms_sus,
+                     "steps": n_sus, "seconds": s1 - s0, "clocks": sus_clocks}
+    sampler.stop()
     st = g.sync_status(stream)
     if st != native.OK:
         raise native.GemmError(st, "watchdog")
-    ms_total = sum(e0.elapsed_time(e1) for e0, e1 in evs) if flush else ev0.elapsed_time(ev1)
     del flush_buf
-    ms_total = reduce_max([ms_total], world, dev)[0]
-    ms_step = ms_total / args.steps
     flops = float(w.flops)
-    value = flops * world / (ms_step * 1e-3) / 1e12
+    value = flops / (ms_step * 1e-3) / 1e12
+    if not clocks.get("samples") and sustained and sustained["clocks"].get("samples"):
+        clocks["note"] += "; the sustained leg's clock record is the nearest one"
 
     # End to end through the public C ABI on pinned host buffers: H2D of A and B, the
     # kernel, D2H of C, synchronised every step.
@@ -483,7 +575,6 @@ def run_ours(args, w):
         devs = step_inputs
         Ch = torch.empty(C.shape, dtype=C.dtype).pin_memory()
         e2e_steps = max(3, min(args.steps, 20))
-        barrier(world)
         torch.cuda.synchronize(dev)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
@@ -493,8 +584,7 @@ def run_ours(args, w):
             Ch.copy_(C, non_blocking=True)
             stream.synchronize()
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        e2e_s = reduce_max([e2e_s], world, dev)[0]
-        e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+        e2e = {"value": flops / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
                "h2d_bytes_per_step": int(sum(h_.numel() * h_.element_size() for h_ in hosts)),
                "d2h_bytes_per_step": int(Ch.numel() * 2)}
     elif not args.no_e2e:
@@ -503,59 +593,56 @@ def run_ours(args, w):
         e2e_steps = max(3, min(args.steps, 20))
         if g.run_host(Ah, Bh, Ch, w.layout, stream) != native.OK:  # sizes the device staging buffers
             raise RuntimeError("gemm_run_host failed")
-        barrier(world)
         t0 = time.perf_counter()
         for _ in range(e2e_steps):
             st = g.run_host(Ah, Bh, Ch, w.layout, stream)
             if st != native.OK:
                 raise native.GemmError(st, "gemm_run_host")
         e2e_s = (time.perf_counter() - t0) / e2e_steps
-        e2e_s = reduce_max([e2e_s], world, dev)[0]
-        e2e = {"value": flops * world / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
+        e2e = {"value": flops / e2e_s / 1e12, "unit": "TFLOP/s", "ms_per_step": e2e_s * 1e3,
                "h2d_bytes_per_step": int(Ah.numel() * 2 + Bh.numel() * 2), "d2h_bytes_per_step": int(Ch.numel() * 2)}
 
     peaks, peak_src = load_peaks()
     roofline = roofline_line(w, ms_step, peaks, peak_src, load_traffic(args.workload, plan))
+    roofline["cycles"] = cycle_figures(w, plan, ms_step, clocks.get("sm_mhz"))
+    if sustained:
+        sustained["frac_of_sustained_peak"] = roofline_line(w, sustained["ms_per_step"], peaks, peak_src,
+                                                            None).get("frac_of_sustained")
+        sustained["cycles"] = cycle_figures(w, plan, sustained["ms_per_step"], sustained["clocks"].get("sm_mhz"))
 
     cpu = None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    if not args.no_cpu_baseline:
         cpu = oracle_rows_sample(A_cpu, B_cpu, w, target_s=args.cpu_seconds)
 
     g.close()
-    if rank == 0:
-        line = {
-            "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype,
-            "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
-                    f"(torch CPU generator, seed {w.seed})"
-                    + (", E8M0 block scales uniform in 124..130 (numpy generator)" if w.scales == "block" else "")
-                    + (", A pruned to a seeded 2:4 pattern along K" if w.sparse else ""),
-            "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
-                       "accumulate": "fp32", "out": w.out_dtype,
-                       "kernel": f"tcgen05 {kind}, {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
-                                 f"ring, {plan['grid']} persistent CTAs"
-                                 + (f" in {plan['grid'] // plan['cluster']} CTA pairs (cta_group::2)"
-                                    if plan["cluster"] == 2 else
-                                    f" in {plan['grid'] // 4} clusters of four (two CTA pairs sharing B by multicast)"
-                                    if plan["cluster"] == 4 else ""),
-                       "l2": (f"inputs larger than L2 (A, B, C = {w.algorithmic_bytes / 2**20:.0f} MiB > 129 MB), "
-                              "no flush") if w.algorithmic_bytes >= L2_BYTES else
-                             (f"inputs fit in L2 ({w.algorithmic_bytes / 2**20:.1f} MiB): a {FLUSH_BYTES >> 20} MiB "
-                              "buffer is written before every step, outside its events (cold L2)"),
-                       "parallelism": f"{world} independent GEMMs, one per GPU" if world > 1 else "1 GPU",
-                       "plan": launch_shape(plan), "kernel_sha": kernel_fingerprint()},
-            "roofline": roofline,
-            "cpu_baseline": cpu,
-            "e2e": e2e,
-            "gpu_launches": args.steps,
-            "clocks": clocks,
-        }
-        print(json.dumps(line), flush=True)
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.destroy_process_group()
+    line = {
+        "metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": w.dtype,
+        "data": f"synthetic: seeded {w.dist} inputs x {w.scale:.3g} rounded to {w.dtype} "
+                f"(torch CPU generator, seed {w.seed})"
+                + (", E8M0 block scales uniform in 124..130 (numpy generator)" if w.scales == "block" else "")
+                + (", A pruned to a seeded 2:4 pattern along K" if w.sparse else ""),
+        "config": {"workload": w.name, "M": w.M, "N": w.N, "K": w.K, "layout": w.layout,
+                   "accumulate": "fp32", "out": w.out_dtype,
+                   "kernel": f"tcgen05 {kind}, {plan['bm']}x{plan['bn']}x{plan['bk']} tile, {plan['stages']}-stage "
+                             f"ring, {plan['grid']} persistent CTAs"
+                             + (f" in {plan['grid'] // plan['cluster']} CTA pairs (cta_group::2)"
+                                if plan["cluster"] == 2 else ""),
+                   "l2": (f"inputs larger than L2 (A, B, C = {w.algorithmic_bytes / 2**20:.0f} MiB > 129 MB), "
+                          "no flush") if w.algorithmic_bytes >= L2_BYTES else
+                         (f"inputs fit in L2 ({w.algorithmic_bytes / 2**20:.1f} MiB): a {FLUSH_BYTES >> 20} MiB "
+                          "buffer is written before every step, outside its events (cold L2)"),
+                   "parallelism": "1 GPU",
+                   "plan": launch_shape(plan), "kernel_sha": kernel_fingerprint()},
+        "roofline": roofline,
+        "sustained": sustained,
+        "cpu_baseline": cpu,
+        "e2e": e2e,
+        "gpu_launches": args.steps,
+        "clocks": clocks,
+    }
+    print(json.dumps(line), flush=True)
     return 0
 
 
@@ -570,11 +657,16 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="c1..c5, c4-e4m3, c4-mx, c4-sp (default c4, the headline workload)")
-    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256", "512x256"], default="auto",
+    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
                     help="kernel configuration (default: the library's own choice)")
+    ap.add_argument("--no-sustained", action="store_true", help="skip the back-to-back sustained leg")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    refusal = one_gpu_refusal(args.gpus)
+    if refusal:
+        print(refusal, file=sys.stderr, flush=True)
+        return 2
     from dense_tiled_gemm_04_gb300.workloads import WORKLOADS
 
     w = WORKLOADS[args.workload]

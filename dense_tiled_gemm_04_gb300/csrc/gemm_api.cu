@@ -25,7 +25,7 @@ constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int32_t kTmapBytes = -1;  // get_tmap element type: raw bytes (side data)
-constexpr int kNumSlots = 96;  // 4 configurations x 12 operand/output types x 2 layouts
+constexpr int kNumSlots = 72;  // 3 configurations x 12 operand/output types x 2 layouts
 constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
@@ -188,7 +188,7 @@ bool is_f8(gemm_dtype_t t) { return t == GEMM_DTYPE_E4M3 || t == GEMM_DTYPE_E5M2
 int elem_bytes(gemm_dtype_t t) { return is_f8(t) ? 1 : 2; }
 
 // Kernel families beyond the dense one: block-scaled 8-bit operands, 2:4-sparse A (each with
-// the one-CTA 128 x 256 tile, the CTA pair and -- sparse only -- two pairs sharing B).
+// the one-CTA 128 x 256 tile and the CTA pair).
 enum Family { kDense = 0, kBlockScaled = 1, kSparse24 = 2 };
 
 // `out` is the type of C: equal to `in` for 16-bit operands, F16 or BF16 for 8-bit ones.
@@ -207,8 +207,7 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
 
 int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
-    const int c = config == GEMM_CONFIG_512x256 ? 3
-                  : config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
+    const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
     const int f8 = 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0);  // 0..3
     const int types = family == kSparse24 ? 10 + in : (is_f8(in) ? (family == kBlockScaled ? 6 : 2) + f8 : in);
     return (c * 12 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
@@ -246,8 +245,7 @@ gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int 
 
 int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N)
 {
-    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256 ||
-        o.config == GEMM_CONFIG_512x256)
+    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256)
         return static_cast<int>(o.config);
     // AUTO: the 256 x 256 CTA-pair tile when there is at least one pair tile per pair of
     // SMs (it halves each SM's shared-memory traffic for B); otherwise the 128 x 256 tile
@@ -364,12 +362,9 @@ int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int
     // Sparse and block-scaled kernels: the CTA pair where the dense choice would take it (or
     // when asked), else the one-CTA 128 x 256 tile (measured with the side-data warp and
     // 128-byte side-data rows: block-scaled, the pair gains 6-9 % at 8192^3, 5-12 % at 6144^3,
-    // ties at 4096^3; sparse at 8192^3, the pair 2236 TF/s, two pairs sharing B 2140).  The pair
-    // addresses the side data by rows of kSideRowBytes with 32-bit TMA coordinates, which must fit.
-    // The multicast configuration (two pairs sharing B, on request) exists for 16-bit dense
-    // operands and 2:4-sparse A; the others run the pair in its place.
+    // ties at 4096^3; sparse: the pair 2236 TF/s at 8192^3).  The pair addresses the side data
+    // by rows of kSideRowBytes with 32-bit TMA coordinates, which must fit.
     int config = pick_config(o, dev, M, N);
-    if (config == GEMM_CONFIG_512x256 && (family == kBlockScaled || is_f8(dtype))) config = GEMM_CONFIG_256x256;
     if (family == kBlockScaled && config == GEMM_CONFIG_128x128) config = GEMM_CONFIG_128x256;
     if (family != kDense) {
         const int64_t lim = int64_t(1) << 31;
@@ -378,8 +373,7 @@ int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int
                 ? cdiv(M, dtg::kBM) * cdiv(K, 64) * (dtg::kMetaChunkBytes / dtg::kSideRowBytes) < lim
                 : (M > N ? cdiv(M, dtg::kBM) : cdiv(N, dtg::kBM)) * cdiv(K, 128) * (dtg::kSfChunkBytes / dtg::kSideRowBytes) <
                       lim;
-        config = ((config == GEMM_CONFIG_256x256 || config == GEMM_CONFIG_512x256) && rows_fit) ? config
-                                                                                               : GEMM_CONFIG_128x256;
+        config = (config == GEMM_CONFIG_256x256 && rows_fit) ? config : GEMM_CONFIG_128x256;
     }
     return config;
 }
@@ -1014,7 +1008,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     switch (opt) {
     case GEMM_OPT_CONFIG:
         if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128 &&
-            value != GEMM_CONFIG_256x256 && value != GEMM_CONFIG_512x256)
+            value != GEMM_CONFIG_256x256)
             return GEMM_ERR_INVALID_ARG;
         o.config = value;
         return GEMM_OK;

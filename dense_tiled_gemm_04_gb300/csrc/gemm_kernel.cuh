@@ -32,11 +32,9 @@
 // accumulator (their side data takes the other TMEM columns) and read it whole into registers
 // before storing, which hands it back to the MMA thread early.
 //
-// Clusters: CLUSTER = 1 (one CTA), 2 (a CTA pair) or 4 (two CTA pairs on vertically adjacent
-// tiles that share their B boxes by TMA multicast; each stage's empty barrier then counts both
-// pairs).
+// Clusters: CLUSTER = 1 (one CTA) or 2 (a CTA pair).
 //
-// CTA pairs (CLUSTER >= 2): a cluster of two CTAs on two SMs computes a 256 x BN tile with
+// CTA pairs (CLUSTER == 2): a cluster of two CTAs on two SMs computes a 256 x BN tile with
 // tcgen05.mma.cta_group::2 (M = 256).  This is the two-warpgroup kernel of the same page
 // (two workers share one B tile, each takes its own rows of A) moved to the SM level:
 // CTA r loads rows [128 r, 128 r + 128) of the A tile and B rows/columns
@@ -45,7 +43,7 @@
 // rows into that CTA's TMEM.  Per SM this halves the shared-memory bytes of B per MMA.
 //   full[s]      lives in the leader, armed with both CTAs' bytes; both CTAs' TMA loads
 //                complete on it (.cta_group::2 loads may signal the peer's barrier).
-//   empty[s], acc_full[b]  in both CTAs; the leader's commits arrive on both (multicast).
+//   empty[s], acc_full[b]  in both CTAs; each commit of the leader arrives on both.
 //   acc_empty[b] lives in the leader and counts the epilogue warps of both CTAs.
 //
 // Work schedule ("NineToothed GEMM 语法入门" §4: output tiles are independent, the K loop
@@ -338,14 +336,12 @@ __host__ __device__ constexpr uint32_t idesc_mma()
 struct Watchdog {
     volatile int32_t* abort_flag;  // shared memory
     const KernelParams* p;
-    uint32_t peer_abort[3] = {0, 0, 0};  // shared::cluster addresses of the other CTAs' flags, 0 = none
+    uint32_t peer_abort = 0;  // shared::cluster address of the peer CTA's flag (CTA pair), 0 = none
 
     __device__ __forceinline__ void fail(int role, int64_t tile, int kb) const
     {
         *abort_flag = 1;
-#pragma unroll
-        for (int i = 0; i < 3; ++i)
-            if (peer_abort[i]) ptx::st_shared_cluster_u32(peer_abort[i], 1u);
+        if (peer_abort) ptx::st_shared_cluster_u32(peer_abort, 1u);
         if (atomicCAS(p->err, 0, 1) == 0) {
             p->err[1] = role;
             p->err[2] = static_cast<int32_t>(blockIdx.x);
@@ -581,10 +577,8 @@ __device__ __forceinline__ int64_t sk_slot(const KernelParams& p, int64_t u, int
     return u * 2 + (sk_start(p.sk_base, p.sk_extra, u) >= tr * p.num_kb ? 0 : 1);
 }
 
-// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  CLUSTER: 1 (one CTA), 2
-// (a CTA pair) or 4 (two CTA pairs computing vertically adjacent tiles -- tile rows 2 r and
-// 2 r + 1 of one tile column -- that share their B boxes by TMA multicast: each CTA loads half
-// of its pair-rank's B box for both pairs, which halves the L2 reads of B).  tmS, tmS2: the side data
+// IN: operand type (see Operand); OUT_BF16: C is bf16 (else fp16).  CLUSTER: 1 (one CTA) or 2
+// (a CTA pair).  tmS, tmS2: the side data
 // of a CTA-pair kernel seen as rows of kSideRowBytes -- the metadata chunks (sparse), or the A and
 // the B scale chunks (block-scaled); unused otherwise.
 template <int BN, int STAGES, int IN, bool OUT_BF16, bool NN, int CLUSTER>
@@ -594,8 +588,8 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         const __grid_constant__ CUtensorMap tmS2, const KernelParams p)
 {
     using T = Operand<IN>;
-    constexpr bool PAIR = CLUSTER >= 2;
-    constexpr bool MC = CLUSTER == 4;          // two pairs sharing B (multicast)
+    static_assert(CLUSTER == 1 || CLUSTER == 2, "one CTA or a CTA pair");
+    constexpr bool PAIR = CLUSTER == 2;
     constexpr int kRanks = PAIR ? 2 : 1;       // CTAs per MMA (pair)
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
@@ -633,19 +627,16 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;  // rank in the cluster
-    const uint32_t rank = crank & 1u;         // rank in the pair; 0: the pair's leader (issues its MMAs)
-    const uint32_t pp = crank >> 1;           // pair within the cluster (MC)
-    const uint32_t lead_rank = crank & ~1u;   // cluster rank of this pair's leader
+    const uint32_t crank = PAIR ? ptx::cluster_ctarank() : 0u;  // rank in the pair; 0: the leader (issues its MMAs)
+    const uint32_t rank = crank;
     const bool leader = rank == 0;
-    static_assert(!MC || (!T::kMX && !T::kF8 && BN == 256), "multicast: 16-bit (dense or sparse) 256-wide pair tiles");
     const int64_t unit = PAIR ? static_cast<int64_t>(ptx::cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
     const int64_t units = PAIR ? static_cast<int64_t>(ptx::num_clusters_x()) : static_cast<int64_t>(gridDim.x);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             ptx::mbar_init(full_bar(s), 1);
-            ptx::mbar_init(empty_bar(s), MC ? 2 : 1);  // MC: both pairs release the stage
+            ptx::mbar_init(empty_bar(s), 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(accf_bar(b), 1);
@@ -689,11 +680,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
     Watchdog wd{abort_flag, &p};
     if constexpr (PAIR) {
         const uint32_t own = ptx::smem_addr(const_cast<int32_t*>(abort_flag));
-        wd.peer_abort[0] = ptx::mapa_shared(own, crank ^ 1u);
-        if constexpr (MC) {
-            wd.peer_abort[1] = ptx::mapa_shared(own, crank ^ 2u);
-            wd.peer_abort[2] = ptx::mapa_shared(own, crank ^ 3u);
-        }
+        wd.peer_abort = ptx::mapa_shared(own, crank ^ 1u);
     }
 
     if (warp == kProducerWarp) {
@@ -709,19 +696,19 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             while (it.next(p, tile, kb0, kb1)) {
                 int64_t tm, tn;
                 tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-                if constexpr (MC) tm = 2 * tm + pp;  // a cluster's item is two tile rows
                 const int32_t y_a = static_cast<int32_t>(tm * kTileM + rank * kBM);
                 const int32_t n_b = static_cast<int32_t>(tn * BN + rank * kBRows);
                 for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
                     if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
-                    if (p.fault_inject && crank == 0 && unit == 0 && loaded == 1) {
-                        // Test hook: leave this stage unarmed so the MMA thread's wait on it
-                        // runs out and the watchdog path is exercised.
+                    if (p.fault_inject && unit == 0 && loaded == 1) {
+                        // Test hook: every CTA of the first unit leaves this stage unloaded (and
+                        // the leader leaves it unarmed), so the MMA thread's wait on it runs out
+                        // and the watchdog path is exercised with no load of that stage in flight.
                     } else {
                         const uint32_t sa = base + stage * L::kStageBytes;
                         const uint32_t sb = sa + L::kABytes;
                         const int32_t k0 = kb * T::kStageK;
-                        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), lead_rank) : full_bar(stage);
+                        const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0u) : full_bar(stage);
                         // Block scales: the A chunk of this tile row and the B chunks of this
                         // tile's columns that exist (a ragged N may leave out the last).
                         int sf_b_chunks = 0;
@@ -747,22 +734,9 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         if constexpr (NN) {
                             // B stored K x N: boxes of one 128-byte row of N (kNBlock elements)
                             // by kStageK rows of K, kStageK * 128 bytes each.
-                            // MC: this CTA loads box pp of its pair-rank's two for both pairs.
-                            if constexpr (MC) {
-                                ptx::tma_load_2d_pair_mc(sb + pp * (T::kStageK * 128), &tmB,
-                                                         n_b + static_cast<int32_t>(pp) * T::kNBlock, k0, fb,
-                                                         static_cast<uint16_t>(0x5u << rank));
-                            } else {
 #pragma unroll
-                                for (int q = 0; q < kBRows / T::kNBlock; ++q)
-                                    load(sb + q * (T::kStageK * 128), &tmB, n_b + q * T::kNBlock, k0);
-                            }
-                        } else if constexpr (MC) {
-                            // B stored N x K, MC: rows [64 pp, 64 pp + 64) of this pair-rank's
-                            // kBRows rows, multicast to the same-rank CTA of both pairs.
-                            ptx::tma_load_2d_pair_mc(sb + pp * (kBRows / 2) * kRowBytes, &tmB, k0,
-                                                     n_b + static_cast<int32_t>(pp) * (kBRows / 2), fb,
-                                                     static_cast<uint16_t>(0x5u << rank));
+                            for (int q = 0; q < kBRows / T::kNBlock; ++q)
+                                load(sb + q * (T::kStageK * 128), &tmB, n_b + q * T::kNBlock, k0);
                         } else {
                             // B stored N x K: one box of kStageK (K) x kBRows (N rows).
                             load(sb, &tmB, k0, n_b);
@@ -906,7 +880,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                     }
                     // The stage is free once these MMAs finish (in both CTAs of a pair).
                     if constexpr (PAIR)
-                        ptx::mma_commit_pair_mc(empty_bar(stage), MC ? 0xF : 0x3);
+                        ptx::mma_commit_pair(empty_bar(stage), 0x3);
                     else
                         ptx::mma_commit_cta1(empty_bar(stage));
                     if (++stage == STAGES) {
@@ -916,7 +890,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                 }
                 if (aborted) break;
                 if constexpr (PAIR)
-                    ptx::mma_commit_pair_mc(accf_bar(acc), static_cast<uint16_t>(0x3u << lead_rank));  // accumulator complete
+                    ptx::mma_commit_pair(accf_bar(acc), 0x3);  // accumulator complete
                 else
                     ptx::mma_commit_cta1(accf_bar(acc));
                 if (++acc == kAccBufs) {
@@ -927,7 +901,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             if (aborted) {
                 // Let every MMA issued so far finish before the TMEM is released.
                 if constexpr (PAIR)
-                    ptx::mma_commit_pair_mc(drain_bar, static_cast<uint16_t>(1u << crank));
+                    ptx::mma_commit_pair(drain_bar, static_cast<uint16_t>(1u << crank));
                 else
                     ptx::mma_commit_cta1(drain_bar);
                 wd.drain(drain_bar, 0);
@@ -989,7 +963,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         }
                     }
                     if constexpr (PAIR)
-                        ptx::mma_commit_pair_mc(sfr_bar(stage), static_cast<uint16_t>(1u << crank));
+                        ptx::mma_commit_pair(sfr_bar(stage), static_cast<uint16_t>(1u << crank));
                     else
                         ptx::mma_commit_cta1(sfr_bar(stage));
                     if (++stage == STAGES) {
@@ -1000,7 +974,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             }
             // Every copy issued here completes before the TMEM is released.
             if constexpr (PAIR)
-                ptx::mma_commit_pair_mc(sdrain_bar, static_cast<uint16_t>(1u << crank));
+                ptx::mma_commit_pair(sdrain_bar, static_cast<uint16_t>(1u << crank));
             else
                 ptx::mma_commit_cta1(sdrain_bar);
             wd.drain(sdrain_bar, 0);
@@ -1025,7 +999,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             __syncwarp();
             if (lane == 0) {
                 if constexpr (PAIR)
-                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), lead_rank));
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(acce_bar(acc), 0u));
                 else
                     ptx::mbar_arrive(acce_bar(acc));
             }
@@ -1033,7 +1007,6 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
         while (it.next(p, tile, kb0, kb1)) {
             int64_t tm, tn;
             tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
-            if constexpr (MC) tm = 2 * tm + pp;
             const bool ok = wd.wait(accf_bar(acc), acc_phase, kRoleEpilogue, tile, -1);
             if (!epilogue_bar_and(ok)) break;  // all four epilogue warps leave together
             ptx::tc_fence_after_sync();

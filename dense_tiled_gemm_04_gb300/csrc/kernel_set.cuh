@@ -40,14 +40,7 @@ KernelChoice one_cta_choice(int config)
 template <int IN, bool OUT_BF16, bool NN>
 KernelChoice choice_for(int config)
 {
-    if constexpr (IN < 2) {
-        if (config == 4)  // GEMM_CONFIG_512x256: two pairs sharing B; a CTA loads 64 B rows (TN)
-            return {config, 4 * kBM, 256, 64, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
-                    kPairStages, 4,
-                    reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kPairStages, IN, OUT_BF16, NN, 4>),
-                    KernelLayout<256, kPairStages, IN, true>::S::kAlloc};
-    }
-    if (config == 3 || config == 4)  // GEMM_CONFIG_256x256
+    if (config == 3)  // GEMM_CONFIG_256x256
         return {3, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kPairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kPairStages, IN, OUT_BF16, NN, 2>),
@@ -71,8 +64,8 @@ KernelChoice choice_e5m2(int config, bool out_bf16, bool nn);
 // Block-scaled 8-bit operands: config GEMM_CONFIG_256x256 (the CTA pair) or anything else (the
 // one-CTA 128 x 256 tile).
 KernelChoice choice_mx(int config, bool e5m2, bool out_bf16, bool nn);
-// 2:4-sparse A, fp16 or bf16 (C of the same type): config GEMM_CONFIG_256x256 (the CTA pair),
-// GEMM_CONFIG_512x256 (two pairs sharing B) or anything else (the one-CTA 128 x 256 tile).
+// 2:4-sparse A, fp16 or bf16 (C of the same type): config GEMM_CONFIG_256x256 (the CTA pair) or
+// anything else (the one-CTA 128 x 256 tile).
 KernelChoice choice_sparse(int config, bool bf16, bool nn);
 
 }  // namespace dtg

@@ -1,5 +1,5 @@
-// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output: the one-CTA 128 x 256 tile,
-// the 256 x 256 CTA pair and two pairs sharing B by multicast.
+// 2:4-sparse A (kind::f16 .sp), fp16 or bf16 operands and output: the one-CTA 128 x 256 tile
+// and the 256 x 256 CTA pair.
 #include "kernel_set.cuh"
 
 namespace dtg {
@@ -11,11 +11,6 @@ constexpr int kSparsePairStages = 7;
 template <int IN, bool BF16, bool NN>
 KernelChoice sparse_choice(int config)
 {
-    if (config == 4)  // GEMM_CONFIG_512x256: two pairs sharing B by multicast
-        return {config, 4 * kBM, 256, 64, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
-                kSparsePairStages, 4,
-                reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kSparsePairStages, IN, BF16, NN, 4>),
-                KernelLayout<256, kSparsePairStages, IN, true>::S::kAlloc, kThreadsSide};
     if (config == 3)  // GEMM_CONFIG_256x256
         return {config, 2 * kBM, 256, 128, Operand<IN>::kStageK, Operand<IN>::kNBlock, Operand<IN>::kAStageK,
                 kSparsePairStages, 2,

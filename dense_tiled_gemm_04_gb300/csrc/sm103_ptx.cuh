@@ -338,19 +338,6 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const void* tmap,
         : "memory");
 }
 
-// Pair form with cluster multicast: the box lands at the same offset in the shared memory of
-// every CTA in cta_mask, and each destination's bytes complete on the mbarrier at the offset of
-// cluster_bar in the even-ranked CTA of that destination's pair (cluster_bar names such a CTA).
-__device__ __forceinline__ void tma_load_2d_pair_mc(uint32_t dst, const void* tmap, int32_t x, int32_t y,
-                                                    uint32_t cluster_bar, uint16_t cta_mask)
-{
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster.cta_group::2"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(dst),
-        "l"(reinterpret_cast<uint64_t>(tmap)), "r"(x), "r"(y), "r"(cluster_bar), "h"(cta_mask)
-        : "memory");
-}
-
 // tcgen05 for a CTA pair: allocation, MMA and commit act on both CTAs' tensor memory.
 __device__ __forceinline__ void tmem_alloc_pair(uint32_t slot, uint32_t ncols)
 {
@@ -430,9 +417,10 @@ __device__ __forceinline__ void tmem_cp_32x128b_warpx4_pair(uint32_t taddr, uint
     asm volatile("tcgen05.cp.cta_group::2.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc) : "memory");
 }
 
-// Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of `cta_mask` when
-// all tcgen05 operations this thread issued so far complete.
-__device__ __forceinline__ void mma_commit_pair_mc(uint32_t bar, uint16_t cta_mask)
+// Arrive once on the mbarrier at CTA-local offset `bar` in every CTA of the pair named in
+// `cta_mask` (bit r: the CTA of rank r) when all tcgen05 operations this thread issued so far
+// complete.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar, uint16_t cta_mask)
 {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(

@@ -73,8 +73,9 @@ enum {
     GEMM_OPT_MAX_CTAS = 2,     /* cap on persistent CTAs (0 = one per SM); tests use it to
                                   make each CTA walk several tiles                            */
     GEMM_OPT_RASTER_GROUP = 3, /* output-tile raster: M tiles per group (L2 reuse), >= 1      */
-    GEMM_OPT_FAULT_INJECT = 4, /* test hook: 1 = CTA 0's producer leaves one ring stage unarmed,
-                                  so a consumer wait runs out and the watchdog path returns
+    GEMM_OPT_FAULT_INJECT = 4, /* test hook: 1 = the first work unit (a CTA, or both CTAs of a
+                                  pair) loads one ring stage nowhere and leaves it unarmed, so
+                                  a consumer wait runs out and the watchdog path returns
                                   GEMM_ERR_TIMEOUT through gemm_sync_status (no GPU fault)   */
     GEMM_OPT_STREAM_K = 5,     /* 1 (default): when whole tiles would leave the last wave
                                   part-empty, share the K blocks of the last tiles evenly
@@ -91,10 +92,7 @@ enum {
     GEMM_CONFIG_AUTO = 0,
     GEMM_CONFIG_128x256 = 1,   /* 1-CTA tile 128 x 256 x 64, 4-stage ring                      */
     GEMM_CONFIG_128x128 = 2,   /* 1-CTA tile 128 x 128 x 64, 6-stage ring (more tiles)         */
-    GEMM_CONFIG_256x256 = 3,   /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
-    GEMM_CONFIG_512x256 = 4    /* 4-CTA cluster: two CTA pairs on tiles (2r, c) and (2r+1, c),
-                                  sharing B boxes by TMA multicast (16-bit dense operands;
-                                  other operand kinds run the CTA pair instead)               */
+    GEMM_CONFIG_256x256 = 3    /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
 };
 
 /* What gemm_run would launch for a problem (for benchmarks and tests). */
@@ -102,7 +100,7 @@ typedef struct {
     int32_t config;     /* GEMM_CONFIG_* actually chosen                                     */
     int32_t bm, bn, bk; /* output tile (per cluster) and K block                             */
     int32_t stages;     /* shared-memory ring depth                                          */
-    int32_t cluster;    /* CTAs per cluster (1, 2 or 4)                                       */
+    int32_t cluster;    /* CTAs per cluster (1 or 2)                                          */
     int64_t tiles_m, tiles_n, k_blocks;
     int64_t grid;       /* CTAs launched (persistent)                                        */
     int32_t threads;    /* threads per CTA                                                   */
@@ -176,7 +174,7 @@ gemm_status_t gemm_run_ex(gemm_handle_t h, const gemm_args_t* args, void* stream
  *   - args: as for gemm_run_ex, with dtype E4M3 or E5M2 (anything else: INVALID_ARG).
  *     Configurations: the 256 x 256 CTA pair where gemm_run would take a pair tile (at least
  *     one pair tile per pair of SMs), else the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask
- *     for either (GEMM_CONFIG_256x256 / _512x256: the pair; _128x256 / _128x128: one CTA).
+ *     for either (GEMM_CONFIG_256x256: the pair; _128x256 / _128x128: one CTA).
  *   - sfa: the exponents ea of A (M x ceil(K/32)), sfb: those of B (one row per column n of
  *     Beff, N x ceil(K/32)), both device pointers, 16-byte aligned, in the chunked layout that
  *     gemm_mx_pack_scales writes (gemm_mx_scale_bytes(M, K) and (N, K) bytes).  Unused when
@@ -205,8 +203,7 @@ gemm_status_t gemm_run_mx(gemm_handle_t h, const gemm_args_t* args, const void* 
  *   - dtype F16 or BF16 with out_dtype == dtype; K a multiple of 4 (else UNSUPPORTED); B, C,
  *     alpha, beta, c_col_major and the status codes as in gemm_run_ex.  K == 0 gives C = beta
  *     * C and ignores meta.  Configurations: the CTA pair where gemm_run would take it, else
- *     the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask for either, or for two pairs sharing
- *     B (GEMM_CONFIG_512x256). */
+ *     the one-CTA 128 x 256 tile; GEMM_OPT_CONFIG may ask for either. */
 gemm_status_t gemm_run_sp(gemm_handle_t h, const gemm_args_t* args, const void* meta, void* stream);
 
 /* Bytes of the chunked sparsity metadata for M rows and K: ceil(M/128) * ceil(K/64) * 4096

@@ -179,7 +179,6 @@ def test_binding_constants_match_the_header(lib):
         "GEMM_OPT_HOST_ROW_CHUNKS": lib.OPT_HOST_ROW_CHUNKS, "GEMM_OPT_HOST_COL_CHUNKS": lib.OPT_HOST_COL_CHUNKS,
         "GEMM_CONFIG_AUTO": lib.CONFIG_AUTO, "GEMM_CONFIG_128x256": lib.CONFIG_128x256,
         "GEMM_CONFIG_128x128": lib.CONFIG_128x128, "GEMM_CONFIG_256x256": lib.CONFIG_256x256,
-        "GEMM_CONFIG_512x256": lib.CONFIG_512x256,
         "GEMM_KIND_DENSE": lib.KINDS["dense"], "GEMM_KIND_BLOCK_SCALED": lib.KINDS["block_scaled"],
         "GEMM_KIND_SPARSE24": lib.KINDS["sparse24"],
     }

@@ -14,7 +14,7 @@ from dense_tiled_gemm_04_gb300 import native
 from dense_tiled_gemm_04_gb300.workloads import WORKLOADS, make_inputs, round_up, workload_inputs
 
 import oracle
-from test_gpu_parity import SENTINEL, assert_close, assert_exact, sample_rows, to_device
+from test_gpu_parity import SENTINEL, assert_close, assert_exact, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -80,8 +80,7 @@ SHAPES = [(65, 97, 130), (300, 257, 200), (1000, 1000, 520), (1003, 131, 77)]
 
 
 @pytest.mark.parametrize("col_major", [0, 1])
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256,
-                                    native.CONFIG_512x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256])
 @pytest.mark.parametrize("layout,dtype", [("NN", "f16"), ("TN", "bf16"), ("TN", "f16"), ("NN", "bf16")])
 def test_alpha_beta_and_layout(g, col_major, config, layout, dtype):
     g.set_option(native.OPT_CONFIG, config)
@@ -136,7 +135,7 @@ def test_k_zero_scales_c(g, col_major):
     assert_exact(got, oracle.encode(-2.0 * oracle.decode(C0, "f16"), "f16"), "K=0: C = beta C")
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_128x128, native.CONFIG_256x256, native.CONFIG_512x256])
+@pytest.mark.parametrize("config", [native.CONFIG_128x128, native.CONFIG_256x256])
 @pytest.mark.parametrize("col_major", [0, 1])
 def test_stream_k_with_epilogue(g, config, col_major):
     M, N, K = 1000, 1000, 2048
@@ -156,14 +155,13 @@ def test_stream_k_with_epilogue(g, config, col_major):
 
 
 def test_full_size_column_major_accumulate(g):
-    # The headline shape, C += A·B into a column-major C: sampled rows against the oracle.
+    # The headline shape, C += A·B into a column-major C: every element against the oracle.
     w = WORKLOADS["c4"].with_dist("int")
     A, B = workload_inputs(w)
     C0 = int_codes(w.M, w.N, "bf16", 10)
     got, _, _ = run_ex(g, A, B, w.layout, "bf16", 1.0, 1.0, 1, C0, pad=0, extra=0)
-    rows = sample_rows(w.M, 8, seed=3)
-    ref = oracle.gemm_axpby(A, B, w.layout, "bf16", 1.0, 1.0, C0, rows=rows)
-    assert_exact(got[rows], ref, "c4 C += A·B, column-major")
+    ref = oracle.gemm_axpby(A, B, w.layout, "bf16", 1.0, 1.0, C0)
+    assert_exact(got, ref, "c4 C += A·B, column-major")
 
 
 def test_invalid_epilogue_arguments(g):

@@ -20,7 +20,7 @@ from dense_tiled_gemm_04_gb300 import native
 from dense_tiled_gemm_04_gb300.workloads import make_inputs, round_up
 
 import oracle
-from test_gpu_parity import SENTINEL, assert_close, assert_exact, sample_rows
+from test_gpu_parity import SENTINEL, assert_close, assert_exact
 
 pytestmark = pytest.mark.gpu
 
@@ -101,8 +101,7 @@ def int_c(M, N, out, seed):
     return c.view(torch.int16).numpy().view(np.uint16)
 
 
-CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256,
-           native.CONFIG_512x256]  # 512x256 runs the pair for 8-bit operands
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256]
 IN_TYPES = ["e4m3", "e5m2"]
 
 
@@ -205,13 +204,12 @@ def test_multi_tile_stream_k_bit_exact(g, in_dtype, stream_k):
     finally:
         g.set_option(native.OPT_STREAM_K, 1)
     got = C.cpu().view(torch.int16).numpy().view(np.uint16)
-    rows = sample_rows(M, 24, seed=18)
-    ref = oracle.gemm_typed(A, B, "TN", in_dtype, "bf16", rows=rows)
-    assert_exact(got[rows], ref, f"{in_dtype} stream_k={stream_k}")
+    ref = oracle.gemm_typed(A, B, "TN", in_dtype, "bf16")
+    assert_exact(got, ref, f"{in_dtype} stream_k={stream_k}")
 
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_full_size_e4m3_8192_sampled(g, layout):
+def test_full_size_e4m3_8192_full_matrix(g, layout):
     # The square 8192^3 problem with E4M3 operands (unit-normal draws, 1/sqrt(K) as the two
     # per-tensor scales), bf16 C, default plan.
     M = N = K = 8192
@@ -221,9 +219,8 @@ def test_full_size_e4m3_8192_sampled(g, layout):
     torch.cuda.synchronize()
     assert g.sync_status() == native.OK
     got = C.cpu().view(torch.int16).numpy().view(np.uint16)
-    rows = sample_rows(M, 12, seed=20)
-    ref = oracle.gemm_typed(A, B, layout, "e4m3", "bf16", alpha=factor(1.0, s, s), rows=rows)
-    assert_close(got[rows], ref, "bf16", f"e4m3 8192^3 {layout}")
+    ref = oracle.gemm_typed(A, B, layout, "e4m3", "bf16", alpha=factor(1.0, s, s))
+    assert_close(got, ref, "bf16", f"e4m3 8192^3 {layout}")
 
 
 def test_run_ex_wrapper_matches_raw_call(g):

@@ -18,7 +18,7 @@ from dense_tiled_gemm_04_gb300.workloads import make_inputs, prune_24, round_up
 
 import oracle
 from test_gpu_fp8 import int_c
-from test_gpu_parity import SENTINEL, assert_close, assert_exact, codes, sample_rows, to_device
+from test_gpu_parity import SENTINEL, assert_close, assert_exact, codes, to_device
 
 pytestmark = pytest.mark.gpu
 
@@ -40,7 +40,7 @@ def g():
 
 
 # AUTO picks the CTA pair for large problems; 128x256 / 256x256 force the one-CTA tile / the pair.
-CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256, native.CONFIG_512x256]
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256]
 
 
 @pytest.fixture
@@ -221,12 +221,11 @@ def test_multi_tile_stream_k_bit_exact(g, config, stream_k):
         assert g.sync_status() == native.OK
     finally:
         g.set_option(native.OPT_STREAM_K, 1)
-    rows = sample_rows(M, 24, seed=115)
-    assert_exact(codes(C)[rows], oracle.gemm_rows(A, B, "TN", "bf16", rows)[0], f"stream_k={stream_k}")
+    assert_exact(codes(C), oracle.gemm(A, B, "TN", "bf16"), f"stream_k={stream_k}")
 
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
-def test_full_size_8192_sampled(g, layout):
+def test_full_size_8192_full_matrix(g, layout):
     M = N = K = 8192
     A, B = make_inputs(M, N, K, layout, "bf16", "normal", seed=116, scale=1 / 64)
     A = prune_24(A, seed=117)
@@ -235,8 +234,7 @@ def test_full_size_8192_sampled(g, layout):
     C = g.run_sp(Ac, B.cuda(), meta, layout=layout)
     torch.cuda.synchronize()
     assert g.sync_status() == native.OK
-    rows = sample_rows(M, 10, seed=118)
-    assert_close(codes(C)[rows], oracle.gemm_rows(A, B, layout, "bf16", rows)[0], "bf16", f"8192^3 {layout}")
+    assert_close(codes(C), oracle.gemm(A, B, layout, "bf16"), "bf16", f"8192^3 {layout}")
 
 
 @pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
