@@ -497,7 +497,12 @@ def run_ours(args, w):
     lib_build.build()
     g = native.Gemm(0)
     g.set_option(native.OPT_CONFIG, {"auto": native.CONFIG_AUTO, "128x256": native.CONFIG_128x256,
-                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256}[args.config])
+                                     "128x128": native.CONFIG_128x128, "256x256": native.CONFIG_256x256,
+                                     "128x64": native.CONFIG_128x64}[args.config])
+    if args.sk_min_blocks:
+        g.set_option(native.OPT_SK_MIN_BLOCKS, args.sk_min_blocks)
+    if args.raster_group:
+        g.set_option(native.OPT_RASTER_GROUP, args.raster_group)
 
     A_cpu, B_cpu = workload_inputs(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
@@ -657,9 +662,13 @@ def main(argv=None):
     ap.add_argument("--no-e2e", action="store_true", help="skip the host-buffer end-to-end leg (profiling runs)")
     ap.add_argument("--workload", default=WORKLOAD,
                     help="c1..c5, c4-e4m3, c4-mx, c4-sp (default c4, the headline workload)")
-    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256"], default="auto",
+    ap.add_argument("--config", choices=["auto", "128x256", "128x128", "256x256", "128x64"], default="auto",
                     help="kernel configuration (default: the library's own choice)")
     ap.add_argument("--no-sustained", action="store_true", help="skip the back-to-back sustained leg")
+    ap.add_argument("--sk-min-blocks", type=int, default=0,
+                    help="shortest stream-K share in K blocks (default: the library's, 8)")
+    ap.add_argument("--raster-group", type=int, default=0,
+                    help="tile rows per group of the grouped raster (default: the library's, 8)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -25,8 +25,9 @@ constexpr int kGroupDefault = 8;
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int32_t kTmapBytes = -1;  // get_tmap element type: raw bytes (side data)
-constexpr int kNumSlots = 72;  // 3 configurations x 12 operand/output types x 2 layouts
-constexpr int64_t kMinStreamKBlocks = 8;  // shortest stream-K range worth its partial-sum traffic
+constexpr int kNumSlots = 96;  // 4 configurations x 12 operand/output types x 2 layouts
+constexpr int64_t kMinStreamKBlocks = 8;   // default shortest stream-K share (GEMM_OPT_SK_MIN_BLOCKS)
+constexpr int64_t kMinSplitBlocks = 32;    // default shortest share of a split under one wave (GEMM_OPT_SPLIT_MIN_BLOCKS)
 
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 std::once_flag g_encode_once;
@@ -82,6 +83,8 @@ struct LaunchOptions {
     int64_t raster_group = kGroupDefault;
     int64_t fault_inject = 0;
     int64_t stream_k = 1;
+    int64_t sk_min_blocks = kMinStreamKBlocks;
+    int64_t split_min_blocks = kMinSplitBlocks;
     int64_t host_row_chunks = 8;
     int64_t host_col_chunks = 4;
 };
@@ -207,7 +210,9 @@ KernelChoice kernel_choice(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_l
 
 int slot_of(int config, gemm_dtype_t in, gemm_dtype_t out, gemm_layout_t layout, int family = kDense)
 {
-    const int c = config == GEMM_CONFIG_256x256 ? 2 : (config == GEMM_CONFIG_128x128 ? 1 : 0);
+    const int c = config == GEMM_CONFIG_128x64    ? 3
+                  : config == GEMM_CONFIG_256x256 ? 2
+                  : config == GEMM_CONFIG_128x128 ? 1 : 0;
     const int f8 = 2 * (in - GEMM_DTYPE_E4M3) + (out == GEMM_DTYPE_BF16 ? 1 : 0);  // 0..3
     const int types = family == kSparse24 ? 10 + in : (is_f8(in) ? (family == kBlockScaled ? 6 : 2) + f8 : in);
     return (c * 12 + types) * 2 + (layout == GEMM_LAYOUT_NN ? 1 : 0);
@@ -243,18 +248,25 @@ gemm_status_t ensure_kernel_ready(DeviceState& dev, const KernelChoice& kc, int 
     return GEMM_OK;
 }
 
-int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N)
+int pick_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int64_t N, int64_t K)
 {
-    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256)
+    if (o.config == GEMM_CONFIG_128x256 || o.config == GEMM_CONFIG_128x128 || o.config == GEMM_CONFIG_256x256 ||
+        o.config == GEMM_CONFIG_128x64)
         return static_cast<int>(o.config);
     // AUTO: the 256 x 256 CTA-pair tile when there is at least one pair tile per pair of
     // SMs (it halves each SM's shared-memory traffic for B); otherwise the 128 x 256 tile
-    // unless that leaves most SMs idle, then 128 x 128.
+    // unless that leaves most SMs idle, then 128 x 128.  Below half a wave of those, a short
+    // K loop runs on 128 x 64 tiles (more SMs taking in operands: 1000^3, 64 tiles of
+    // 128 x 128 or 128 of 128 x 64, cold L2: 14.0 against 12.7 us), a long one (64 K blocks or
+    // more) stays on 128 x 128 tiles whose K blocks fill_plan splits between CTAs (1000 x 1000
+    // x 8192: 43.7 us on 128 whole 128 x 64 tiles, 34.4 us split over 152 CTAs).
     const int64_t pair_tiles = cdiv(M, 256) * cdiv(N, 256);
     if (pair_tiles >= dev.num_sms / 2) return GEMM_CONFIG_256x256;
     const int64_t tiles256 = cdiv(M, 128) * cdiv(N, 256);
-    if (tiles256 < dev.num_sms / 2) return GEMM_CONFIG_128x128;
-    return GEMM_CONFIG_128x256;
+    if (tiles256 >= dev.num_sms / 2) return GEMM_CONFIG_128x256;
+    const int64_t tiles128 = cdiv(M, 128) * cdiv(N, 128);
+    if (tiles128 >= dev.num_sms / 2 || cdiv(K, 64) >= 64) return GEMM_CONFIG_128x128;
+    return GEMM_CONFIG_128x64;
 }
 
 // Workspace a stream-K plan with `units` work units needs (see the kernel's slot layout).
@@ -290,17 +302,37 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     if (units < 1) units = 1;
     plan->dp_tiles = tiles;
     // Stream-K when whole tiles would leave the last wave part-empty: every unit does
-    // (full waves - 1) whole tiles, then an equal share of the K blocks of the rest.
+    // (full waves - 1) whole tiles, then an equal share of the K blocks of the rest.  A
+    // share shorter than sk_min_blocks would cost more in partial-sum traffic than it saves.
+    // A problem under one wave (fewer tiles than units) is split only when every share still
+    // holds split_min_blocks and every tile gets at least two shares: the merge through the
+    // workspace is a few microseconds of dependent global-memory traffic, so only long K loops
+    // spread over many more units gain from it (measured, cold L2, 1000 x 1000 x K: 128 x 128
+    // tiles at K = 1000 ran 13.6 us whole and 17.1 us as two 8-block shares per tile; at
+    // K = 4096, 26.7 us whole and 23.8 us as two 32-block shares; 128 x 64 tiles, 128 of them,
+    // were slower split over 152 CTAs at every K); fewer units then take shares of that
+    // length.
     if (ws && o.stream_k && tiles % units != 0) {
         const int64_t dp = tiles >= units ? (tiles / units - 1) * units : 0;
         const int64_t sk_tiles = tiles - dp;
         const int64_t sk_blocks = sk_tiles * plan->k_blocks;
-        const int64_t base = sk_blocks / units;
-        if (base >= kMinStreamKBlocks && sk_partial_floats(units, kc) <= ws->partial_floats &&
+        int64_t sk_units = units;
+        int64_t min_share = o.sk_min_blocks;
+        if (tiles < units) {
+            min_share = o.split_min_blocks > 0 ? o.split_min_blocks : sk_blocks + 1;  // 0: never split
+            if (sk_blocks / units < min_share) sk_units = sk_blocks / min_share;
+            if (sk_units < 2 * tiles) {  // fewer than two shares a tile: whole tiles
+                sk_units = units;
+                min_share = sk_blocks + 1;
+            }
+        }
+        const int64_t base = sk_blocks / sk_units;
+        if (base >= min_share && sk_partial_floats(sk_units, kc) <= ws->partial_floats &&
             sk_counter_count(sk_tiles, kc) <= ws->counter_count) {
+            units = sk_units;
             plan->dp_tiles = dp;
             plan->sk_base = base;
-            plan->sk_extra = sk_blocks % units;
+            plan->sk_extra = sk_blocks % sk_units;
         }
     }
     if (plan->dp_tiles == tiles && tiles < units) units = tiles;  // whole tiles only: no idle units
@@ -364,8 +396,10 @@ int choose_config(const LaunchOptions& o, const DeviceState& dev, int64_t M, int
     // 128-byte side-data rows: block-scaled, the pair gains 6-9 % at 8192^3, 5-12 % at 6144^3,
     // ties at 4096^3; sparse: the pair 2236 TF/s at 8192^3).  The pair addresses the side data
     // by rows of kSideRowBytes with 32-bit TMA coordinates, which must fit.
-    int config = pick_config(o, dev, M, N);
+    int config = pick_config(o, dev, M, N, K);
     if (family == kBlockScaled && config == GEMM_CONFIG_128x128) config = GEMM_CONFIG_128x256;
+    // An N-major 8-bit B row is 128 elements wide: 8-bit operands take 128 x 128 for 128 x 64.
+    if (config == GEMM_CONFIG_128x64 && is_f8(dtype)) config = GEMM_CONFIG_128x128;
     if (family != kDense) {
         const int64_t lim = int64_t(1) << 31;
         const bool rows_fit =
@@ -471,13 +505,19 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
                       CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
-    if (family == kBlockScaled && kc.cluster >= 2) {
+    // Block scales (every block-scaled kernel): boxes of kScGroup consecutive chunks of one
+    // row block, i.e. the scales of kScGroup ring stages (past the end of a row block the box
+    // reads the next block's chunks, or zeros past the buffer; the kernel uses neither).
+    if (family == kBlockScaled) {
         constexpr uint32_t kRb = dtg::kSideRowBytes;
         constexpr uint32_t kRows = dtg::kSfChunkBytes / kRb;
         const uint64_t rows_a = static_cast<uint64_t>(cdiv(M, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
         const uint64_t rows_b = static_cast<uint64_t>(cdiv(N, dtg::kSfChunkRows) * cdiv(K, 128)) * kRows;
-        if (!get_tmap(cache, ep.sfa, kRb, rows_a, kRb, kRb, kRows, kTmapBytes, &tS, CU_TENSOR_MAP_SWIZZLE_NONE) ||
-            !get_tmap(cache, ep.sfb, kRb, rows_b, kRb, kRb, kRows, kTmapBytes, &tS2, CU_TENSOR_MAP_SWIZZLE_NONE))
+        if (rows_a >= (uint64_t(1) << 31) || rows_b >= (uint64_t(1) << 31)) return GEMM_ERR_UNSUPPORTED;
+        if (!get_tmap(cache, ep.sfa, kRb, rows_a, kRb, kRb, kRows * dtg::kScGroup, kTmapBytes, &tS,
+                      CU_TENSOR_MAP_SWIZZLE_NONE) ||
+            !get_tmap(cache, ep.sfb, kRb, rows_b, kRb, kRb, kRows * dtg::kScGroup, kTmapBytes, &tS2,
+                      CU_TENSOR_MAP_SWIZZLE_NONE))
             return GEMM_ERR_CUDA;
     }
     void* args[] = {&tA, &tB, &tC, &tS, &tS2, &kp};
@@ -1008,7 +1048,7 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     switch (opt) {
     case GEMM_OPT_CONFIG:
         if (value != GEMM_CONFIG_AUTO && value != GEMM_CONFIG_128x256 && value != GEMM_CONFIG_128x128 &&
-            value != GEMM_CONFIG_256x256)
+            value != GEMM_CONFIG_256x256 && value != GEMM_CONFIG_128x64)
             return GEMM_ERR_INVALID_ARG;
         o.config = value;
         return GEMM_OK;
@@ -1031,6 +1071,14 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
     case GEMM_OPT_STREAM_K:
         if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
         o.stream_k = value;
+        return GEMM_OK;
+    case GEMM_OPT_SK_MIN_BLOCKS:
+        if (value < 1 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+        o.sk_min_blocks = value;
+        return GEMM_OK;
+    case GEMM_OPT_SPLIT_MIN_BLOCKS:
+        if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
+        o.split_min_blocks = value;
         return GEMM_OK;
     case GEMM_OPT_HOST_ROW_CHUNKS:
         if (value < 1 || value > HostPipe::kMaxRowChunks) return GEMM_ERR_INVALID_ARG;
@@ -1056,6 +1104,8 @@ gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value
     case GEMM_OPT_RASTER_GROUP: *value = o.raster_group; return GEMM_OK;
     case GEMM_OPT_FAULT_INJECT: *value = o.fault_inject; return GEMM_OK;
     case GEMM_OPT_STREAM_K: *value = o.stream_k; return GEMM_OK;
+    case GEMM_OPT_SK_MIN_BLOCKS: *value = o.sk_min_blocks; return GEMM_OK;
+    case GEMM_OPT_SPLIT_MIN_BLOCKS: *value = o.split_min_blocks; return GEMM_OK;
     case GEMM_OPT_HOST_ROW_CHUNKS: *value = o.host_row_chunks; return GEMM_OK;
     case GEMM_OPT_HOST_COL_CHUNKS: *value = o.host_col_chunks; return GEMM_OK;
     default: return GEMM_ERR_INVALID_ARG;

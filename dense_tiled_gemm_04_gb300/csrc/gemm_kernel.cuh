@@ -15,9 +15,10 @@
 //                 E8M0 scales, kind::f16 .sp -- two MMAs of 32 K -- for a 2:4-sparse A), then
 //                 tcgen05.commit releases the stage; after the item's last K block a commit
 //                 marks the accumulator full.  The first MMA of an item overwrites (the
-//                 zero-filled accumulator of §2), later ones add.  Block scales and sparsity
-//                 metadata arrive with the stage; the MMA thread waits until warp 6 has
-//                 copied them into TMEM.
+//                 zero-filled accumulator of §2), later ones add.  Sparsity metadata arrives
+//                 with the stage, block scales in a ring of their own (one load per block for
+//                 kScGroup stages); the MMA thread waits until warp 6 has copied them into
+//                 TMEM.
 //   warp 6        block-scaled and sparse kernels only (side data): per K block, once the
 //                 stage is in, tcgen05.cp of its scales or metadata into the stage's TMEM
 //                 columns, then a commit the MMA thread waits on.
@@ -116,6 +117,11 @@ struct Operand {
 // a matrix with G = ceil(K / 128) K groups starts at byte (rb * G + g) * 512.
 constexpr int kSfChunkBytes = 512;
 constexpr int kSfChunkRows = 128;
+// The chunks of kScGroup consecutive K groups of one row block are contiguous, so the producer
+// loads a block's scales for kScGroup stages at once (one box per block instead of one per
+// stage) into a ring of kScSlots slots of its own.
+constexpr int kScGroup = 4;
+constexpr int kScSlots = 2;
 constexpr int kSfTmemCol = 256;  // first TMEM column of the per-stage side data (after one 256-column accumulator)
 // CTA-pair kernels load side data (scale chunks, metadata chunks) through tensor maps that view
 // the chunked buffer as rows of this many bytes, so a chunk is a box of whole rows.
@@ -228,9 +234,10 @@ struct WorkIter {
     }
 };
 
-// SF_BYTES: side-data bytes per ring stage (block scales or sparsity metadata; 0 without);
-// STG_BUFS: staging buffers per epilogue warp; A_ROW_BYTES: bytes of an A row per stage.
-template <int B_ROWS, int STAGES, int SF_BYTES = 0, int STG_BUFS = 2, int A_ROW_BYTES = kRowBytes>
+// SF_BYTES: side-data bytes per ring stage (sparsity metadata; 0 without); SC_BYTES: bytes of
+// one slot of the block-scale ring (kScSlots slots; 0 without); STG_BUFS: staging buffers per
+// epilogue warp; A_ROW_BYTES: bytes of an A row per stage.
+template <int B_ROWS, int STAGES, int SF_BYTES = 0, int STG_BUFS = 2, int A_ROW_BYTES = kRowBytes, int SC_BYTES = 0>
 struct Smem {
     static constexpr int kABytes = kBM * A_ROW_BYTES;
     static constexpr int kBBytes = B_ROWS * kRowBytes;
@@ -238,12 +245,15 @@ struct Smem {
     static constexpr int kRing = STAGES * kStageBytes;
     static constexpr int kSfOff = kRing;
     static constexpr int kSfBytes = SF_BYTES;
-    static constexpr int kStgOff = (kSfOff + STAGES * SF_BYTES + 1023) / 1024 * 1024;
+    static constexpr int kScOff = kSfOff + STAGES * SF_BYTES;
+    static constexpr int kScBytes = SC_BYTES;
+    static constexpr int kStgOff = (kScOff + kScSlots * SC_BYTES + 1023) / 1024 * 1024;
     static constexpr int kStgBufs = STG_BUFS;
     static constexpr int kStg = kEpiWarps * STG_BUFS * kStgBytes;
     static constexpr int kBarOff = kStgOff + kStg;
-    // full, empty, acc_full[2], acc_empty[2], drain, scales-in-TMEM per stage, scale-copy drain
-    static constexpr int kNumBars = 3 * STAGES + 6;
+    // full, empty, acc_full[2], acc_empty[2], drain, side-data-in-TMEM per stage, side-copy
+    // drain, scale-ring full and empty per slot
+    static constexpr int kNumBars = 3 * STAGES + 6 + 2 * kScSlots;
     static constexpr int kMiscOff = kBarOff + kNumBars * 8;
     static constexpr int kTotal = kMiscOff + 16;     // tmem slot, abort flag, stream-K "last" flag
     static constexpr int kAlloc = kTotal + 1024;     // slack for aligning the base to 1 KB
@@ -253,20 +263,21 @@ struct Smem {
 };
 
 // Shared-memory layout of a kernel instantiation (host and device agree through this).
-// Block-scaled kernels add the scale chunks of each stage (one for A, one per 128 B rows)
-// and, to stay within 227 KB, keep one staging buffer per epilogue warp; sparse kernels add
-// the stage's metadata chunk and store A rows of 64 bytes (the CTA-pair sparse kernel also
-// keeps one staging buffer, for a deeper ring).
+// Block-scaled kernels add a ring of scale slots (each the scale chunks of kScGroup stages:
+// one chunk for A, one per 128 B rows, per stage) and, to stay within 227 KB, keep one staging
+// buffer per epilogue warp; sparse kernels add the stage's metadata chunk and store A rows of
+// 64 bytes (the CTA-pair sparse kernel also keeps one staging buffer, for a deeper ring).
 template <int BN, int STAGES, int IN, bool PAIR>
 struct KernelLayout {
     static constexpr int kBRows = BN / (PAIR ? 2 : 1);
     static constexpr bool kMX = Operand<IN>::kMX;
     static constexpr bool kSparse = Operand<IN>::kSparse;
-    // Block scales per CTA and stage: its A rows' chunk and the B chunks of the whole tile (each
-    // CTA of a pair produces all BN columns of its rows, so it holds every column's scales).
-    static constexpr int kSfBytes =
-        kMX ? kSfChunkBytes * (1 + BN / kSfChunkRows) : (kSparse ? kMetaChunkBytes : 0);
-    using S = Smem<kBRows, STAGES, kSfBytes, (kMX || (kSparse && PAIR)) ? 1 : 2, Operand<IN>::kARowBytes>;
+    // Block-scale chunks per CTA and stage: its A rows' chunk and the B chunks of the whole tile
+    // (each CTA of a pair produces all BN columns of its rows, so it holds every column's scales).
+    static constexpr int kSfChunks = kMX ? 1 + BN / kSfChunkRows : 0;
+    static constexpr int kSfBytes = kSparse ? kMetaChunkBytes : 0;
+    static constexpr int kScBytes = kSfChunks * kScGroup * kSfChunkBytes;
+    using S = Smem<kBRows, STAGES, kSfBytes, (kMX || (kSparse && PAIR)) ? 1 : 2, Operand<IN>::kARowBytes, kScBytes>;
 };
 
 // tcgen05 shared-memory matrix descriptor for a 128-byte-swizzled operand tile.
@@ -593,15 +604,17 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
     constexpr int kRanks = PAIR ? 2 : 1;       // CTAs per MMA (pair)
     constexpr int kTileM = kBM * kRanks;       // output rows per tile
     constexpr int kBRows = BN / kRanks;        // B rows (TN) / columns (NN) this CTA loads
+    static_assert(BN == 64 || BN == 128 || BN == 256, "one MMA of N = BN per K step");
+    static_assert(!NN || kBRows % T::kNBlock == 0, "an N-major B box is one 128-byte row of N");
     // Block-scaled and sparse kernels keep one accumulator and put the side data of every
     // ring stage (scales, metadata) in the TMEM columns after it; the others double-buffer
     // the accumulator.
     constexpr bool kSide = T::kMX || T::kSparse;
     constexpr int kAccBufs = kSide ? 1 : 2;
     constexpr uint32_t kTmemCols = kSide ? 512 : 2 * BN;
-    static_assert(kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
+    static_assert(kTmemCols == 128 || kTmemCols == 256 || kTmemCols == 512, "TMEM allocations are powers of two");
     using L = typename KernelLayout<BN, STAGES, IN, PAIR>::S;
-    constexpr int kSfChunks = T::kMX ? L::kSfBytes / kSfChunkBytes : 0;  // per stage: A, then B
+    constexpr int kSfChunks = KernelLayout<BN, STAGES, IN, PAIR>::kSfChunks;  // block-scale chunks per stage: A, then B
     constexpr int kSideCols = T::kMX ? kSfChunks * 4 : (T::kSparse ? 2 * kMetaTmemStride : 0);  // TMEM cols / stage
     static_assert(!kSide || (BN <= kSfTmemCol &&
                              kSfTmemCol + STAGES * kSideCols <= static_cast<int>(kTmemCols)),
@@ -621,6 +634,8 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
     const uint32_t drain_bar = bar0 + 8u * (2 * STAGES + 4);
     auto sfr_bar = [&](int s) { return bar0 + 8u * (2 * STAGES + 5 + s); };  // side data of stage s in TMEM
     const uint32_t sdrain_bar = bar0 + 8u * (3 * STAGES + 5);
+    auto scf_bar = [&](int q) { return bar0 + 8u * (3 * STAGES + 6 + q); };             // scale slot q loaded
+    auto sce_bar = [&](int q) { return bar0 + 8u * (3 * STAGES + 6 + kScSlots + q); };  // scale slot q free
     uint32_t* const tmem_slot = reinterpret_cast<uint32_t*>(smem + L::kMiscOff);
     volatile int32_t* const abort_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMiscOff + 4);
     volatile int32_t* const last_flag = reinterpret_cast<volatile int32_t*>(smem + L::kMiscOff + 8);
@@ -646,6 +661,11 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
         if constexpr (kSide) {
             for (int s = 0; s < STAGES; ++s) ptx::mbar_init(sfr_bar(s), 1);
             ptx::mbar_init(sdrain_bar, 1);
+            if constexpr (T::kMX)
+                for (int q = 0; q < kScSlots; ++q) {
+                    ptx::mbar_init(scf_bar(q), 1);
+                    ptx::mbar_init(sce_bar(q), 1);
+                }
         }
         *abort_flag = 0;
         *last_flag = 0;
@@ -653,8 +673,11 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmB);
         ptx::prefetch_tmap(&tmC);
-        if constexpr (kSide && PAIR) ptx::prefetch_tmap(&tmS);
-        if constexpr (T::kMX && PAIR) ptx::prefetch_tmap(&tmS2);
+        if constexpr (T::kSparse && PAIR) ptx::prefetch_tmap(&tmS);
+        if constexpr (T::kMX) {
+            ptx::prefetch_tmap(&tmS);
+            ptx::prefetch_tmap(&tmS2);
+        }
     }
     if (warp == kMmaWarp) {
         if constexpr (PAIR) {
@@ -687,8 +710,11 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
         if (lane == 0) {
             // ---------------------------------------------------------------- producer
             uint32_t armed_mask = 0, armed_parity = 0;  // leader: stages armed, last parity
+            uint32_t sc_armed_mask = 0, sc_armed_parity = 0;  // leader: scale slots armed, last parity
             int stage = 0;
             uint32_t phase = 0;
+            int sc_slot = 0;  // block-scale ring
+            uint32_t sc_phase = 0;
             int64_t loaded = 0;
             WorkIter it(p, unit, units);
             int64_t tile;
@@ -698,8 +724,43 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                 tile_coord(tile, p.tiles_m, p.tiles_n, p.group_m, tm, tn);
                 const int32_t y_a = static_cast<int32_t>(tm * kTileM + rank * kBM);
                 const int32_t n_b = static_cast<int32_t>(tn * BN + rank * kBRows);
+                // Block scales: the A chunk of this tile row and the B chunks of this tile's
+                // columns that exist (a ragged N may leave out the last).
+                int sf_b_chunks = 0;
+                if constexpr (T::kMX) {
+                    const int64_t nb0 = tn * (BN / kSfChunkRows);
+                    sf_b_chunks = static_cast<int>(p.sfb_blocks - nb0);
+                    if (sf_b_chunks > kSfChunks - 1) sf_b_chunks = kSfChunks - 1;
+                }
                 for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
                     if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
+                    if constexpr (T::kMX) {
+                        // Every kScGroup stages of an item: the scale chunks of those stages, one
+                        // box of kScGroup chunks per block (A's, then B's), into the next slot of
+                        // the scale ring, completing on that slot's barrier in the leader.
+                        if ((kb - kb0) % kScGroup == 0) {
+                            if (!wd.wait(sce_bar(sc_slot), sc_phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
+                            const uint32_t sc = base + L::kScOff + sc_slot * L::kScBytes;
+                            const uint32_t scb = PAIR ? ptx::mapa_shared(scf_bar(sc_slot), 0u) : scf_bar(sc_slot);
+                            if (leader) {
+                                ptx::mbar_arrive_expect_tx(scf_bar(sc_slot),
+                                                           kRanks * (1 + sf_b_chunks) * kScGroup * kSfChunkBytes);
+                                sc_armed_mask |= 1u << sc_slot;
+                                sc_armed_parity = (sc_armed_parity & ~(1u << sc_slot)) | (sc_phase << sc_slot);
+                            }
+                            auto load_sc = [&](uint32_t dst, const CUtensorMap* tm_, int64_t chunk) {
+                                const int32_t y = static_cast<int32_t>(chunk * (kSfChunkBytes / kSideRowBytes));
+                                if constexpr (PAIR)
+                                    ptx::tma_load_2d_pair(dst, tm_, 0, y, scb);
+                                else
+                                    ptx::tma_load_2d(dst, tm_, 0, y, scb);
+                            };
+                            const int64_t nb0 = tn * (BN / kSfChunkRows);
+                            load_sc(sc, &tmS, (tm * kRanks + rank) * p.num_kb + kb);
+                            for (int j = 0; j < sf_b_chunks; ++j)
+                                load_sc(sc + (1 + j) * (kScGroup * kSfChunkBytes), &tmS2, (nb0 + j) * p.num_kb + kb);
+                        }
+                    }
                     if (p.fault_inject && unit == 0 && loaded == 1) {
                         // Test hook: every CTA of the first unit leaves this stage unloaded (and
                         // the leader leaves it unarmed), so the MMA thread's wait on it runs out
@@ -709,17 +770,8 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         const uint32_t sb = sa + L::kABytes;
                         const int32_t k0 = kb * T::kStageK;
                         const uint32_t fb = PAIR ? ptx::mapa_shared(full_bar(stage), 0u) : full_bar(stage);
-                        // Block scales: the A chunk of this tile row and the B chunks of this
-                        // tile's columns that exist (a ragged N may leave out the last).
-                        int sf_b_chunks = 0;
-                        if constexpr (T::kMX) {
-                            const int64_t nb0 = tn * (BN / kSfChunkRows);
-                            sf_b_chunks = static_cast<int>(p.sfb_blocks - nb0);
-                            if (sf_b_chunks > kSfChunks - 1) sf_b_chunks = kSfChunks - 1;
-                        }
                         if (leader) {
-                            const int sf_bytes =
-                                T::kMX ? (1 + sf_b_chunks) * kSfChunkBytes : (T::kSparse ? kMetaChunkBytes : 0);
+                            const int sf_bytes = T::kSparse ? kMetaChunkBytes : 0;
                             ptx::mbar_arrive_expect_tx(full_bar(stage), kRanks * (L::kStageBytes + sf_bytes));
                             armed_mask |= 1u << stage;
                             armed_parity = (armed_parity & ~(1u << stage)) | (phase << stage);
@@ -753,51 +805,50 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                                 ptx::bulk_load_1d(base + L::kSfOff + stage * L::kSfBytes,
                                                   p.meta + chunk * kMetaChunkBytes, kMetaChunkBytes, fb);
                         }
-                        if constexpr (T::kMX) {
-                            // This CTA's A rows' chunk and the tile's B chunks: 1-D bulk copies,
-                            // or, in a pair, TMA boxes of whole kSideRowBytes rows completing on the
-                            // leader's barrier.
-                            const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
-                            const int64_t g = kb;
-                            const int64_t ca = (tm * kRanks + rank) * p.num_kb + g;
-                            const int64_t nb0 = tn * (BN / kSfChunkRows);
-                            constexpr int kRows = kSfChunkBytes / kSideRowBytes;
-                            if constexpr (PAIR) {
-                                load(sf, &tmS, 0, static_cast<int32_t>(ca * kRows));
-                                for (int j = 0; j < sf_b_chunks; ++j)
-                                    load(sf + (1 + j) * kSfChunkBytes, &tmS2, 0,
-                                         static_cast<int32_t>(((nb0 + j) * p.num_kb + g) * kRows));
-                            } else {
-                                ptx::bulk_load_1d(sf, p.sfa + ca * kSfChunkBytes, kSfChunkBytes, fb);
-                                for (int j = 0; j < sf_b_chunks; ++j)
-                                    ptx::bulk_load_1d(sf + (1 + j) * kSfChunkBytes,
-                                                      p.sfb + ((nb0 + j) * p.num_kb + g) * kSfChunkBytes,
-                                                      kSfChunkBytes, fb);
-                            }
-                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
+                    if constexpr (T::kMX) {
+                        if ((kb - kb0) % kScGroup == kScGroup - 1 || kb == kb1 - 1) {
+                            if (++sc_slot == kScSlots) {
+                                sc_slot = 0;
+                                sc_phase ^= 1u;
+                            }
+                        }
+                    }
                 }
             }
             // Tail: wait (bounded) until the MMA thread has released every stage this
-            // producer filled, so no tcgen05.commit arrival is still heading for this
-            // CTA's barriers when it leaves.
+            // producer filled (and the side-data warp every scale slot), so no
+            // tcgen05.commit arrival is still heading for this CTA's barriers when it leaves.
             for (int i = 0; i < STAGES; ++i) {
-                if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, -1, i)) break;
+                if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, -1, i)) goto producer_done;
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
                 }
             }
+            if constexpr (T::kMX) {
+                for (int i = 0; i < kScSlots; ++i) {
+                    if (!wd.wait(sce_bar(sc_slot), sc_phase ^ 1u, kRoleProducer, -1, i)) break;
+                    if (++sc_slot == kScSlots) {
+                        sc_slot = 0;
+                        sc_phase ^= 1u;
+                    }
+                }
+            }
         producer_done:
             // The leader's full barriers count every load of the CTA (pair): waiting on them
             // (bounded) covers every load still in flight.
-            if (leader)
+            if (leader) {
                 for (int s = 0; s < STAGES; ++s)
                     if (armed_mask & (1u << s)) wd.drain(full_bar(s), (armed_parity >> s) & 1u);
+                if constexpr (T::kMX)
+                    for (int q = 0; q < kScSlots; ++q)
+                        if (sc_armed_mask & (1u << q)) wd.drain(scf_bar(q), (sc_armed_parity >> q) & 1u);
+            }
         }
     } else if (warp == kMmaWarp) {
         if (lane == 0 && leader) {
@@ -843,6 +894,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         // sparse A, 64-byte-swizzled rows with 512-byte groups.
                         const uint64_t adesc =
                             T::kSparse ? smem_desc_sw64(sa + k * 32, 16, 512) : smem_desc_sw128(sa + k * 32, 16, 1024);
+                        const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
                         uint64_t bdesc;
                         if constexpr (NN) {
                             // B (N-major): rows are K; the k-th slice starts kMmaK rows of 128 B
@@ -853,7 +905,6 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                             // B (K-major): the k-th slice starts kMmaK elements along each row.
                             bdesc = smem_desc_sw128(sb + k * (T::kMmaK * T::kBytes), 16, 1024);
                         }
-                        const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
                         if constexpr (PAIR) {
                             if constexpr (T::kMX)
                                 ptx::mma_mxf8_pair(d_tmem, adesc, bdesc, idesc | mx_scale_ids(k), sf_tmem, sf_tmem + 4,
@@ -918,15 +969,29 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             // these copies held its MMAs back (measured: three copies per stage cost ~15 % of
             // the tensor pipe's time); from this warp they overlap the MMAs.  The stage is
             // released (empty barrier) only after the MMAs that follow the copies, so no copy
-            // outlives its source.
+            // outlives its source.  Block scales come from their own ring (a slot holds
+            // kScGroup stages' chunks): a slot is released by a commit after the copies of its
+            // last stage.
             int stage = 0;
             uint32_t phase = 0;
+            int sc_slot = 0;
+            uint32_t sc_phase = 0;
             bool aborted = false;
             WorkIter it(p, unit, units);
             int64_t tile;
             int kb0, kb1;
             while (!aborted && it.next(p, tile, kb0, kb1)) {
                 for (int kb = kb0; kb < kb1; ++kb) {
+                    const int pos = (kb - kb0) % kScGroup;  // stage within its scale slot
+                    if constexpr (T::kMX) {
+                        if (pos == 0 && !wd.wait(scf_bar(sc_slot), sc_phase, kRoleSide, tile, kb)) {
+                            aborted = true;
+                            break;
+                        }
+                    }
+                    // Copies wait for the whole stage (issued as soon as the stage's TMEM columns
+                    // were free, they ran between the MMAs of the stage before and slowed them:
+                    // 8192^3 E4M3 2880 against 3259 TF/s).
                     if (!wd.wait(full_bar(stage), phase, kRoleSide, tile, kb)) {
                         aborted = true;
                         break;
@@ -936,9 +1001,11 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                     const uint32_t sf_tmem = tmem_base + col;
                     const uint32_t sf = base + L::kSfOff + stage * L::kSfBytes;
                     if constexpr (T::kMX) {
+                        // Chunk c of this stage: block c's box in the slot, stage pos of kScGroup.
+                        const uint32_t sc = base + L::kScOff + sc_slot * L::kScBytes + pos * kSfChunkBytes;
 #pragma unroll
                         for (int c = 0; c < kSfChunks; ++c) {
-                            const uint64_t d = smem_desc_plain(sf + c * kSfChunkBytes, 0, 128);
+                            const uint64_t d = smem_desc_plain(sc + c * (kScGroup * kSfChunkBytes), 0, 128);
                             if constexpr (PAIR)
                                 ptx::tmem_cp_32x128b_warpx4_pair(sf_tmem + 4 * c, d);
                             else
@@ -969,6 +1036,20 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
+                    }
+                    if constexpr (T::kMX) {
+                        if (pos == kScGroup - 1 || kb == kb1 - 1) {
+                            // The slot's last copies issued: free it (in both CTAs of a pair, each
+                            // of which refills its own) once they complete.
+                            if constexpr (PAIR)
+                                ptx::mma_commit_pair(sce_bar(sc_slot), 0x3);
+                            else
+                                ptx::mma_commit_cta1(sce_bar(sc_slot));
+                            if (++sc_slot == kScSlots) {
+                                sc_slot = 0;
+                                sc_phase ^= 1u;
+                            }
+                        }
                     }
                 }
             }

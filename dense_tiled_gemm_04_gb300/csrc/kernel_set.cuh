@@ -45,8 +45,12 @@ KernelChoice choice_for(int config)
                 kPairStages, 2,
                 reinterpret_cast<const void*>(&gemm_tcgen05_kernel<256, kPairStages, IN, OUT_BF16, NN, 2>),
                 KernelLayout<256, kPairStages, IN, true>::S::kAlloc};
-    if (config == 2)  // GEMM_CONFIG_128x128
-        return one_cta_choice<128, 6, IN, OUT_BF16, NN>(config);
+    if constexpr (Operand<IN>::kBytes == 2) {
+        if (config == 4)  // GEMM_CONFIG_128x64: 24 KB stages (16-bit operands: 8-bit ones take 128 x 128)
+            return one_cta_choice<64, 8, IN, OUT_BF16, NN>(config);
+    }
+    if (config == 2 || config == 4)  // GEMM_CONFIG_128x128
+        return one_cta_choice<128, 6, IN, OUT_BF16, NN>(2);
     return one_cta_choice<256, 4, IN, OUT_BF16, NN>(1);  // GEMM_CONFIG_128x256
 }
 
@@ -56,7 +60,7 @@ KernelChoice choice_for_layout(int config, bool nn)
     return nn ? choice_for<IN, OUT_BF16, true>(config) : choice_for<IN, OUT_BF16, false>(config);
 }
 
-// config: GEMM_CONFIG_128x256, _128x128 or _256x256 (never AUTO).
+// config: GEMM_CONFIG_128x256, _128x128, _128x64 or _256x256 (never AUTO).
 KernelChoice choice_f16(int config, bool nn);
 KernelChoice choice_bf16(int config, bool nn);
 KernelChoice choice_e4m3(int config, bool out_bf16, bool nn);

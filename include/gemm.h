@@ -78,13 +78,24 @@ enum {
                                   a consumer wait runs out and the watchdog path returns
                                   GEMM_ERR_TIMEOUT through gemm_sync_status (no GPU fault)   */
     GEMM_OPT_STREAM_K = 5,     /* 1 (default): when whole tiles would leave the last wave
-                                  part-empty, share the K blocks of the last tiles evenly
-                                  between CTAs (partial sums merged in K order, so results
-                                  are deterministic); 0: whole tiles only                     */
+                                  part-empty (or the whole problem is under one wave), share
+                                  the K blocks of the last tiles evenly between CTAs (partial
+                                  sums merged in K order, so results are deterministic);
+                                  0: whole tiles only ("NineToothed GEMM 语法入门" §4: a K
+                                  loop split across programs needs a merge)                  */
     GEMM_OPT_HOST_ROW_CHUNKS = 6, /* gemm_run_host: row chunks of A and C, 1..16 (default 8;
                                   chunks are at least 1024 rows)                              */
-    GEMM_OPT_HOST_COL_CHUNKS = 7  /* gemm_run_host: column chunks of C (B's rows for TN, its
+    GEMM_OPT_HOST_COL_CHUNKS = 7, /* gemm_run_host: column chunks of C (B's rows for TN, its
                                   columns for NN), 1..8 (default 4; at least 2048 columns)   */
+    GEMM_OPT_SK_MIN_BLOCKS = 8, /* shortest stream-K share of a part-empty last wave, in K
+                                  blocks (default 8, >= 1)                                  */
+    GEMM_OPT_SPLIT_MIN_BLOCKS = 9 /* a problem under one wave (fewer tiles than the CTAs or
+                                  pairs that fit) has its K blocks split over more units only
+                                  when every share holds at least this many (default 32;
+                                  0 = never): the merge costs a few microseconds of dependent
+                                  global-memory traffic, which only long K loops repay.  The
+                                  units are then as many as shares of that length allow, if
+                                  more than the tiles                                         */
 };
 
 typedef int32_t gemm_config_t;
@@ -92,7 +103,10 @@ enum {
     GEMM_CONFIG_AUTO = 0,
     GEMM_CONFIG_128x256 = 1,   /* 1-CTA tile 128 x 256 x 64, 4-stage ring                      */
     GEMM_CONFIG_128x128 = 2,   /* 1-CTA tile 128 x 128 x 64, 6-stage ring (more tiles)         */
-    GEMM_CONFIG_256x256 = 3    /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
+    GEMM_CONFIG_256x256 = 3,   /* 2-CTA cluster tile 256 x 256 x 64 (cta_group::2)             */
+    GEMM_CONFIG_128x64 = 4     /* 1-CTA tile 128 x 64 x 64, 8-stage ring (small problems: more
+                                  SMs taking in operands; 8-bit operands run 128 x 128 and
+                                  side-data kernels 128 x 256 instead)                       */
 };
 
 /* What gemm_run would launch for a problem (for benchmarks and tests). */

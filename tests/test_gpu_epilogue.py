@@ -80,7 +80,8 @@ SHAPES = [(65, 97, 130), (300, 257, 200), (1000, 1000, 520), (1003, 131, 77)]
 
 
 @pytest.mark.parametrize("col_major", [0, 1])
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x64,
+                                    native.CONFIG_256x256])
 @pytest.mark.parametrize("layout,dtype", [("NN", "f16"), ("TN", "bf16"), ("TN", "f16"), ("NN", "bf16")])
 def test_alpha_beta_and_layout(g, col_major, config, layout, dtype):
     g.set_option(native.OPT_CONFIG, config)

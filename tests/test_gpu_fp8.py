@@ -101,7 +101,8 @@ def int_c(M, N, out, seed):
     return c.view(torch.int16).numpy().view(np.uint16)
 
 
-CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256]
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256,
+           native.CONFIG_128x64]  # 128x64 runs 128x128 for 8-bit operands
 IN_TYPES = ["e4m3", "e5m2"]
 
 

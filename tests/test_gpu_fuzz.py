@@ -19,7 +19,8 @@ from test_gpu_parity import assert_exact, assert_guard, gpu_gemm
 
 pytestmark = pytest.mark.gpu
 
-CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256]
+CONFIGS = [native.CONFIG_AUTO, native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_128x64,
+           native.CONFIG_256x256]
 
 
 @pytest.fixture(scope="module")

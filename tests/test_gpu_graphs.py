@@ -31,7 +31,8 @@ def g():
     h.close()
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x128, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x128, native.CONFIG_128x64,
+                                    native.CONFIG_256x256])
 def test_gemm_run_captured_and_replayed(g, config):
     M, N, K = 1100, 1000, 1800  # several tiles, a part-empty last wave: stream-K in the graph too
     A, B = make_inputs(M, N, K, "TN", "bf16", "int", seed=301)

@@ -226,6 +226,26 @@ def test_multi_tile_stream_k_bit_exact(g, config, stream_k):
     assert_exact(got, ref, f"stream_k={stream_k}")
 
 
+@pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
+@pytest.mark.parametrize("layout", ["NN", "TN"])
+def test_scale_ring_across_split_items_bit_exact(g, config, layout):
+    # Scales travel in slots of four stages, counted from each work item's first K block: K of
+    # 21 stages (a last slot of one stage) and few CTAs, so stream-K items start and end inside
+    # slots and several items pass through the two-slot ring per CTA.
+    M, N, K = 1000, 1000, 2600
+    A, B = make_inputs(M, N, K, layout, "e4m3", "int", seed=87)
+    sa, sb = scales(M, K, 2, seed=88), scales(N, K, 2, seed=89)
+    g.set_option(native.OPT_MAX_CTAS, 10)
+    try:
+        pl = g.plan(M, N, K, layout, "e4m3", "block_scaled")
+        assert pl["k_blocks"] == 21 and pl["dp_tiles"] < pl["tiles_m"] * pl["tiles_n"], pl
+        got, guard = run_mx(g, A, B, sa, sb, layout, "bf16")
+    finally:
+        g.set_option(native.OPT_MAX_CTAS, 0)
+    assert guard
+    assert_exact(got, oracle.gemm_blockscaled(A, B, sa, sb, layout, "e4m3", "bf16"), f"{layout}")
+
+
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 def test_full_size_8192_full_matrix(g, layout):
     M = N = K = 8192

@@ -163,7 +163,8 @@ SHAPES = [(1, 1, 1), (1, 8, 3), (3, 5, 7), (8, 8, 8), (17, 9, 33), (64, 64, 64),
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])
 @pytest.mark.parametrize("dtype", ["f16", "bf16"])
-@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_128x256, native.CONFIG_128x128, native.CONFIG_128x64,
+                                    native.CONFIG_256x256])
 def test_ragged_shapes(g, layout, dtype, config):
     g.set_option(native.OPT_CONFIG, config)
     try:
@@ -305,6 +306,24 @@ def test_plan_reports_pair_clusters(g):
     assert pl["tiles_m"] == 32 and pl["tiles_n"] == 32 and pl["k_blocks"] == 128
 
 
+def test_plan_of_the_narrow_tile(g):
+    # 128 x 64 on one CTA, 8-stage ring, for 16-bit dense operands; 8-bit operands take
+    # 128 x 128 (an N-major 8-bit B row is 128 wide), side-data kernels 128 x 256.
+    g.set_option(native.OPT_CONFIG, native.CONFIG_128x64)
+    try:
+        pl = g.plan(1000, 1000, 1000, "NN", "f16")
+        f8 = g.plan(1000, 1000, 1000, "NN", "e4m3")
+        mx = g.plan(1000, 1000, 1024, "TN", "e4m3", "block_scaled")
+        sp = g.plan(1000, 1000, 1000, "TN", "bf16", "sparse24")
+    finally:
+        g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
+    assert (pl["config"], pl["bm"], pl["bn"], pl["cluster"], pl["stages"]) == (native.CONFIG_128x64, 128, 64, 1, 8)
+    assert pl["tiles_m"] == 8 and pl["tiles_n"] == 16
+    assert (f8["config"], f8["bn"]) == (native.CONFIG_128x128, 128)
+    for other in (mx, sp):
+        assert (other["config"], other["bn"]) == (native.CONFIG_128x256, 256)
+
+
 def test_large_extents(g):
     # Long M (131072 rows) and long N (65536 columns) with a short K: the TMA coordinates
     # and the tile scheduler at sizes far beyond the workloads' tile counts.
@@ -417,7 +436,8 @@ def test_watchdog_timeout_is_reported_and_context_survives(g, config):
     assert_exact(got, oracle.gemm(A, B, w.layout, w.dtype), "after timeout")
 
 
-@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x128, native.CONFIG_256x256])
+@pytest.mark.parametrize("config", [native.CONFIG_AUTO, native.CONFIG_128x128, native.CONFIG_128x64,
+                                    native.CONFIG_256x256])
 def test_dependent_gemms_on_one_stream(g, config):
     # GEMM launches may be scheduled while the stream's previous kernel drains; they must still
     # read that kernel's results.  Chain on one stream, no host sync in between: a torch kernel
