@@ -12,6 +12,10 @@ inputs resident in HBM.  Prints one JSON line.  The library is a one-GPU library
 --gpus > 1, or under a launcher that starts more than one rank (WORLD_SIZE > 1), the
 benchmark refuses to run and exits with status 2.
 
+The line also carries the CPU oracle timed on a sample of whole rows of C (``cpu_baseline``)
+and the error of the GPU's result on those rows against the oracle's (``accuracy``: maximum
+absolute and relative error, bit-identical fraction, the per-element tolerance check).
+
 ``--impl reference`` times the CPU oracle (fp64 triple loop) on bounded samples of the
 same workload on the host cores: the slow reference arm, not a GPU implementation.
 """
@@ -247,27 +251,32 @@ def one_gpu_refusal(gpus: int, env=None):
 
 
 def oracle_rows_fn(A, B, w):
-    """rows -> threads used, computing those rows of C with the oracle routine of the workload."""
+    """rows -> (those rows of C as output-type codes, threads used), from the oracle routine of
+    the workload."""
     import oracle
     from dense_tiled_gemm_04_gb300.workloads import block_scales, tensor_scales
 
     threads = oracle.max_threads()
     if w.sparse:
         Ac, E, _ = oracle.sparse24_compress(A)
-        return lambda rows: (oracle.gemm_sparse24(Ac, E, B, w.layout, w.dtype, rows=rows), threads)[1]
+        return lambda rows: (oracle.gemm_sparse24(Ac, E, B, w.layout, w.dtype, rows=rows), threads)
     if w.elem_bytes == 2:
-        return lambda rows: oracle.gemm_rows(A, B, w.layout, w.dtype, rows)[2]
+        def dense(rows):
+            codes, _, used = oracle.gemm_rows(A, B, w.layout, w.dtype, rows)
+            return codes, used
+        return dense
     if w.scales == "block":
         sa, sb = block_scales(w)
         return lambda rows: (oracle.gemm_blockscaled(A, B, sa, sb, w.layout, w.dtype, w.out_dtype, rows=rows),
-                             threads)[1]
+                             threads)
     s_a, s_b = tensor_scales(w)
     return lambda rows: (oracle.gemm_typed(A, B, w.layout, w.dtype, w.out_dtype, alpha=s_a * s_b, rows=rows),
-                         threads)[1]
+                         threads)
 
 
 def oracle_rows_sample(A, B, w, target_s: float):
-    """Time the oracle on whole rows of C: calibrate on one batch, then run ~target_s."""
+    """Time the oracle on whole rows of C: calibrate on one batch, then run ~target_s.  Returns
+    (the cpu_baseline object, the rows, the oracle's codes for them)."""
     import numpy as np
 
     import oracle
@@ -277,17 +286,45 @@ def oracle_rows_sample(A, B, w, target_s: float):
     rng = np.random.default_rng(0)
     calib = rng.integers(0, w.M, threads)
     t0 = time.perf_counter()
-    used = fn(calib)
+    fn(calib)
     t_cal = time.perf_counter() - t0
     batches = max(1, int(target_s / max(t_cal, 1e-3)))
     rows = rng.integers(0, w.M, threads * batches)
     t0 = time.perf_counter()
-    used = fn(rows)
+    ref, used = fn(rows)
     dt = time.perf_counter() - t0
     flops = 2.0 * rows.size * w.N * w.K
-    return {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
-            "sample": f"{rows.size} random rows of C ({rows.size}x{w.N} outputs, K={w.K}), fp64 sums, "
-                      f"{dt:.1f} s on {used} threads"}
+    cpu = {"value": flops / dt / 1e12, "unit": "TFLOP/s", "cores": int(used), "kind": "oracle",
+           "sample": f"{rows.size} random rows of C ({rows.size}x{w.N} outputs, K={w.K}), fp64 sums, "
+                     f"{dt:.1f} s on {used} threads"}
+    return cpu, rows, ref
+
+
+# Per-element tolerance on random inputs (fp16 / bf16 output): |gpu - ref| <= atol + rtol * |ref|.
+TOLERANCE = {"f16": (1e-2, 1e-2), "bf16": (3e-2, 3e-2)}
+
+
+def accuracy_line(got_codes, ref_codes, out_dtype: str):
+    """Error of the GPU's rows of C against the oracle's (both rounded to the output type)."""
+    import numpy as np
+
+    import oracle
+
+    g = oracle.decode(np.asarray(got_codes), out_dtype)
+    r = oracle.decode(np.asarray(ref_codes), out_dtype)
+    d = np.abs(g - r)
+    atol, rtol = TOLERANCE[out_dtype]
+    big = np.abs(r) >= atol / rtol  # where the relative term of the tolerance dominates
+    ratio = d / (atol + rtol * np.abs(r))
+    finite = bool(np.isfinite(g).all())
+    return {"elements": int(g.size), "max_abs_err": float(d.max()) if finite else None,
+            "max_rel_err": float((d[big] / np.abs(r[big])).max()) if finite and big.any() else None,
+            "max_rel_err_where": f"|ref| >= {atol / rtol:g}",
+            "bit_identical_frac": float(np.mean(np.asarray(got_codes) == np.asarray(ref_codes))),
+            "worst_tolerance_ratio": float(ratio.max()) if finite else None,
+            "within_tolerance": bool(finite and (ratio <= 1.0).all()),
+            "tolerance": f"|gpu - ref| <= {atol:g} + {rtol:g} |ref| ({out_dtype} output)",
+            "reference": "the CPU oracle: fp64 sums rounded once to the output type"}
 
 
 def run_reference(args, w):
@@ -615,9 +652,13 @@ def run_ours(args, w):
                                                             None).get("frac_of_sustained")
         sustained["cycles"] = cycle_figures(w, plan, sustained["ms_per_step"], sustained["clocks"].get("sm_mhz"))
 
-    cpu = None
+    # The CPU baseline: the oracle timed on a sample of whole rows of C; the same rows of the
+    # GPU's C (the last timed step's) are then compared with them.
+    cpu = accuracy = None
     if not args.no_cpu_baseline:
-        cpu = oracle_rows_sample(A_cpu, B_cpu, w, target_s=args.cpu_seconds)
+        cpu, rows, ref = oracle_rows_sample(A_cpu, B_cpu, w, target_s=args.cpu_seconds)
+        got = C[torch.from_numpy(rows).to(dev)].cpu().contiguous().view(torch.int16).numpy().view("uint16")
+        accuracy = dict(accuracy_line(got, ref, w.out_dtype), rows=int(rows.size))
 
     g.close()
     line = {
@@ -643,6 +684,7 @@ def run_ours(args, w):
         "roofline": roofline,
         "sustained": sustained,
         "cpu_baseline": cpu,
+        "accuracy": accuracy,
         "e2e": e2e,
         "gpu_launches": args.steps,
         "clocks": clocks,

@@ -91,3 +91,35 @@ def test_cycle_figures_of_the_headline_plan():
     # One pair tile: 256 x 256 x 8192 multiply-adds over two SMs at 4096 per clock each.
     assert c["min_cycles_per_tile"] == pytest.approx(256 * 256 * 8192 / 2 / 4096)
     assert bench.cycle_figures(w, plan, 0.6, None) is None
+
+
+def test_accuracy_line_against_the_oracles_codes():
+    import numpy as np
+
+    import oracle
+
+    ref = oracle.encode(np.array([[1.0, -2.0, 0.5, 100.0]]), "bf16")
+    same = bench.accuracy_line(ref, ref, "bf16")
+    assert same["max_abs_err"] == 0.0 and same["within_tolerance"] and same["bit_identical_frac"] == 1.0
+    off = ref.copy()
+    off[0, 3] += 1  # one bf16 ulp at 100: 0.5, inside 3e-2 + 3e-2 * 100
+    one = bench.accuracy_line(off, ref, "bf16")
+    assert one["max_abs_err"] == 0.5 and one["within_tolerance"] and one["bit_identical_frac"] == 0.75
+    assert one["max_rel_err"] == 0.5 / 100.0 and one["max_rel_err_where"] == "|ref| >= 1"
+    far = oracle.encode(np.array([[1.0, -2.0, 0.5, 110.0]]), "bf16")
+    assert not bench.accuracy_line(far, ref, "bf16")["within_tolerance"]
+    nan = oracle.encode(np.array([[np.nan, -2.0, 0.5, 100.0]]), "bf16")
+    assert not bench.accuracy_line(nan, ref, "bf16")["within_tolerance"]
+
+
+def test_cpu_baseline_sample_returns_the_oracles_rows(oracle_lib):
+    import numpy as np
+
+    from dense_tiled_gemm_04_gb300.workloads import make_inputs
+    from dense_tiled_gemm_04_gb300.workloads import WORKLOADS as W
+
+    w = W["c1"]
+    A, B = make_inputs(w.M, w.N, w.K, w.layout, w.dtype, "int", seed=3)
+    cpu, rows, ref = bench.oracle_rows_sample(A, B, w, target_s=0.01)
+    assert cpu["kind"] == "oracle" and cpu["cores"] >= 1 and ref.shape == (rows.size, w.N)
+    assert np.array_equal(ref, oracle_lib.gemm(A, B, w.layout, w.dtype)[rows])
