@@ -60,7 +60,8 @@ def _code_only(text: str) -> str:
 
 
 # What a launch's DRAM traffic depends on besides the kernel's code: the launch shape.
-PLAN_KEYS = ("config", "bm", "bn", "bk", "stages", "cluster", "grid", "dp_tiles", "sk_base", "sk_extra")
+PLAN_KEYS = ("config", "bm", "bn", "bk", "stages", "cluster", "grid", "dp_tiles", "sk_base", "sk_extra",
+             "raster_group")
 HOST_SOURCE = "gemm_api.cu"  # argument checks, tensor maps, plans and the host pipeline
 
 
@@ -710,7 +711,7 @@ def main(argv=None):
     ap.add_argument("--sk-min-blocks", type=int, default=0,
                     help="shortest stream-K share in K blocks (default: the library's, 8)")
     ap.add_argument("--raster-group", type=int, default=0,
-                    help="tile rows per group of the grouped raster (default: the library's, 8)")
+                    help="tile rows per group of the grouped raster (default: the library's, min(8, tile columns))")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -33,7 +33,8 @@ class gemm_plan_t(ctypes.Structure):
                 ("bk", ctypes.c_int32), ("stages", ctypes.c_int32), ("cluster", ctypes.c_int32),
                 ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
                 ("grid", ctypes.c_int64), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
-                ("dp_tiles", ctypes.c_int64), ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64)]
+                ("dp_tiles", ctypes.c_int64), ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64),
+                ("raster_group", ctypes.c_int64)]
 
 
 class gemm_args_t(ctypes.Structure):

@@ -94,6 +94,8 @@ static void host_checks(void)
     const gemm_status_t st = gemm_create(&none, 9999);
     CHECK(st != GEMM_OK && none == NULL, "create on a missing device: %d", st);
     CHECK(gemm_destroy(NULL) == GEMM_OK, "destroy NULL");
+    /* Struct sizes as a C compiler lays them out (the Python binding checks against these). */
+    printf("sizeof gemm_plan_t %zu gemm_args_t %zu\n", sizeof(gemm_plan_t), sizeof(gemm_args_t));
 }
 
 /* Deterministic integers in {-2..2}, as 16-bit codes of the type. */

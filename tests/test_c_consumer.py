@@ -5,6 +5,7 @@ On the CPU it checks the host-side entry points; on a GB300 it also runs GEMMs o
 buffers through gemm_run_host in every configuration and compares them bit for bit with
 the CPU oracle linked into the same program.
 """
+import ctypes
 import os
 import subprocess
 
@@ -33,6 +34,11 @@ def test_c_program_host_entry_points(tmp_path):
     r = subprocess.run([exe, "host"], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stdout + r.stderr
     assert "gemm_c_consumer host: ok" in r.stdout
+    # The ctypes binding lays the ABI's structs out as the C compiler does.
+    from dense_tiled_gemm_04_gb300 import native
+
+    sizes = dict(zip(["gemm_plan_t", "gemm_args_t"], (int(x) for x in r.stdout.split("sizeof ")[1].split()[1::2])))
+    assert sizes == {"gemm_plan_t": ctypes.sizeof(native.gemm_plan_t), "gemm_args_t": ctypes.sizeof(native.gemm_args_t)}
 
 
 @pytest.mark.gpu

@@ -54,7 +54,7 @@ def with_options(g, case, fn):
     finally:
         g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
         g.set_option(native.OPT_STREAM_K, 1)
-        g.set_option(native.OPT_RASTER_GROUP, 8)
+        g.set_option(native.OPT_RASTER_GROUP, 0)
         g.set_option(native.OPT_MAX_CTAS, 0)
 
 

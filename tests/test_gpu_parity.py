@@ -261,7 +261,7 @@ def test_several_tiles_per_cta_and_raster_groups(g, config, layout):
             assert_exact(got, ref, f"cfg{config} max_ctas={max_ctas} group={group}")
     finally:
         g.set_option(native.OPT_MAX_CTAS, 0)
-        g.set_option(native.OPT_RASTER_GROUP, 16)
+        g.set_option(native.OPT_RASTER_GROUP, 0)
         g.set_option(native.OPT_CONFIG, native.CONFIG_AUTO)
 
 
@@ -304,6 +304,19 @@ def test_plan_reports_pair_clusters(g):
     assert pl["cluster"] == 2 and pl["bm"] == 256 and pl["bn"] == 256
     assert pl["grid"] % 2 == 0 and 2 <= pl["grid"] <= torch.cuda.get_device_properties(0).multi_processor_count
     assert pl["tiles_m"] == 32 and pl["tiles_n"] == 32 and pl["k_blocks"] == 128
+
+
+def test_automatic_raster_group_follows_the_grid_width(g):
+    # min(8, tile columns): 8 on the square 8192^3 grid (32 columns), 4 on the tall-skinny
+    # 16384 x 1024 x 8192 grid (4 columns); an explicit option wins.
+    assert g.plan(8192, 8192, 8192, "TN", "bf16")["raster_group"] == 8
+    assert g.plan(16384, 1024, 8192, "TN", "f16")["raster_group"] == 4
+    assert g.plan(128, 256, 192, "NN", "f16")["raster_group"] == 4  # 4 tiles of 128 x 64
+    g.set_option(native.OPT_RASTER_GROUP, 3)
+    try:
+        assert g.plan(16384, 1024, 8192, "TN", "f16")["raster_group"] == 3
+    finally:
+        g.set_option(native.OPT_RASTER_GROUP, 0)
 
 
 def test_plan_of_the_narrow_tile(g):

@@ -39,7 +39,7 @@ def _with(g, **opts):
 
 
 def _reset(g):
-    _with(g, config=native.CONFIG_AUTO, max_ctas=0, stream_k=1, group=8, min_blocks=8, split=32)
+    _with(g, config=native.CONFIG_AUTO, max_ctas=0, stream_k=1, group=0, min_blocks=8, split=32)
 
 
 CASES = [
