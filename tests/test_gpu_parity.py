@@ -306,10 +306,14 @@ def test_plan_reports_pair_clusters(g):
     assert pl["tiles_m"] == 32 and pl["tiles_n"] == 32 and pl["k_blocks"] == 128
 
 
-def test_automatic_raster_group_follows_the_grid_width(g):
-    # min(8, tile columns): 8 on the square 8192^3 grid (32 columns), 4 on the tall-skinny
-    # 16384 x 1024 x 8192 grid (4 columns); an explicit option wins.
+def test_automatic_raster_group_follows_the_a_panel_bytes(g):
+    # The tile rows whose A holds about 32 MiB, at most the tile columns: 8 rows of 256 x 8192
+    # bf16 (4 MiB each), 16 of E4M3 or of a 2:4-compressed bf16 A (2 MiB each), 4 on the
+    # 4-column tall-skinny grid; an explicit option wins.
     assert g.plan(8192, 8192, 8192, "TN", "bf16")["raster_group"] == 8
+    assert g.plan(8192, 8192, 8192, "TN", "e4m3")["raster_group"] == 16
+    assert g.plan(8192, 8192, 8192, "TN", "e4m3", "block_scaled")["raster_group"] == 16
+    assert g.plan(8192, 8192, 8192, "TN", "bf16", "sparse24")["raster_group"] == 16
     assert g.plan(16384, 1024, 8192, "TN", "f16")["raster_group"] == 4
     assert g.plan(128, 256, 192, "NN", "f16")["raster_group"] == 4  # 4 tiles of 128 x 64
     g.set_option(native.OPT_RASTER_GROUP, 3)
