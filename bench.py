@@ -541,6 +541,8 @@ def run_ours(args, w):
         g.set_option(native.OPT_SK_MIN_BLOCKS, args.sk_min_blocks)
     if args.raster_group:
         g.set_option(native.OPT_RASTER_GROUP, args.raster_group)
+    if args.k_snake >= 0:
+        g.set_option(native.OPT_K_SNAKE, args.k_snake)
 
     A_cpu, B_cpu = workload_inputs(w)
     A, B = A_cpu.to(dev), B_cpu.to(dev)
@@ -711,7 +713,9 @@ def main(argv=None):
     ap.add_argument("--sk-min-blocks", type=int, default=0,
                     help="shortest stream-K share in K blocks (default: the library's, 8)")
     ap.add_argument("--raster-group", type=int, default=0,
-                    help="tile rows per group of the grouped raster (default: the library's, min(8, tile columns))")
+                    help="tile rows per group of the grouped raster (default: the library's, about 32 MiB of A)")
+    ap.add_argument("--k-snake", type=int, choices=[0, 1], default=-1,
+                    help="1: every second work item walks its K blocks backwards (default: the library's)")
     args = ap.parse_args(argv)
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")

@@ -85,6 +85,7 @@ struct LaunchOptions {
     int64_t stream_k = 1;
     int64_t sk_min_blocks = kMinStreamKBlocks;
     int64_t split_min_blocks = kMinSplitBlocks;
+    int64_t k_snake = 1;
     int64_t host_row_chunks = 8;
     int64_t host_col_chunks = 4;
 };
@@ -487,6 +488,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
     kp.group_m = static_cast<int32_t>(plan.raster_group);
     kp.fault_inject = static_cast<int32_t>(o.fault_inject);
+    kp.k_snake = static_cast<int32_t>(o.k_snake);
     kp.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
     kp.err = err;
     kp.C = C;
@@ -1090,6 +1092,10 @@ gemm_status_t gemm_set_option(gemm_handle_t h, gemm_option_t opt, int64_t value)
         if (value < 0 || value > (1 << 20)) return GEMM_ERR_INVALID_ARG;
         o.split_min_blocks = value;
         return GEMM_OK;
+    case GEMM_OPT_K_SNAKE:
+        if (value != 0 && value != 1) return GEMM_ERR_INVALID_ARG;
+        o.k_snake = value;
+        return GEMM_OK;
     case GEMM_OPT_HOST_ROW_CHUNKS:
         if (value < 1 || value > HostPipe::kMaxRowChunks) return GEMM_ERR_INVALID_ARG;
         o.host_row_chunks = value;
@@ -1116,6 +1122,7 @@ gemm_status_t gemm_get_option(gemm_handle_t h, gemm_option_t opt, int64_t* value
     case GEMM_OPT_STREAM_K: *value = o.stream_k; return GEMM_OK;
     case GEMM_OPT_SK_MIN_BLOCKS: *value = o.sk_min_blocks; return GEMM_OK;
     case GEMM_OPT_SPLIT_MIN_BLOCKS: *value = o.split_min_blocks; return GEMM_OK;
+    case GEMM_OPT_K_SNAKE: *value = o.k_snake; return GEMM_OK;
     case GEMM_OPT_HOST_ROW_CHUNKS: *value = o.host_row_chunks; return GEMM_OK;
     case GEMM_OPT_HOST_COL_CHUNKS: *value = o.host_col_chunks; return GEMM_OK;
     default: return GEMM_ERR_INVALID_ARG;

@@ -169,6 +169,9 @@ struct KernelParams {
     const uint8_t* sfb;          // sfb_blocks x num_kb chunks
     // 2:4 sparsity metadata (sparse kernels only): ceil(M / 128) x num_kb chunks of kMetaChunkBytes
     const uint8_t* meta;
+    // 1: every second work item of a unit walks its K blocks backwards (not in block-scaled
+    // kernels), so a wave of items starts on the A and B data the previous wave touched last
+    int32_t k_snake;
 };
 
 // Linear tile index -> (tile row, tile column).  Tiles are taken in groups of group_m
@@ -199,9 +202,11 @@ __host__ __device__ __forceinline__ int64_t sk_owner(int64_t sk_base, int64_t sk
     return x < big ? x / (sk_base + 1) : sk_extra + (x - big) / sk_base;
 }
 
-// The work items of one unit, in order: (tile, first K block, end K block).
+// The work items of one unit, in order: (tile, first K block, end K block).  With k_snake,
+// every second item (the 2nd, 4th, ... of the unit) is walked from its last K block down.
 struct WorkIter {
     int64_t next_dp, step, u, u_end;
+    int64_t count = 0;  // items returned so far
 
     __device__ __forceinline__ WorkIter(const KernelParams& p, int64_t unit, int64_t units)
         : next_dp(unit), step(units), u(0), u_end(0)
@@ -219,6 +224,7 @@ struct WorkIter {
             kb0 = 0;
             kb1 = p.num_kb;
             next_dp += step;
+            ++count;
             return true;
         }
         if (u < u_end) {
@@ -228,10 +234,14 @@ struct WorkIter {
             kb1 = static_cast<int>(end < p.num_kb ? end : p.num_kb);
             tile = p.dp_tiles + tr;
             u += kb1 - kb0;
+            ++count;
             return true;
         }
         return false;
     }
+
+    // Whether the item next() returned last is walked from its last K block down.
+    __device__ __forceinline__ bool reversed(const KernelParams& p) const { return p.k_snake && (count & 1) == 0; }
 };
 
 // SF_BYTES: side-data bytes per ring stage (sparsity metadata; 0 without); SC_BYTES: bytes of
@@ -732,13 +742,15 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                     sf_b_chunks = static_cast<int>(p.sfb_blocks - nb0);
                     if (sf_b_chunks > kSfChunks - 1) sf_b_chunks = kSfChunks - 1;
                 }
-                for (int kb = kb0; kb < kb1; ++kb, ++loaded) {
+                const bool rev = !T::kMX && it.reversed(p);
+                for (int i = 0; i < kb1 - kb0; ++i, ++loaded) {
+                    const int kb = rev ? kb1 - 1 - i : kb0 + i;  // the i-th K block this item loads
                     if (!wd.wait(empty_bar(stage), phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
                     if constexpr (T::kMX) {
                         // Every kScGroup stages of an item: the scale chunks of those stages, one
                         // box of kScGroup chunks per block (A's, then B's), into the next slot of
                         // the scale ring, completing on that slot's barrier in the leader.
-                        if ((kb - kb0) % kScGroup == 0) {
+                        if (i % kScGroup == 0) {
                             if (!wd.wait(sce_bar(sc_slot), sc_phase ^ 1u, kRoleProducer, tile, kb)) goto producer_done;
                             const uint32_t sc = base + L::kScOff + sc_slot * L::kScBytes;
                             const uint32_t scb = PAIR ? ptx::mapa_shared(scf_bar(sc_slot), 0u) : scf_bar(sc_slot);
@@ -811,7 +823,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         phase ^= 1u;
                     }
                     if constexpr (T::kMX) {
-                        if ((kb - kb0) % kScGroup == kScGroup - 1 || kb == kb1 - 1) {
+                        if (i % kScGroup == kScGroup - 1 || i == kb1 - kb0 - 1) {
                             if (++sc_slot == kScSlots) {
                                 sc_slot = 0;
                                 sc_phase ^= 1u;
@@ -871,7 +883,9 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                 }
                 ptx::tc_fence_after_sync();
                 const uint32_t d_tmem = tmem_base + static_cast<uint32_t>(acc * BN);
-                for (int kb = kb0; kb < kb1; ++kb) {
+                const bool rev = !T::kMX && it.reversed(p);
+                for (int i = 0; i < kb1 - kb0; ++i) {
+                    const int kb = rev ? kb1 - 1 - i : kb0 + i;
                     // Block-scaled and sparse kernels wait for the stage's side data to be in
                     // TMEM (the side warp copies it once the stage's data is in); the others
                     // for the stage's data.
@@ -894,7 +908,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         // sparse A, 64-byte-swizzled rows with 512-byte groups.
                         const uint64_t adesc =
                             T::kSparse ? smem_desc_sw64(sa + k * 32, 16, 512) : smem_desc_sw128(sa + k * 32, 16, 1024);
-                        const uint32_t accumulate = (kb != kb0 || k != 0) ? 1u : 0u;
+                        const uint32_t accumulate = (i != 0 || k != 0) ? 1u : 0u;  // the item's first MMA overwrites
                         uint64_t bdesc;
                         if constexpr (NN) {
                             // B (N-major): rows are K; the k-th slice starts kMmaK rows of 128 B
@@ -981,8 +995,10 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
             int64_t tile;
             int kb0, kb1;
             while (!aborted && it.next(p, tile, kb0, kb1)) {
-                for (int kb = kb0; kb < kb1; ++kb) {
-                    const int pos = (kb - kb0) % kScGroup;  // stage within its scale slot
+                const bool rev = !T::kMX && it.reversed(p);
+                for (int i = 0; i < kb1 - kb0; ++i) {
+                    const int kb = rev ? kb1 - 1 - i : kb0 + i;
+                    const int pos = i % kScGroup;  // stage within its scale slot
                     if constexpr (T::kMX) {
                         if (pos == 0 && !wd.wait(scf_bar(sc_slot), sc_phase, kRoleSide, tile, kb)) {
                             aborted = true;
@@ -1038,7 +1054,7 @@ __global__ void __launch_bounds__((Operand<IN>::kMX || Operand<IN>::kSparse) ? k
                         phase ^= 1u;
                     }
                     if constexpr (T::kMX) {
-                        if (pos == kScGroup - 1 || kb == kb1 - 1) {
+                        if (pos == kScGroup - 1 || i == kb1 - kb0 - 1) {
                             // The slot's last copies issued: free it (in both CTAs of a pair, each
                             // of which refills its own) once they complete.
                             if constexpr (PAIR)

@@ -24,7 +24,7 @@ TORCH_TO_DTYPE_EX = {**TORCH_TO_DTYPE, torch.float8_e4m3fn: DTYPE_E4M3, torch.fl
 
 OK, ERR_INVALID_ARG, ERR_UNSUPPORTED, ERR_ARCH, ERR_CUDA, ERR_TIMEOUT = range(6)
 OPT_CONFIG, OPT_TIMEOUT_NS, OPT_MAX_CTAS, OPT_RASTER_GROUP, OPT_FAULT_INJECT, OPT_STREAM_K, \
-    OPT_HOST_ROW_CHUNKS, OPT_HOST_COL_CHUNKS, OPT_SK_MIN_BLOCKS, OPT_SPLIT_MIN_BLOCKS = range(10)
+    OPT_HOST_ROW_CHUNKS, OPT_HOST_COL_CHUNKS, OPT_SK_MIN_BLOCKS, OPT_SPLIT_MIN_BLOCKS, OPT_K_SNAKE = range(11)
 CONFIG_AUTO, CONFIG_128x256, CONFIG_128x128, CONFIG_256x256, CONFIG_128x64 = range(5)
 
 

@@ -92,13 +92,20 @@ enum {
                                   columns for NN), 1..8 (default 4; at least 2048 columns)   */
     GEMM_OPT_SK_MIN_BLOCKS = 8, /* shortest stream-K share of a part-empty last wave, in K
                                   blocks (default 8, >= 1)                                  */
-    GEMM_OPT_SPLIT_MIN_BLOCKS = 9 /* a problem under one wave (fewer tiles than the CTAs or
+    GEMM_OPT_SPLIT_MIN_BLOCKS = 9, /* a problem under one wave (fewer tiles than the CTAs or
                                   pairs that fit) has its K blocks split over more units only
                                   when every share holds at least this many (default 32;
                                   0 = never): the merge costs a few microseconds of dependent
                                   global-memory traffic, which only long K loops repay.  The
                                   units are then as many as shares of that length allow, if
                                   more than the tiles                                         */
+    GEMM_OPT_K_SNAKE = 10      /* 1 (default): every second work item of a CTA (or pair) walks
+                                  its K blocks from the last down, so that a wave of items
+                                  starts on the K slices the wave before read last (still in
+                                  L2): bf16 8192^3 ~1 % faster in bursts, ~2 % under the power
+                                  limit; 0: every item from the first K block up.  Block-scaled
+                                  kernels ignore it.  Changes only the order of the fp32
+                                  additions within an item (results stay deterministic)       */
 };
 
 typedef int32_t gemm_config_t;

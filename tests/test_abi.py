@@ -178,6 +178,7 @@ def test_binding_constants_match_the_header(lib):
         "GEMM_OPT_FAULT_INJECT": lib.OPT_FAULT_INJECT, "GEMM_OPT_STREAM_K": lib.OPT_STREAM_K,
         "GEMM_OPT_HOST_ROW_CHUNKS": lib.OPT_HOST_ROW_CHUNKS, "GEMM_OPT_HOST_COL_CHUNKS": lib.OPT_HOST_COL_CHUNKS,
         "GEMM_OPT_SK_MIN_BLOCKS": lib.OPT_SK_MIN_BLOCKS, "GEMM_OPT_SPLIT_MIN_BLOCKS": lib.OPT_SPLIT_MIN_BLOCKS,
+        "GEMM_OPT_K_SNAKE": lib.OPT_K_SNAKE,
         "GEMM_CONFIG_AUTO": lib.CONFIG_AUTO, "GEMM_CONFIG_128x256": lib.CONFIG_128x256,
         "GEMM_CONFIG_128x128": lib.CONFIG_128x128, "GEMM_CONFIG_256x256": lib.CONFIG_256x256,
         "GEMM_CONFIG_128x64": lib.CONFIG_128x64,

@@ -187,12 +187,14 @@ def test_k_zero_scales_c(g, out):
 
 
 @pytest.mark.parametrize("in_dtype", IN_TYPES)
-@pytest.mark.parametrize("stream_k", [0, 1])
-def test_multi_tile_stream_k_bit_exact(g, in_dtype, stream_k):
+@pytest.mark.parametrize("stream_k,k_snake", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_multi_tile_stream_k_bit_exact(g, in_dtype, stream_k, k_snake):
     # 16384 x 1024 tiles leave the last wave part-empty: stream-K shares its K blocks out.
     M, N, K = 16384, 1024, 2048
     A, B = make_inputs(M, N, K, "TN", in_dtype, "int", seed=17)
+    snake0 = g.get_option(native.OPT_K_SNAKE)
     g.set_option(native.OPT_STREAM_K, stream_k)
+    g.set_option(native.OPT_K_SNAKE, k_snake)
     try:
         plan = g.plan(M, N, K, "TN", in_dtype)
         assert plan["bk"] == 128 and plan["k_blocks"] == K // 128
@@ -204,9 +206,10 @@ def test_multi_tile_stream_k_bit_exact(g, in_dtype, stream_k):
         assert g.sync_status() == native.OK
     finally:
         g.set_option(native.OPT_STREAM_K, 1)
+        g.set_option(native.OPT_K_SNAKE, snake0)
     got = C.cpu().view(torch.int16).numpy().view(np.uint16)
     ref = oracle.gemm_typed(A, B, "TN", in_dtype, "bf16")
-    assert_exact(got, ref, f"{in_dtype} stream_k={stream_k}")
+    assert_exact(got, ref, f"{in_dtype} stream_k={stream_k} k_snake={k_snake}")
 
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])

@@ -295,6 +295,14 @@ def test_host_chunk_options_defaults_and_limits(g):
     assert g.get_option(native.OPT_HOST_ROW_CHUNKS) == 8
 
 
+def test_k_snake_option_default_and_limits(g):
+    assert g.get_option(native.OPT_K_SNAKE) == 1
+    for bad in (-1, 2):
+        with pytest.raises(native.GemmError):
+            g.set_option(native.OPT_K_SNAKE, bad)
+    assert g.get_option(native.OPT_K_SNAKE) == 1
+
+
 def test_plan_reports_pair_clusters(g):
     g.set_option(native.OPT_CONFIG, native.CONFIG_256x256)
     try:

@@ -208,20 +208,23 @@ def test_edge_shapes(g, config, shape, layout):
 
 
 @pytest.mark.parametrize("config", CONFIGS[1:], indirect=True)
-@pytest.mark.parametrize("stream_k", [0, 1])
-def test_multi_tile_stream_k_bit_exact(g, config, stream_k):
+@pytest.mark.parametrize("stream_k,k_snake", [(0, 0), (1, 0), (0, 1), (1, 1)])
+def test_multi_tile_stream_k_bit_exact(g, config, stream_k, k_snake):
     M, N, K = 16384, 1024, 2048
     A, B = make_inputs(M, N, K, "TN", "bf16", "int", seed=113)
     A = prune_24(A, seed=114)
     Ac, meta, _ = compress(g, A)
+    snake0 = g.get_option(native.OPT_K_SNAKE)
     g.set_option(native.OPT_STREAM_K, stream_k)
+    g.set_option(native.OPT_K_SNAKE, k_snake)
     try:
         C = g.run_sp(Ac, B.cuda(), meta, layout="TN")
         torch.cuda.synchronize()
         assert g.sync_status() == native.OK
     finally:
         g.set_option(native.OPT_STREAM_K, 1)
-    assert_exact(codes(C), oracle.gemm(A, B, "TN", "bf16"), f"stream_k={stream_k}")
+        g.set_option(native.OPT_K_SNAKE, snake0)
+    assert_exact(codes(C), oracle.gemm(A, B, "TN", "bf16"), f"stream_k={stream_k} k_snake={k_snake}")
 
 
 @pytest.mark.parametrize("layout", ["NN", "TN"])

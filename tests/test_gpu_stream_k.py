@@ -26,6 +26,7 @@ def g():
     build.build()
     oracle.build()
     h = native.Gemm(0)
+    h.default_k_snake = h.get_option(native.OPT_K_SNAKE)
     yield h
     h.close()
 
@@ -33,13 +34,14 @@ def g():
 def _with(g, **opts):
     names = {"config": native.OPT_CONFIG, "max_ctas": native.OPT_MAX_CTAS, "stream_k": native.OPT_STREAM_K,
              "group": native.OPT_RASTER_GROUP, "min_blocks": native.OPT_SK_MIN_BLOCKS,
-             "split": native.OPT_SPLIT_MIN_BLOCKS}
+             "split": native.OPT_SPLIT_MIN_BLOCKS, "k_snake": native.OPT_K_SNAKE}
     for k, v in opts.items():
         g.set_option(names[k], v)
 
 
 def _reset(g):
-    _with(g, config=native.CONFIG_AUTO, max_ctas=0, stream_k=1, group=0, min_blocks=8, split=32)
+    _with(g, config=native.CONFIG_AUTO, max_ctas=0, stream_k=1, group=0, min_blocks=8, split=32,
+          k_snake=g.default_k_snake)
 
 
 CASES = [
@@ -185,3 +187,45 @@ def test_worked_example_split_by_shorter_shares(g, min_blocks, grid, layout):
                 assert_close(got, ref, "f16", f"min_blocks={min_blocks} uniform")
     finally:
         _reset(g)
+
+
+@pytest.mark.parametrize("stream_k", [0, 1])
+@pytest.mark.parametrize("case", CASES)
+def test_k_snake_parity(g, case, stream_k):
+    # Every second work item of a unit walks its K blocks from the last down.  The CTA caps
+    # give each unit several whole tiles and (with stream-K) shares, so both directions run
+    # on whole tiles and on shares merged through the workspace.
+    M, N, K, layout, dtype, config, max_ctas = case
+    try:
+        _with(g, config=config, max_ctas=max_ctas, stream_k=stream_k, k_snake=1)
+        pl = g.plan(M, N, K, layout, dtype)
+        assert pl["tiles_m"] * pl["tiles_n"] > pl["grid"] // pl["cluster"]
+        for dist in ("int", "normal"):
+            bcols = N if layout == "NN" else K
+            A, B = make_inputs(M, N, K, layout, dtype, dist, seed=M + N + K + 1,
+                               lda=round_up(K, 8), ldb=round_up(bcols, 8))
+            got, buf = gpu_gemm(g, A, B, layout, dtype, extra_rows=1, ldc_pad=8)
+            assert_guard(buf, M, N)
+            ref = oracle.gemm(A, B, layout, dtype)
+            if dist == "int":
+                assert_exact(got, ref, f"{case} int, k_snake")
+            else:
+                assert_close(got, ref, dtype, f"{case} normal, k_snake")
+                again, _ = gpu_gemm(g, A, B, layout, dtype, extra_rows=1, ldc_pad=8)
+                assert np.array_equal(got, again), "k_snake result changed between runs"
+    finally:
+        _reset(g)
+
+
+@pytest.mark.parametrize("k_snake", [0, 1])
+def test_k_snake_on_the_square_workload_int(g, k_snake):
+    # The 8192^3 bf16 TN workload on its default plan (the CTA pair, 8 tile rows per group),
+    # both K orders, every element against the oracle.
+    w = WORKLOADS["c4"]
+    _, A, B, ref = workload_case("c4", "int")
+    try:
+        _with(g, k_snake=k_snake)
+        got, _ = gpu_gemm(g, A, B, w.layout, w.dtype)
+    finally:
+        _reset(g)
+    assert_exact(got, ref, f"c4 int, k_snake={k_snake}")
