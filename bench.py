@@ -713,7 +713,7 @@ def main(argv=None):
     ap.add_argument("--sk-min-blocks", type=int, default=0,
                     help="shortest stream-K share in K blocks (default: the library's, 8)")
     ap.add_argument("--raster-group", type=int, default=0,
-                    help="tile rows per group of the grouped raster (default: the library's, about 32 MiB of A)")
+                    help="tile rows per group of the grouped raster (default: the library's, about 48 MiB of A, at most 16 rows)")
     ap.add_argument("--k-snake", type=int, choices=[0, 1], default=-1,
                     help="1: every second work item walks its K blocks backwards (default: the library's)")
     args = ap.parse_args(argv)

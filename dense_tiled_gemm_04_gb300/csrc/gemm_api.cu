@@ -21,7 +21,8 @@ namespace {
 using dtg::KernelChoice;
 using dtg::KernelParams;
 
-constexpr int64_t kGroupPanelBytes = 32ll << 20;  // automatic raster group: A bytes of a group's tile rows
+constexpr int64_t kGroupPanelBytes = 48ll << 20;  // automatic raster group: A bytes of a group's tile rows
+constexpr int64_t kMaxAutoGroup = 16;             // and at most this many tile rows
 constexpr int64_t kTimeoutDefaultNs = 2000000000LL;  // 2 s per wait
 constexpr int kTmapCacheMax = 64;
 constexpr int32_t kTmapBytes = -1;  // get_tmap element type: raw bytes (side data)
@@ -293,15 +294,18 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     plan->tiles_n = cdiv(N, kc.bn);
     plan->k_blocks = cdiv(K, kc.stage_k);
     // Raster group: tile rows walked together.  Automatic: the tile rows whose A holds about
-    // kGroupPanelBytes (the group's A stays in L2 while its B columns stream), at most as many
-    // rows as the grid has tile columns.  Measured at 8192^3: bf16 (4 MiB of A per tile row)
-    // reads the least DRAM with 8 rows (1.24 GB per launch; 1.65 at 4, 1.50 at 16), E4M3 (2 MiB)
-    // runs fastest with 16 (3555 against 3506 TF/s at 8); 16384 x 1024 x 8192 fp16, 4 tile
-    // columns, with 4 (0.40 GB against 0.57 at 8 and 0.66 at 1).
+    // kGroupPanelBytes (the group's A stays in L2 while its B columns stream), at most
+    // kMaxAutoGroup and at most as many rows as the grid has tile columns.  Measured at 8192^3
+    // with every second item's K loop walked backwards: bf16 (4 MiB of A per tile row) runs
+    // fastest with 12 rows (1926 TF/s burst, 1657 sustained, against 1917 / 1645 at 8, 1918 /
+    // 1651 at 16, 1861 / 1600 at 4); a 2:4-compressed A (2 MiB) with 12-16 (2300 against 2289
+    // at 8); E4M3 (2 MiB, forward K loops) with 16 (3555 against 3506 at 8, 3538 at 12);
+    // 16384 x 1024 x 8192 fp16, 4 tile columns, with 4 (0.40 GB of DRAM per launch against
+    // 0.57 at 8 and 0.66 at 1).
     const int64_t a_row_bytes = K * 128 / kc.stage_k * kc.a_stage_k / kc.stage_k;  // per matrix row (2:4: compressed)
     const int64_t panel = kc.bm * (a_row_bytes > 0 ? a_row_bytes : 1);
-    const int64_t group = std::max<int64_t>(1, (kGroupPanelBytes + panel / 2) / panel);
-    plan->raster_group = o.raster_group > 0 ? o.raster_group : std::min<int64_t>(std::min<int64_t>(group, plan->tiles_n), 1 << 20);
+    const int64_t group = std::min<int64_t>(std::max<int64_t>(1, (kGroupPanelBytes + panel / 2) / panel), kMaxAutoGroup);
+    plan->raster_group = o.raster_group > 0 ? o.raster_group : std::min<int64_t>(group, plan->tiles_n);
     const int64_t tiles = plan->tiles_m * plan->tiles_n;
     // Clusters (CTA pairs, or single CTAs) that can run at once, capped by the option.
     int64_t units = kc.cluster > 1 ? (max_clusters > 0 ? max_clusters : dev.num_sms / kc.cluster)

@@ -73,9 +73,10 @@ enum {
     GEMM_OPT_MAX_CTAS = 2,     /* cap on persistent CTAs (0 = one per SM); tests use it to
                                   make each CTA walk several tiles                            */
     GEMM_OPT_RASTER_GROUP = 3, /* output-tile raster: M tiles per group (L2 reuse), >= 1; 0 (the
-                                  default) = the tile rows whose A holds about 32 MiB, at most
-                                  the tile columns (8192^3 bf16: 8; E4M3: 16; 16384 x 1024 x
-                                  8192 fp16: 4); gemm_query_plan reports the value used       */
+                                  default) = the tile rows whose A holds about 48 MiB, at most
+                                  16 and at most the tile columns (8192^3 bf16: 12; E4M3: 16;
+                                  16384 x 1024 x 8192 fp16: 4); gemm_query_plan reports the
+                                  value used                                                  */
     GEMM_OPT_FAULT_INJECT = 4, /* test hook: 1 = the first work unit (a CTA, or both CTAs of a
                                   pair) loads one ring stage nowhere and leaves it unarmed, so
                                   a consumer wait runs out and the watchdog path returns

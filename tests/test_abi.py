@@ -187,3 +187,14 @@ def test_binding_constants_match_the_header(lib):
     }
     assert set(pairs) <= set(values), sorted(set(pairs) - set(values))
     assert {k: values[k] for k in pairs} == pairs
+
+
+def test_package_exports_every_option_and_configuration():
+    import dense_tiled_gemm_04_gb300 as pkg
+
+    values = header_enum_values()
+    for name, value in values.items():
+        if name.startswith(("GEMM_OPT_", "GEMM_CONFIG_")):
+            short = name[len("GEMM_"):]
+            assert short in pkg.__all__, f"{short} missing from the package's exports"
+            assert getattr(pkg, short) == value

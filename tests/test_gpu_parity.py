@@ -315,10 +315,11 @@ def test_plan_reports_pair_clusters(g):
 
 
 def test_automatic_raster_group_follows_the_a_panel_bytes(g):
-    # The tile rows whose A holds about 32 MiB, at most the tile columns: 8 rows of 256 x 8192
-    # bf16 (4 MiB each), 16 of E4M3 or of a 2:4-compressed bf16 A (2 MiB each), 4 on the
-    # 4-column tall-skinny grid; an explicit option wins.
-    assert g.plan(8192, 8192, 8192, "TN", "bf16")["raster_group"] == 8
+    # The tile rows whose A holds about 48 MiB, at most 16 and at most the tile columns: 12 rows
+    # of 256 x 8192 bf16 (4 MiB each), 16 of E4M3 or of a 2:4-compressed bf16 A (2 MiB each,
+    # 24 capped), 4 on the 4-column tall-skinny grid; an explicit option wins.
+    assert g.plan(8192, 8192, 8192, "TN", "bf16")["raster_group"] == 12
+    assert g.plan(4096, 4096, 4096, "NN", "f16")["raster_group"] == 16
     assert g.plan(8192, 8192, 8192, "TN", "e4m3")["raster_group"] == 16
     assert g.plan(8192, 8192, 8192, "TN", "e4m3", "block_scaled")["raster_group"] == 16
     assert g.plan(8192, 8192, 8192, "TN", "bf16", "sparse24")["raster_group"] == 16

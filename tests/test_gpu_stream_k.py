@@ -219,7 +219,7 @@ def test_k_snake_parity(g, case, stream_k):
 
 @pytest.mark.parametrize("k_snake", [0, 1])
 def test_k_snake_on_the_square_workload_int(g, k_snake):
-    # The 8192^3 bf16 TN workload on its default plan (the CTA pair, 8 tile rows per group),
+    # The 8192^3 bf16 TN workload on its default plan (the CTA pair, 12 tile rows per group),
     # both K orders, every element against the oracle.
     w = WORKLOADS["c4"]
     _, A, B, ref = workload_case("c4", "int")
