@@ -1,9 +1,9 @@
 """Seeded random sweep of shapes and launch options against the oracle (GPU).
 
 Each case draws M, N, K (log-uniform, ragged), the layout, the 16-bit type, the kernel
-configuration, stream-K on or off, the raster group and a cap on the number of CTAs, then
-runs integer-valued inputs through the C ABI and compares with the oracle bit for bit, with
-sentinel guard rows and columns around C.  The epilogue sweep adds alpha, beta and a
+configuration, stream-K on or off, the raster group, the K order of every second work item
+and a cap on the number of CTAs, then runs integer-valued inputs through the C ABI and
+compares with the oracle bit for bit, with sentinel guard rows and columns around C.  The epilogue sweep adds alpha, beta and a
 column-major C.  The seed is fixed, so a failure reproduces.
 """
 import numpy as np
@@ -41,7 +41,7 @@ def draw_case(rng):
     return dict(M=dim(1100), N=dim(1100), K=dim(700), layout=str(rng.choice(["NN", "TN"])),
                 dtype=str(rng.choice(["f16", "bf16"])), config=int(rng.choice(CONFIGS)),
                 stream_k=int(rng.integers(0, 2)), group=int(rng.choice([1, 2, 8, 64])),
-                max_ctas=int(rng.choice([0, 0, 7, 40])))
+                max_ctas=int(rng.choice([0, 0, 7, 40])), k_snake=int(rng.integers(0, 2)))
 
 
 def with_options(g, case, fn):
@@ -49,6 +49,7 @@ def with_options(g, case, fn):
     g.set_option(native.OPT_STREAM_K, case["stream_k"])
     g.set_option(native.OPT_RASTER_GROUP, case["group"])
     g.set_option(native.OPT_MAX_CTAS, case["max_ctas"])
+    g.set_option(native.OPT_K_SNAKE, case["k_snake"])
     try:
         return fn()
     finally:
@@ -56,6 +57,7 @@ def with_options(g, case, fn):
         g.set_option(native.OPT_STREAM_K, 1)
         g.set_option(native.OPT_RASTER_GROUP, 0)
         g.set_option(native.OPT_MAX_CTAS, 0)
+        g.set_option(native.OPT_K_SNAKE, 1)
 
 
 @pytest.mark.parametrize("chunk", range(4))
