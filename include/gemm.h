@@ -323,7 +323,7 @@ gemm_status_t gemm_tile_coord(int64_t tile, int64_t tiles_m, int64_t tiles_n, in
 
 /* C = A·B without a handle and without allocating any device memory.
  *
- * The paper has no counterpart to this entry point; it exists for callers that cannot
+ * None of the source pages has a counterpart to this entry point; it exists for callers that cannot
  * call cudaMalloc: plug-ins running inside an engine that owns every byte of device
  * memory through its own pool, latency-critical paths that cannot afford the implicit device-wide
  * synchronisation an allocation may cause, or a process already at its memory limit.
