@@ -61,7 +61,7 @@ def _code_only(text: str) -> str:
 
 # What a launch's DRAM traffic depends on besides the kernel's code: the launch shape.
 PLAN_KEYS = ("config", "bm", "bn", "bk", "stages", "cluster", "grid", "dp_tiles", "sk_base", "sk_extra",
-             "raster_group")
+             "raster_group", "k_snake")
 HOST_SOURCE = "gemm_api.cu"  # argument checks, tensor maps, plans and the host pipeline
 
 

@@ -281,7 +281,7 @@ int64_t sk_counter_count(int64_t sk_tiles, const KernelChoice& kc) { return sk_t
 
 // `ws` == nullptr: no workspace, every tile is done whole (data-parallel).
 void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters, const Workspace* ws, int64_t M,
-               int64_t N, int64_t K, const KernelChoice& kc, gemm_plan_t* plan)
+               int64_t N, int64_t K, const KernelChoice& kc, int family, gemm_plan_t* plan)
 {
     std::memset(plan, 0, sizeof(*plan));
     plan->config = kc.config;
@@ -306,6 +306,9 @@ void fill_plan(const LaunchOptions& o, const DeviceState& dev, int max_clusters,
     const int64_t panel = kc.bm * (a_row_bytes > 0 ? a_row_bytes : 1);
     const int64_t group = std::min<int64_t>(std::max<int64_t>(1, (kGroupPanelBytes + panel / 2) / panel), kMaxAutoGroup);
     plan->raster_group = o.raster_group > 0 ? o.raster_group : std::min<int64_t>(group, plan->tiles_n);
+    // Block-scaled kernels walk every item's K blocks forward: each scale box covers the four
+    // K blocks from the one a slot starts at.
+    plan->k_snake = (o.k_snake && family != kBlockScaled) ? 1 : 0;
     const int64_t tiles = plan->tiles_m * plan->tiles_n;
     // Clusters (CTA pairs, or single CTAs) that can run at once, capped by the option.
     int64_t units = kc.cluster > 1 ? (max_clusters > 0 ? max_clusters : dev.num_sms / kc.cluster)
@@ -455,7 +458,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     const gemm_status_t ready = ensure_kernel_ready(dev, kc, slot);
     if (ready != GEMM_OK) return ready;
     gemm_plan_t plan;
-    fill_plan(o, dev, dev.max_clusters[slot], ws, M, N, K, kc, &plan);
+    fill_plan(o, dev, dev.max_clusters[slot], ws, M, N, K, kc, family, &plan);
 
     CUtensorMap tA, tB, tC;
     const bool nn = layout == GEMM_LAYOUT_NN;
@@ -492,7 +495,7 @@ gemm_status_t launch_gemm(const LaunchOptions& o, DeviceState& dev, const Worksp
     kp.num_tiles = static_cast<int32_t>(plan.tiles_m * plan.tiles_n);
     kp.group_m = static_cast<int32_t>(plan.raster_group);
     kp.fault_inject = static_cast<int32_t>(o.fault_inject);
-    kp.k_snake = static_cast<int32_t>(o.k_snake);
+    kp.k_snake = static_cast<int32_t>(plan.k_snake);
     kp.timeout_ns = static_cast<uint64_t>(o.timeout_ns);
     kp.err = err;
     kp.C = C;
@@ -1153,7 +1156,7 @@ gemm_status_t gemm_query_plan_kind(gemm_handle_t h, int64_t M, int64_t N, int64_
     const int slot = slot_of(config, dtype, out, layout, family);
     const gemm_status_t ready = ensure_kernel_ready(h->dev, kc, slot);
     if (ready != GEMM_OK) return ready;
-    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], &h->ws, M, N, K, kc, plan);
+    fill_plan(h->opts, h->dev, h->dev.max_clusters[slot], &h->ws, M, N, K, kc, family, plan);
     return GEMM_OK;
 }
 

@@ -13,6 +13,7 @@ import torch
 
 from . import build as _build
 
+API_VERSION = 3  # GEMM_API_VERSION the structures below are laid out for
 LAYOUT_NN, LAYOUT_TN = 0, 1
 DTYPE_F16, DTYPE_BF16, DTYPE_E4M3, DTYPE_E5M2 = 0, 1, 2, 3
 LAYOUTS = {"NN": LAYOUT_NN, "TN": LAYOUT_TN}
@@ -34,7 +35,7 @@ class gemm_plan_t(ctypes.Structure):
                 ("tiles_m", ctypes.c_int64), ("tiles_n", ctypes.c_int64), ("k_blocks", ctypes.c_int64),
                 ("grid", ctypes.c_int64), ("threads", ctypes.c_int32), ("smem_bytes", ctypes.c_int32),
                 ("dp_tiles", ctypes.c_int64), ("sk_base", ctypes.c_int64), ("sk_extra", ctypes.c_int64),
-                ("raster_group", ctypes.c_int64)]
+                ("raster_group", ctypes.c_int64), ("k_snake", ctypes.c_int64)]
 
 
 class gemm_args_t(ctypes.Structure):
@@ -96,6 +97,9 @@ def load() -> ctypes.CDLL:
         f = getattr(lib, name)
         f.argtypes = args
         f.restype = res
+    if lib.gemm_api_version() != API_VERSION:
+        raise ImportError(f"{_build.LIB} implements API version {lib.gemm_api_version()}, this binding "
+                          f"version {API_VERSION}: rebuild it with dense_tiled_gemm_04_gb300.build.build()")
     _lib = lib
     return lib
 

@@ -42,7 +42,7 @@
 extern "C" {
 #endif
 
-#define GEMM_API_VERSION 2
+#define GEMM_API_VERSION 3
 
 typedef struct gemm_handle_s* gemm_handle_t;
 
@@ -134,6 +134,8 @@ typedef struct {
     int64_t sk_base;    /* stream-K K blocks per work unit (the first sk_extra units: +1)    */
     int64_t sk_extra;
     int64_t raster_group; /* tile rows per group of the raster order the launch uses        */
+    int64_t k_snake;      /* 1: every second work item walks its K blocks from the last down
+                             (GEMM_OPT_K_SNAKE; always 0 for block-scaled operands)         */
 } gemm_plan_t;
 
 /* Create a handle bound to CUDA device `device`.  Checks that the device is sm_103,

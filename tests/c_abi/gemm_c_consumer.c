@@ -169,7 +169,7 @@ static void gpu_checks(void)
     CHECK(gemm_set_option(h, GEMM_OPT_CONFIG, GEMM_CONFIG_AUTO) == GEMM_OK, "reset config");
     gemm_plan_t plan;
     CHECK(gemm_query_plan(h, 8192, 8192, 8192, GEMM_LAYOUT_TN, GEMM_DTYPE_BF16, &plan) == GEMM_OK &&
-              plan.cluster == 2 && plan.bm == 256 && plan.bn == 256,
+              plan.cluster == 2 && plan.bm == 256 && plan.bn == 256 && plan.raster_group == 12 && plan.k_snake == 1,
           "plan of the square 8192^3 problem");
     CHECK(gemm_destroy(h) == GEMM_OK, "destroy");
 }

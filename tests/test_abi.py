@@ -38,7 +38,7 @@ def test_every_declared_symbol_is_exported(lib):
 
 def test_status_strings_and_version(lib):
     so = lib.load()
-    assert so.gemm_api_version() == 2
+    assert so.gemm_api_version() == 3 == lib.API_VERSION
     for s in range(6):
         assert lib.status_string(s).startswith("GEMM_")
     assert "unknown" in lib.status_string(99)

@@ -47,7 +47,7 @@ def test_flush_policy_follows_the_inputs_size():
 
 PLAN = {"config": 3, "bm": 256, "bn": 256, "bk": 64, "stages": 6, "cluster": 2, "tiles_m": 32, "tiles_n": 32,
         "k_blocks": 128, "grid": 152, "threads": 192, "smem_bytes": 200000, "dp_tiles": 988, "sk_base": 60,
-        "sk_extra": 48, "raster_group": 8}
+        "sk_extra": 48, "raster_group": 8, "k_snake": 1}
 
 
 def test_stored_traffic_needs_the_same_kernel_code_and_launch_shape(tmp_path):
@@ -60,6 +60,8 @@ def test_stored_traffic_needs_the_same_kernel_code_and_launch_shape(tmp_path):
     assert bench.load_traffic("c4", PLAN, str(path)) == 123
     assert bench.load_traffic("c3", PLAN, str(path)) is None
     assert bench.load_traffic("c4", dict(PLAN, grid=148), str(path)) is None
+    assert bench.load_traffic("c4", dict(PLAN, raster_group=12), str(path)) is None
+    assert bench.load_traffic("c4", dict(PLAN, k_snake=0), str(path)) is None
     path.write_text(json.dumps({"c4": dict(entry, kernel_sha="0" * 16)}))
     assert bench.load_traffic("c4", PLAN, str(path)) is None
 

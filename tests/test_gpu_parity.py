@@ -295,12 +295,22 @@ def test_host_chunk_options_defaults_and_limits(g):
     assert g.get_option(native.OPT_HOST_ROW_CHUNKS) == 8
 
 
-def test_k_snake_option_default_and_limits(g):
+def test_k_snake_option_default_limits_and_plan(g):
     assert g.get_option(native.OPT_K_SNAKE) == 1
     for bad in (-1, 2):
         with pytest.raises(native.GemmError):
             g.set_option(native.OPT_K_SNAKE, bad)
     assert g.get_option(native.OPT_K_SNAKE) == 1
+    # The plan reports the K order the launch uses: block-scaled kernels always walk forward.
+    assert g.plan(8192, 8192, 8192, "TN", "bf16")["k_snake"] == 1
+    assert g.plan(8192, 8192, 8192, "TN", "e4m3")["k_snake"] == 1
+    assert g.plan(8192, 8192, 8192, "TN", "bf16", "sparse24")["k_snake"] == 1
+    assert g.plan(8192, 8192, 8192, "TN", "e4m3", "block_scaled")["k_snake"] == 0
+    g.set_option(native.OPT_K_SNAKE, 0)
+    try:
+        assert g.plan(8192, 8192, 8192, "TN", "bf16")["k_snake"] == 0
+    finally:
+        g.set_option(native.OPT_K_SNAKE, 1)
 
 
 def test_plan_reports_pair_clusters(g):
